@@ -1,0 +1,268 @@
+/*
+ * pagedkv.h — C ABI of the GB300 (sm_103a) paged KV-cache decode library.
+ *
+ * What the library computes comes from four web pages on vLLM's PagedAttention:
+ *   [HowVLLM]   "How vLLM gets real throughput on H100s: PagedAttention and
+ *               continuous batching explained"
+ *   [DeepDive]  "High-Throughput LLM Inference & Training: A Deep Dive into vLLM"
+ *               (single paragraph; Figures 1 and 2; the KV-footprint equation)
+ *   [ArchBench] "vLLM architecture, memory and benchmarks deep dive"
+ *   [Dissect]   "Dissecting vLLM: How PagedAttention and Continuous Batching
+ *               Maximize Throughput"
+ *
+ * The KV cache of every layer is a pool of fixed-size physical blocks of
+ * B = 16 or 32 tokens ([HowVLLM] "PagedAttention borrows from operating
+ * systems"; [ArchBench] "PagedAttention: a 1960s idea for modern GPUs"). Each
+ * sequence owns a block table: logical block i of the sequence lives in
+ * physical block block_tables[s][i]. The decode kernel walks that table and
+ * gathers K/V from the scattered blocks ([Dissect] "PagedAttention: Virtual
+ * Memory for KV Cache", last paragraph).
+ *
+ * Cache layout (the pages only say that the kernel assumes one fixed layout,
+ * [Dissect] "A Balanced Take: The Sharp Edges"; this is the one used here):
+ *   k_cache, v_cache : [num_blocks][num_kv_heads][block_size][head_dim],
+ *                      row-major; element type bf16 (2 bytes) or OCP FP8 E4M3
+ *                      (1 byte). One (block, head) page is one contiguous run
+ *                      of block_size*head_dim elements.
+ *   q, out           : [num_seqs][num_heads][head_dim] bf16.
+ *                      Query head j reads KV head j / (num_heads/num_kv_heads).
+ *   block_tables     : int32 [num_seqs][max_blocks_per_seq]; entries past
+ *                      ceil(context_len/block_size) are never read.
+ *   context_lens     : int32 [num_seqs], number of cached tokens to attend to
+ *                      (the token written this step included).
+ *   slot_mapping     : int64 [num_tokens], slot = block*block_size + offset;
+ *                      -1 means "skip this token".
+ *
+ * Conventions shared by every entry point:
+ *   - Pointers named as "device" must point to device memory (any allocator);
+ *     the library never allocates or frees device memory and never keeps a
+ *     pointer after the call returns.
+ *   - Device buffers must be 16-byte aligned (q, out, k, v, caches, workspace);
+ *     a misaligned pointer returns PKV_ERR_INVALID_ARG.
+ *   - Every launch is asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *     default stream). PKV_OK means "validated and enqueued". A launch failure
+ *     returns PKV_ERR_CUDA. Faults inside a kernel surface at the caller's
+ *     next synchronisation.
+ *   - Kernels check every block id and slot they dereference. An out-of-range
+ *     id is skipped (the affected output is unspecified) and, if a device
+ *     error word was registered with pkv_set_device_check, an error code is
+ *     written there. Every wait inside a kernel is bounded; a wait that runs
+ *     out also sets the error word and the kernel returns normally.
+ *   - No function throws, prints or aborts. Functions are re-entrant except the
+ *     allocator, whose handle must have one owner at a time.
+ */
+#ifndef PAGEDKV_H_
+#define PAGEDKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  PKV_OK = 0,
+  PKV_ERR_INVALID_ARG = -1,   /* null/misaligned pointer, bad size or shape   */
+  PKV_ERR_UNSUPPORTED = -2,   /* shape outside the supported set (see below)  */
+  PKV_ERR_CUDA = -3,          /* a CUDA runtime call failed                   */
+  PKV_ERR_OUT_OF_BLOCKS = -4, /* allocator: free pool exhausted (state kept)  */
+  PKV_ERR_NOT_FOUND = -5,     /* allocator: unknown sequence id               */
+  PKV_ERR_DEVICE_CHECK = -6   /* a kernel reported a bad id or a timed-out wait */
+} pkv_status;
+
+typedef enum { PKV_DTYPE_BF16 = 0, PKV_DTYPE_FP8_E4M3 = 1 } pkv_dtype;
+
+/* Device error codes written into the registered error word (first error wins). */
+#define PKV_DEVERR_NONE 0
+#define PKV_DEVERR_BLOCK_ID 1    /* block table entry outside [0, num_blocks) */
+#define PKV_DEVERR_SLOT 2        /* slot_mapping entry outside the pool       */
+#define PKV_DEVERR_WAIT_TIMEOUT 3 /* a bounded barrier wait gave up           */
+#define PKV_DEVERR_CONTEXT 4     /* context_len > max_blocks_per_seq*block_size */
+
+/* Geometry of one layer's K and V pools (both share it). */
+typedef struct {
+  int num_blocks;   /* physical blocks in the pool                     */
+  int block_size;   /* tokens per block: 16 or 32                      */
+  int num_kv_heads; /* KV heads                                        */
+  int head_dim;     /* 128 or 256                                      */
+  int dtype;        /* pkv_dtype                                       */
+} pkv_cache_desc;
+
+/* Supported shapes: head_dim in {128, 256}; block_size in {16, 32};
+ * num_heads / num_kv_heads (the GQA group) in [1, 8]; Q and out bf16. */
+
+/* ------------------------------------------------------------------------ *
+ * kv_cache_write: store this step's new K/V into their slots.
+ *
+ * Blocks are filled only as tokens are produced ([HowVLLM] "PagedAttention
+ * borrows from operating systems"; [ArchBench] "PagedAttention: a 1960s
+ * idea for modern GPUs"), so every decode step scatters one K and one V row
+ * per sequence into the slot the allocator handed out.
+ *
+ *   k, v         : device bf16 [num_tokens][num_kv_heads][head_dim]
+ *   slot_mapping : device int64 [num_tokens]; -1 skips the token
+ *   k_cache, v_cache : device pools described by `cache`
+ *   k_scale, v_scale : device fp32 [num_kv_heads], FP8 pools only (else NULL).
+ *     FP8 code = round-to-nearest-even, saturating to +-448, of the fp32
+ *     quotient x / scale[h] (IEEE division), OCP E4M3.
+ * For bf16 pools the copy is bit-exact.
+ * Errors: PKV_ERR_INVALID_ARG (null pointers, num_tokens < 0, misaligned),
+ * PKV_ERR_UNSUPPORTED (shape), PKV_ERR_CUDA. num_tokens == 0 is a no-op.
+ * ------------------------------------------------------------------------ */
+int pkv_kv_cache_write(const void* k, const void* v, const int64_t* slot_mapping,
+                       int num_tokens, void* k_cache, void* v_cache,
+                       pkv_cache_desc cache, const float* k_scale,
+                       const float* v_scale, void* stream);
+
+/* ------------------------------------------------------------------------ *
+ * paged_attention_decode: one query token per sequence, grouped-query
+ * attention over the paged cache ([Dissect] "PagedAttention: Virtual Memory
+ * for KV Cache"; decode as the bandwidth-bound phase: [HowVLLM] "Decode is a
+ * memory problem, not a math problem").
+ *
+ * For sequence s and query head j (KV head h = j / g, g = num_heads /
+ * num_kv_heads), with K_s, V_s the sequence's logical rows 0..ctx-1:
+ *     z_t = scale * <q[s,j,:], K_s[t,:]>,  out[s,j,:] = sum_t softmax(z)_t V_s[t,:]
+ * FP8 pools dequantise as code * k_scale[h] (resp. v_scale[h]).
+ * The softmax is the max-subtracted one, accumulated online in fp32.
+ *
+ *   out       : device bf16 [num_seqs][num_heads][head_dim] (written when
+ *               partition_size == 0; untouched otherwise)
+ *   q         : device bf16 [num_seqs][num_heads][head_dim]
+ *   block_tables : device int32 [num_seqs][max_blocks_per_seq]
+ *   context_lens : device int32 [num_seqs]; a context of 0 yields zeros
+ *   max_context  : host upper bound of context_lens (sizes the grid)
+ *   scale        : logit scale, normally 1/sqrt(head_dim)
+ *   partition_size : 0 = one pass over the whole context, the result goes to
+ *               `out`. Otherwise a multiple of block_size: the context is cut
+ *               into partitions [p*P, (p+1)*P) starting at token 0, and each
+ *               partition's (max, sum, normalised output) is written to
+ *               `workspace`; pkv_paged_attention_reduce then merges them.
+ *   workspace, workspace_bytes : device scratch for the split form, at least
+ *               pkv_decode_workspace_bytes(...) bytes (ignored when
+ *               partition_size == 0; may be NULL then).
+ * Errors: PKV_ERR_INVALID_ARG, PKV_ERR_UNSUPPORTED, PKV_ERR_CUDA.
+ * ------------------------------------------------------------------------ */
+size_t pkv_decode_workspace_bytes(int num_seqs, int num_heads, int head_dim,
+                                  int max_context, int partition_size);
+
+int pkv_paged_attention_decode(void* out, const void* q, const void* k_cache,
+                               const void* v_cache, pkv_cache_desc cache,
+                               const float* k_scale, const float* v_scale,
+                               const int32_t* block_tables, int max_blocks_per_seq,
+                               const int32_t* context_lens, int num_seqs,
+                               int num_heads, int max_context, float scale,
+                               int partition_size, void* workspace,
+                               size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------ *
+ * paged_attention_reduce: merge the per-partition partials of a split decode.
+ * With m_p, l_p the partition's running max and exp-sum and o_p its
+ * normalised output, M = max_p m_p, w_p = l_p * exp(m_p - M):
+ *     out = sum_p (w_p / sum_q w_q) * o_p          over p < ceil(ctx / P).
+ * One partition reproduces o_0 exactly. The split form is not described on
+ * the pages; it is the log-sum-exp merge that makes the split result equal
+ * to the one-pass softmax.
+ *
+ *   out       : device bf16 [num_seqs][num_heads][head_dim]
+ *   workspace : the same buffer the split decode wrote
+ *   other args: as passed to the split decode
+ * Errors: PKV_ERR_INVALID_ARG, PKV_ERR_UNSUPPORTED, PKV_ERR_CUDA.
+ * ------------------------------------------------------------------------ */
+int pkv_paged_attention_reduce(void* out, const void* workspace,
+                               size_t workspace_bytes,
+                               const int32_t* context_lens, int num_seqs,
+                               int num_heads, int head_dim, int max_context,
+                               int partition_size, void* stream);
+
+/* ------------------------------------------------------------------------ *
+ * copy_blocks: copy-on-write duplication. Sequences forked from one prompt
+ * share its physical blocks; a block is cloned only when a sibling is about
+ * to write into it ([HowVLLM] "PagedAttention borrows from operating
+ * systems"; [ArchBench] "PagedAttention: a 1960s idea for modern GPUs";
+ * [Dissect] "PagedAttention: Virtual Memory for KV Cache").
+ * For every pair (src, dst): k_cache[dst] = k_cache[src] and
+ * v_cache[dst] = v_cache[src], all heads, byte for byte.
+ *
+ *   block_pairs : device int32 [num_pairs][2] = {src, dst}
+ * Destinations must be distinct and must not appear as a source of another
+ * pair in the same call (the allocator guarantees this).
+ * Errors: PKV_ERR_INVALID_ARG, PKV_ERR_UNSUPPORTED, PKV_ERR_CUDA.
+ * num_pairs == 0 is a no-op.
+ * ------------------------------------------------------------------------ */
+int pkv_copy_blocks(void* k_cache, void* v_cache, pkv_cache_desc cache,
+                    const int32_t* block_pairs, int num_pairs, void* stream);
+
+/* Register a device int32 that kernels write a PKV_DEVERR_* code into (first
+ * error wins; the caller clears it). NULL switches reporting off; the kernels
+ * still skip out-of-range ids. Process-wide; returns PKV_OK. */
+int pkv_set_device_check(int* dev_error_flag);
+
+/* Static description of a status code. Never NULL. */
+const char* pkv_status_string(int status);
+
+/* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
+int pkv_version(void);
+
+/* ------------------------------------------------------------------------ *
+ * Host block allocator ([HowVLLM] "PagedAttention borrows from operating
+ * systems" and "Continuous batching removes straggler bubbles"; [ArchBench]
+ * "PagedAttention: a 1960s idea for modern GPUs"; [Dissect] "PagedAttention:
+ * Virtual Memory for KV Cache"; [DeepDive] Figures 1 and 2).
+ *
+ * - Free list: at creation the pool's block ids are shuffled with a seeded
+ *   Fisher-Yates (std::mt19937_64); blocks are popped from and pushed back to
+ *   the same end (last freed, first reused).
+ * - A sequence holds exactly ceil(len / block_size) blocks: a block is taken
+ *   only when the previous one is full.
+ * - fork gives the child the parent's table and adds one reference to each
+ *   block; no device work happens.
+ * - append of a token into a block whose reference count is > 1 takes a fresh
+ *   block, emits the pair (old, new) for pkv_copy_blocks and drops one
+ *   reference from the old block (copy-on-write). A holder that finds the
+ *   count at 1 writes in place.
+ * - free drops one reference from each block; blocks that reach 0 go back to
+ *   the free list.
+ * All calls are O(blocks touched). A failing call leaves the state unchanged.
+ * The handle is not thread-safe.
+ * ------------------------------------------------------------------------ */
+typedef struct pkv_allocator pkv_allocator;
+
+int pkv_alloc_create(int num_blocks, int block_size, uint64_t seed,
+                     pkv_allocator** out);
+void pkv_alloc_destroy(pkv_allocator* a);
+/* New empty sequence; its id is written to *seq_id. */
+int pkv_seq_new(pkv_allocator* a, int* seq_id);
+/* New sequence sharing every block of `parent`. */
+int pkv_seq_fork(pkv_allocator* a, int parent, int* child);
+/* Reserve n_tokens new slots at the end of `seq`.
+ *   slots_out     : host int64 [n_tokens], the slot of each new token
+ *   cow_pairs_out : host int32 [n_tokens][2] (may be NULL if the caller knows
+ *                   no block is shared); receives the (src, dst) pairs
+ *   n_cow         : number of pairs written (NULL allowed when cow_pairs_out
+ *                   is NULL)
+ * PKV_ERR_OUT_OF_BLOCKS if the pool cannot hold the new tokens (nothing is
+ * changed); PKV_ERR_INVALID_ARG if a shared block must be cloned but
+ * cow_pairs_out is NULL. */
+int pkv_seq_append(pkv_allocator* a, int seq, int n_tokens, int64_t* slots_out,
+                   int32_t* cow_pairs_out, int* n_cow);
+/* Release the sequence and its references. */
+int pkv_seq_free(pkv_allocator* a, int seq);
+/* Copy the sequence's block table into out[0..cap); *n_blocks = its length.
+ * Returns PKV_ERR_INVALID_ARG if cap is too small (nothing written). */
+int pkv_seq_block_table(const pkv_allocator* a, int seq, int32_t* out, int cap,
+                        int* n_blocks);
+int pkv_seq_len(const pkv_allocator* a, int seq, int* len);
+/* Reference count of one physical block (0 = free). */
+int pkv_block_refcount(const pkv_allocator* a, int block, int* refcount);
+/* free_blocks + used_blocks == num_blocks; used_slots = sum of live lengths
+ * counted once per physical slot (shared slots count once). */
+int pkv_alloc_stats(const pkv_allocator* a, int* free_blocks, int* used_blocks,
+                    long long* used_slots);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDKV_H_ */
