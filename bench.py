@@ -1,0 +1,450 @@
+"""Benchmark of the paged decode step on GB300.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
+
+A step is one pass of the whole hot path over the workload's batch: for every
+layer the new token's K/V are written into their slots (kv_cache_write), the
+split decode attends over the paged cache (paged_attention_decode) and the
+partitions are merged (paged_attention_reduce); shared-prefix workloads also
+replay their copy-on-write block copies (copy_blocks) once per step. Inputs
+are resident in HBM; the default workload (64 sequences x 8192 tokens x 16
+layers, 34 GB of K/V per step) is far larger than L2, smaller workloads flush
+L2 before every step.
+
+Prints one JSON line (rank 0). value = algorithmic bytes of the step (K/V
+pages touched + Q + out + block tables, per layer) / step time, in GB/s.
+`--impl reference` times the CPU oracle instead, on a bounded sample of the
+same workload, and prints the same metric.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "paged decode-attention HBM GB/s (% of GB300 peak) and decode tokens/s per layer"
+L2_BYTES = 129 * 1024 * 1024
+DECODE_SOURCES = ["paged_kv_cache_220_gb300/csrc/decode.cu",
+                  "paged_kv_cache_220_gb300/csrc/common.cuh"]
+
+
+def workload_for(name: str):
+    from paged_kv_cache_220_gb300 import synth
+    table = {
+        "qwen_like": lambda: synth.qwen_like(),
+        "tiny": lambda: synth.tiny(),
+        "mixed": lambda: synth.mixed(),
+        "cow": lambda: synth.cow(prompt_len=2048),
+        "cow2040": lambda: synth.cow(prompt_len=2040),
+        "long_fp8": lambda: synth.long_fp8(),
+    }
+    w = table[name]()
+    if name == "tiny":
+        import dataclasses
+        w = dataclasses.replace(w, partition_size=0)
+    return w
+
+
+def decode_bytes(w) -> int:
+    """Algorithmic bytes of one decode launch (one layer): K/V pages touched,
+    Q, out and the block tables."""
+    esz = 1 if w.fp8 else 2
+    B = w.block_size
+    kv = sum(w.ctx) * w.num_kv_heads * w.head_dim * esz * 2
+    qo = 2 * w.num_seqs * w.num_heads * w.head_dim * 2
+    mb = max(-(-c // B) for c in w.ctx)
+    bt = w.num_seqs * mb * 4
+    return kv + qo + bt
+
+
+def unique_decode_bytes(w) -> int:
+    """Shared prefixes counted once (the bytes a reader of unique pages moves)."""
+    if w.prefix_len <= 0:
+        return decode_bytes(w)
+    esz = 1 if w.fp8 else 2
+    per_tok = w.num_kv_heads * w.head_dim * esz * 2
+    n_prompt = w.num_seqs // w.group
+    tokens = n_prompt * w.prefix_len + sum(c - w.prefix_len for c in w.ctx)
+    return decode_bytes(w) - sum(w.ctx) * per_tok + tokens * per_tok
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def source_hash(paths) -> str:
+    h = hashlib.sha256()
+    for rel in paths:
+        h.update(open(os.path.join(ROOT, rel), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(config: str):
+    """dram bytes per decode launch from the committed ncu summary, if it was
+    taken on the current decode source."""
+    p = os.path.join(ROOT, "profiles", "decode_traffic.json")
+    if not os.path.exists(p):
+        return None, None
+    d = json.load(open(p))
+    ent = d.get(config)
+    if not ent or ent.get("source_hash") != source_hash(DECODE_SOURCES):
+        return None, None
+    return ent.get("dram_bytes_per_launch"), ent.get("note")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", "pkv_clocks_%d_%d.csv" % (os.getpid(), gpu_index))
+
+    def __enter__(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), "--query-gpu=" + self.Q,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return None
+        rows = []
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                rows.append(f)
+            except ValueError:
+                pass
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            for n, v in zip(names, r[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+def run_reference(args, w, rank):
+    """The CPU oracle on a bounded sample of the workload (same metric)."""
+    import numpy as np
+    import oracle
+    from paged_kv_cache_220_gb300 import synth
+
+    def bits(t):
+        return t.contiguous().view(__import__("torch").int16).numpy().view(np.uint16)
+
+    # sample: the first n sequences of layer 0, n sized for ~10-20 s of work
+    budget_tokens = int(os.environ.get("PKV_ORACLE_TOKENS", "131072"))
+    seqs, tok = [], 0
+    for s in range(w.num_seqs):
+        if tok >= budget_tokens and seqs:
+            break
+        seqs.append(s)
+        tok += w.ctx[s]
+    q = bits(w.q(0, "cpu"))[seqs]
+    ks, vs = [], []
+    ksc = vsc = None
+    for s in seqs:
+        K = w.rows(synth.KIND_K, 0, s, 0, w.ctx[s], "cpu")
+        V = w.rows(synth.KIND_V, 0, s, 0, w.ctx[s], "cpu")
+        if w.fp8:
+            if ksc is None:
+                ksc = (K.float().abs().amax(dim=(0, 2)) / 448.0).numpy()
+                vsc = (V.float().abs().amax(dim=(0, 2)) / 448.0).numpy()
+            ks.append(oracle.e4m3_encode((K.float().numpy() / ksc[None, :, None]).astype(np.float32)))
+            vs.append(oracle.e4m3_encode((V.float().numpy() / vsc[None, :, None]).astype(np.float32)))
+        else:
+            ks.append(bits(K))
+            vs.append(bits(V))
+    import dataclasses
+    sub = dataclasses.replace(w, ctx=[w.ctx[s] for s in seqs])
+    sample_bytes = decode_bytes(sub)
+    times = []
+    steps = args.steps if args.impl == "reference" else 1
+    for _ in range(steps):
+        t0 = time.perf_counter()
+        if w.fp8:
+            oracle.decode(q, ks, vs, w.scale, ksc.astype(np.float64), vsc.astype(np.float64))
+        else:
+            oracle.decode(q, ks, vs, w.scale)
+        times.append(time.perf_counter() - t0)
+    t = sum(times) / len(times)
+    gbs = sample_bytes / t / 1e9
+    return {
+        "value": round(gbs, 4), "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
+        "sample": "layer 0, sequences %d..%d (%d tokens), fp64 C oracle, %d repetition(s), "
+                  "%.2f s each" % (seqs[0], seqs[-1], tok, steps, t),
+        "seconds": round(t, 3),
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", default="qwen_like")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    w = workload_for(args.config)
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        cb = run_reference(args, w, rank)
+        line = {"metric": METRIC, "value": cb["value"], "unit": "GB/s", "impl": "reference",
+                "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": round(cb["seconds"] * 1000, 3), "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "config": {"workload": w.name, "sample": cb["sample"]},
+                "cpu_baseline": {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")},
+                "e2e": {"value": cb["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return 0
+
+    import torch
+    import paged_kv_cache_220_gb300 as pkv
+    from paged_kv_cache_220_gb300 import build as pkv_build
+    from paged_kv_cache_220_gb300 import workload
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    if rank == 0:
+        pkv_build.build()
+    if dist is not None:
+        dist.barrier()
+    pkv.lib()
+
+    # weak scaling: every rank runs its own batch of the workload
+    import dataclasses
+    if world > 1:
+        w = dataclasses.replace(w, seed=w.seed + 100 * rank)
+    pw = workload.build(w)
+    L = len(pw.layers)
+    P = w.partition_size
+    out = [torch.empty_like(st.q) for st in pw.layers]
+    ws = pkv.alloc_workspace(w.num_seqs, w.num_heads, w.head_dim, pw.max_context, P) if P else None
+    flush = None
+    per_step_bytes = decode_bytes(w) * L
+    if per_step_bytes < 4 * L2_BYTES:
+        flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    cow = pw.cow_pairs
+
+    def one_step(ev=None):
+        for layer, st in enumerate(pw.layers):
+            if cow is not None:
+                pkv.copy_blocks(st.k_cache, st.v_cache, cow)
+            pkv.kv_cache_write(st.k_new, st.v_new, pw.slot_mapping, st.k_cache, st.v_cache,
+                               st.k_scale, st.v_scale)
+            if ev is not None:
+                ev[layer][0].record(stream)
+            pkv.paged_attention_decode(out[layer], st.q, st.k_cache, st.v_cache, pw.block_tables,
+                                       pw.context_lens, w.scale, pw.max_context, P, ws,
+                                       st.k_scale, st.v_scale)
+            if ev is not None:
+                ev[layer][1].record(stream)
+            if P:
+                pkv.paged_attention_reduce(out[layer], ws, pw.context_lens, pw.max_context, P)
+
+    launches_per_step = L * (2 + (1 if P else 0) + (1 if cow is not None else 0))
+    for _ in range(args.warmup):
+        one_step()
+    torch.cuda.synchronize()
+
+    K = args.steps
+    evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(L)]
+           for _ in range(K)]
+    step_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        for i in range(K):
+            if flush is not None:
+                flush.fill_(i & 0xFF)
+            step_ev[i][0].record(stream)
+            one_step(evs[i])
+            step_ev[i][1].record(stream)
+        torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    step_ms = [a.elapsed_time(b) for a, b in step_ev]
+    total_ms = sum(step_ms)
+    dec_ms = [evs[i][l][0].elapsed_time(evs[i][l][1]) for i in range(K) for l in range(L)]
+    dec_avg_ms = sum(dec_ms) / len(dec_ms)
+    if dist is not None:
+        t = torch.tensor([total_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / K
+    value = per_step_bytes * world / (ms_per_step / 1e3) / 1e9
+
+    # end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, pw, w, out, ws, P, per_step_bytes, world, dist)
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return 0
+
+    peak, peak_kind = peaks()
+    dec_bytes = decode_bytes(w)
+    achieved = dec_bytes / (dec_avg_ms / 1e3) / 1e9
+    traffic, traffic_note = ncu_traffic(args.config)
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        cb = run_reference(args, w, rank)
+        cpu = {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")}
+    tok_per_s_layer = w.num_seqs * world / (ms_per_step / 1e3 / L)
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "fp8_e4m3" if w.fp8 else "bf16", "data": "synthetic",
+        "config": {
+            "workload": w.name, "layers": L, "num_seqs": w.num_seqs,
+            "context": w.ctx[0] if len(set(w.ctx)) == 1 else "mixed (sum %d)" % sum(w.ctx),
+            "num_heads": w.num_heads, "num_kv_heads": w.num_kv_heads,
+            "head_dim": w.head_dim, "block_size": w.block_size, "partition_size": P,
+            "kv_dtype": "fp8_e4m3" if w.fp8 else "bf16",
+            "l2": "flushed before every step" if flush is not None else
+                  "inputs larger than L2 (%.1f GB of K/V per step)" % (per_step_bytes / 1e9),
+            "parallelism": "replicas/weak: each GPU its own batch" if world > 1 else "1 GPU",
+        },
+        "pct_of_peak": round(100 * value / world / peak, 2),
+        "tokens_per_s_per_layer": round(tok_per_s_layer, 1),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "peak_kind": peak_kind, "kernel": "paged_attention_decode",
+                     "bytes_per_launch": dec_bytes, "launch_ms": round(dec_avg_ms, 5),
+                     "traffic": traffic},
+        "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": launches_per_step * K,
+        "clocks": clk.summary(),
+    }
+    if w.prefix_len > 0:
+        line["unique_bytes_gbs"] = round(unique_decode_bytes(w) * L * world / (ms_per_step / 1e3) / 1e9, 2)
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def run_e2e(args, pw, w, out, ws, P, per_step_bytes, world, dist):
+    """Same step through the public API, inputs copied from pinned host
+    memory every step (q, new K/V, slots, block tables, context lengths) and
+    the outputs copied back."""
+    import torch
+    import paged_kv_cache_220_gb300 as pkv
+    L = len(pw.layers)
+    host = []
+    for st in pw.layers:
+        host.append({k: getattr(st, k).cpu().pin_memory() for k in ("q", "k_new", "v_new")})
+    h_sm = pw.slot_mapping.cpu().pin_memory()
+    h_bt = pw.block_tables.cpu().pin_memory()
+    h_cl = pw.context_lens.cpu().pin_memory()
+    h_out = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in out]
+    dev = [{k: torch.empty_like(getattr(st, k)) for k in ("q", "k_new", "v_new")} for st in pw.layers]
+    d_sm, d_bt, d_cl = (torch.empty_like(pw.slot_mapping), torch.empty_like(pw.block_tables),
+                        torch.empty_like(pw.context_lens))
+    h2d = sum(t.numel() * t.element_size() for hl in host for t in hl.values()) + \
+        sum(t.numel() * t.element_size() for t in (h_sm, h_bt, h_cl))
+    d2h = sum(o.numel() * o.element_size() for o in out)
+
+    def step():
+        d_sm.copy_(h_sm, non_blocking=True)
+        d_bt.copy_(h_bt, non_blocking=True)
+        d_cl.copy_(h_cl, non_blocking=True)
+        for layer, st in enumerate(pw.layers):
+            for k in ("q", "k_new", "v_new"):
+                dev[layer][k].copy_(host[layer][k], non_blocking=True)
+            pkv.kv_cache_write(dev[layer]["k_new"], dev[layer]["v_new"], d_sm, st.k_cache,
+                               st.v_cache, st.k_scale, st.v_scale)
+            pkv.paged_attention(dev[layer]["q"], st.k_cache, st.v_cache, d_bt, d_cl, w.scale,
+                                pw.max_context, P, st.k_scale, st.v_scale, out=out[layer],
+                                workspace=ws)
+            h_out[layer].copy_(out[layer], non_blocking=True)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    K = args.steps
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0 = time.perf_counter()
+    a.record()
+    for _ in range(K):
+        step()
+    b.record()
+    torch.cuda.synchronize()
+    wall_ms = (time.perf_counter() - t0) * 1e3
+    ms = max(a.elapsed_time(b), wall_ms) / K
+    if dist is not None:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    return {"value": round(per_step_bytes * world / (ms / 1e3) / 1e9, 2), "unit": "GB/s",
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "ms_per_step": round(ms, 4)}
+
+
+if __name__ == "__main__":
+    sys.exit(main())

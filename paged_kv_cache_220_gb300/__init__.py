@@ -1,0 +1,329 @@
+"""Paged KV-cache decode attention for GB300 (sm_103a).
+
+Python binding of ``libpagedkv.so`` (the C ABI in ``include/pagedkv.h``).
+Every call marshals tensors into raw pointers and sizes and calls the
+library; all arithmetic runs in the library's CUDA kernels. There is no
+fallback: without the built library or a CUDA device the calls raise.
+
+Tensors (caller-owned device memory):
+  k_cache, v_cache : [num_blocks, num_kv_heads, block_size, head_dim],
+                     torch.bfloat16, or torch.uint8 / torch.float8_e4m3fn
+                     holding OCP E4M3 codes
+  q, out           : [num_seqs, num_heads, head_dim] torch.bfloat16
+  block_tables     : [num_seqs, max_blocks_per_seq] torch.int32
+  context_lens     : [num_seqs] torch.int32
+  slot_mapping     : [num_tokens] torch.int64 (-1 = skip)
+  k_scale, v_scale : [num_kv_heads] torch.float32 (FP8 pools)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libpagedkv.so")
+
+PKV_OK = 0
+PKV_ERR_INVALID_ARG = -1
+PKV_ERR_UNSUPPORTED = -2
+PKV_ERR_CUDA = -3
+PKV_ERR_OUT_OF_BLOCKS = -4
+PKV_ERR_NOT_FOUND = -5
+PKV_ERR_DEVICE_CHECK = -6
+PKV_DTYPE_BF16 = 0
+PKV_DTYPE_FP8_E4M3 = 1
+
+DEVERR_NONE = 0
+DEVERR_BLOCK_ID = 1
+DEVERR_SLOT = 2
+DEVERR_WAIT_TIMEOUT = 3
+DEVERR_CONTEXT = 4
+
+
+class PagedKVError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        super().__init__("%s: %s (%d)" % (what or "pagedkv", status_string(status), status))
+
+
+class CacheDesc(ctypes.Structure):
+    _fields_ = [("num_blocks", ctypes.c_int), ("block_size", ctypes.c_int),
+                ("num_kv_heads", ctypes.c_int), ("head_dim", ctypes.c_int),
+                ("dtype", ctypes.c_int)]
+
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_lib = None
+
+# name -> (restype, argtypes); mirrors include/pagedkv.h
+SIGNATURES = {
+    "pkv_kv_cache_write": (_I, [_P, _P, _P, _I, _P, _P, CacheDesc, _P, _P, _P]),
+    "pkv_decode_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I, _I, _I]),
+    "pkv_paged_attention_decode": (_I, [_P, _P, _P, _P, CacheDesc, _P, _P, _P, _I, _P, _I, _I,
+                                        _I, ctypes.c_float, _I, _P, ctypes.c_size_t, _P]),
+    "pkv_paged_attention_reduce": (_I, [_P, _P, ctypes.c_size_t, _P, _I, _I, _I, _I, _I, _P]),
+    "pkv_copy_blocks": (_I, [_P, _P, CacheDesc, _P, _I, _P]),
+    "pkv_set_device_check": (_I, [_P]),
+    "pkv_status_string": (ctypes.c_char_p, [_I]),
+    "pkv_version": (_I, []),
+    "pkv_alloc_create": (_I, [_I, _I, ctypes.c_uint64, ctypes.POINTER(_P)]),
+    "pkv_alloc_destroy": (None, [_P]),
+    "pkv_seq_new": (_I, [_P, ctypes.POINTER(_I)]),
+    "pkv_seq_fork": (_I, [_P, _I, ctypes.POINTER(_I)]),
+    "pkv_seq_append": (_I, [_P, _I, _I, _P, _P, ctypes.POINTER(_I)]),
+    "pkv_seq_free": (_I, [_P, _I]),
+    "pkv_seq_block_table": (_I, [_P, _I, _P, _I, ctypes.POINTER(_I)]),
+    "pkv_seq_len": (_I, [_P, _I, ctypes.POINTER(_I)]),
+    "pkv_block_refcount": (_I, [_P, _I, ctypes.POINTER(_I)]),
+    "pkv_alloc_stats": (_I, [_P, ctypes.POINTER(_I), ctypes.POINTER(_I),
+                             ctypes.POINTER(ctypes.c_longlong)]),
+}
+
+
+def lib() -> ctypes.CDLL:
+    """Load libpagedkv.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError("libpagedkv.so is not built: run "
+                               "`python -m paged_kv_cache_220_gb300.build`")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    try:
+        return lib().pkv_status_string(int(status)).decode()
+    except Exception:  # library missing
+        return "status %d" % status
+
+
+def _check(rc: int, what: str) -> None:
+    if rc != PKV_OK:
+        raise PagedKVError(rc, what)
+
+
+def _dev_ptr(t, name, dtype=None):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if dtype is not None and t.dtype not in (dtype if isinstance(dtype, tuple) else (dtype,)):
+        raise ValueError("%s has dtype %s, expected %s" % (name, t.dtype, dtype))
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+_FP8_DTYPES = (torch.uint8,) + ((torch.float8_e4m3fn,) if hasattr(torch, "float8_e4m3fn") else ())
+
+
+def cache_desc(k_cache: torch.Tensor) -> CacheDesc:
+    """Geometry of a [num_blocks, Hk, B, D] pool tensor."""
+    if k_cache.dim() != 4:
+        raise ValueError("cache must be [num_blocks, num_kv_heads, block_size, head_dim]")
+    nb, hk, bs, d = k_cache.shape
+    if k_cache.dtype == torch.bfloat16:
+        dt = PKV_DTYPE_BF16
+    elif k_cache.dtype in _FP8_DTYPES:
+        dt = PKV_DTYPE_FP8_E4M3
+    else:
+        raise ValueError("cache dtype must be bfloat16 or uint8/float8_e4m3fn (E4M3)")
+    return CacheDesc(nb, bs, hk, d, dt)
+
+
+def kv_cache_write(k, v, slot_mapping, k_cache, v_cache, k_scale=None, v_scale=None,
+                   stream=None) -> None:
+    """Scatter k, v [T, Hk, D] bf16 into their slots (bit-exact for bf16;
+    E4M3 round-to-nearest-even with saturation of x / scale[h] for FP8)."""
+    desc = cache_desc(k_cache)
+    if v_cache.shape != k_cache.shape or v_cache.dtype != k_cache.dtype:
+        raise ValueError("k_cache and v_cache must match")
+    n = int(slot_mapping.shape[0])
+    if k.shape != (n, desc.num_kv_heads, desc.head_dim) or v.shape != k.shape:
+        raise ValueError("k, v must be [num_tokens, num_kv_heads, head_dim]")
+    rc = lib().pkv_kv_cache_write(
+        _dev_ptr(k, "k", torch.bfloat16), _dev_ptr(v, "v", torch.bfloat16),
+        _dev_ptr(slot_mapping, "slot_mapping", torch.int64), n,
+        _dev_ptr(k_cache, "k_cache"), _dev_ptr(v_cache, "v_cache"), desc,
+        _dev_ptr(k_scale, "k_scale", torch.float32), _dev_ptr(v_scale, "v_scale", torch.float32),
+        _stream(stream))
+    _check(rc, "kv_cache_write")
+
+
+def decode_workspace_bytes(num_seqs, num_heads, head_dim, max_context, partition_size) -> int:
+    return int(lib().pkv_decode_workspace_bytes(num_seqs, num_heads, head_dim, max_context,
+                                                partition_size))
+
+
+def alloc_workspace(num_seqs, num_heads, head_dim, max_context, partition_size,
+                    device=None) -> torch.Tensor:
+    n = decode_workspace_bytes(num_seqs, num_heads, head_dim, max_context, partition_size)
+    return torch.empty(max(n, 16), dtype=torch.uint8, device=device or "cuda")
+
+
+def paged_attention_decode(out, q, k_cache, v_cache, block_tables, context_lens, scale,
+                           max_context, partition_size=0, workspace=None, k_scale=None,
+                           v_scale=None, stream=None) -> None:
+    """One launch of the decode kernel (see pkv_paged_attention_decode)."""
+    desc = cache_desc(k_cache)
+    S, Hq, D = q.shape
+    if D != desc.head_dim:
+        raise ValueError("q head_dim does not match the cache")
+    if block_tables.dim() != 2 or block_tables.shape[0] != S or context_lens.shape != (S,):
+        raise ValueError("block_tables must be [S, max_blocks], context_lens [S]")
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    rc = lib().pkv_paged_attention_decode(
+        _dev_ptr(out, "out", torch.bfloat16) if partition_size == 0 else None,
+        _dev_ptr(q, "q", torch.bfloat16), _dev_ptr(k_cache, "k_cache"),
+        _dev_ptr(v_cache, "v_cache"), desc,
+        _dev_ptr(k_scale, "k_scale", torch.float32), _dev_ptr(v_scale, "v_scale", torch.float32),
+        _dev_ptr(block_tables, "block_tables", torch.int32), int(block_tables.shape[1]),
+        _dev_ptr(context_lens, "context_lens", torch.int32), S, Hq, int(max_context),
+        float(scale), int(partition_size), _dev_ptr(workspace, "workspace"), ws_bytes,
+        _stream(stream))
+    _check(rc, "paged_attention_decode")
+
+
+def paged_attention_reduce(out, workspace, context_lens, max_context, partition_size,
+                           stream=None) -> None:
+    S, Hq, D = out.shape
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    rc = lib().pkv_paged_attention_reduce(
+        _dev_ptr(out, "out", torch.bfloat16), _dev_ptr(workspace, "workspace"), ws_bytes,
+        _dev_ptr(context_lens, "context_lens", torch.int32), S, Hq, D, int(max_context),
+        int(partition_size), _stream(stream))
+    _check(rc, "paged_attention_reduce")
+
+
+def paged_attention(q, k_cache, v_cache, block_tables, context_lens, scale, max_context,
+                    partition_size=0, k_scale=None, v_scale=None, out=None, workspace=None,
+                    stream=None) -> torch.Tensor:
+    """Decode attention; with partition_size > 0 the split decode is followed
+    by the reduce. Returns out [S, Hq, D] bf16."""
+    if out is None:
+        out = torch.empty_like(q)
+    if partition_size > 0 and workspace is None:
+        workspace = alloc_workspace(q.shape[0], q.shape[1], q.shape[2], max(int(max_context), 1),
+                                    partition_size, device=q.device)
+    paged_attention_decode(out, q, k_cache, v_cache, block_tables, context_lens, scale,
+                           max_context, partition_size, workspace, k_scale, v_scale, stream)
+    if partition_size > 0:
+        paged_attention_reduce(out, workspace, context_lens, max_context, partition_size, stream)
+    return out
+
+
+def copy_blocks(k_cache, v_cache, block_pairs, stream=None) -> None:
+    """k_cache[dst] = k_cache[src] (same for v) for each row (src, dst) of
+    block_pairs [n, 2] int32."""
+    desc = cache_desc(k_cache)
+    n = int(block_pairs.shape[0]) if block_pairs is not None else 0
+    if n == 0:
+        return
+    rc = lib().pkv_copy_blocks(_dev_ptr(k_cache, "k_cache"), _dev_ptr(v_cache, "v_cache"), desc,
+                               _dev_ptr(block_pairs, "block_pairs", torch.int32), n,
+                               _stream(stream))
+    _check(rc, "copy_blocks")
+
+
+def set_device_check(flag) -> None:
+    """Register a 1-element int32 CUDA tensor as the device error word
+    (None switches reporting off). Keep the tensor alive while registered."""
+    ptr = None if flag is None else _dev_ptr(flag, "flag", torch.int32)
+    lib().pkv_set_device_check(ptr)
+
+
+class BlockAllocator:
+    """Host block allocator (free list, refcounts, fork, copy-on-write)."""
+
+    def __init__(self, num_blocks: int, block_size: int, seed: int = 0):
+        h = ctypes.c_void_p()
+        _check(lib().pkv_alloc_create(int(num_blocks), int(block_size), int(seed),
+                                      ctypes.byref(h)), "alloc_create")
+        self._h = h
+        self.num_blocks = int(num_blocks)
+        self.block_size = int(block_size)
+
+    def close(self) -> None:
+        if getattr(self, "_h", None):
+            lib().pkv_alloc_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def new_seq(self) -> int:
+        sid = ctypes.c_int()
+        _check(lib().pkv_seq_new(self._h, ctypes.byref(sid)), "seq_new")
+        return sid.value
+
+    def fork(self, parent: int) -> int:
+        sid = ctypes.c_int()
+        _check(lib().pkv_seq_fork(self._h, int(parent), ctypes.byref(sid)), "seq_fork")
+        return sid.value
+
+    def append(self, seq: int, n_tokens: int = 1):
+        """Returns (slots int64 [n], cow_pairs int32 [k, 2])."""
+        slots = np.empty(max(n_tokens, 1), dtype=np.int64)
+        pairs = np.empty((max(n_tokens, 1), 2), dtype=np.int32)
+        ncow = ctypes.c_int()
+        rc = lib().pkv_seq_append(self._h, int(seq), int(n_tokens),
+                                  slots.ctypes.data_as(ctypes.c_void_p),
+                                  pairs.ctypes.data_as(ctypes.c_void_p), ctypes.byref(ncow))
+        _check(rc, "seq_append")
+        return slots[:n_tokens], pairs[:ncow.value]
+
+    def free(self, seq: int) -> None:
+        _check(lib().pkv_seq_free(self._h, int(seq)), "seq_free")
+
+    def block_table(self, seq: int) -> np.ndarray:
+        n = ctypes.c_int()
+        rc = lib().pkv_seq_block_table(self._h, int(seq), None, 0, ctypes.byref(n))
+        if rc not in (PKV_OK, PKV_ERR_INVALID_ARG):
+            _check(rc, "seq_block_table")
+        out = np.empty(max(n.value, 1), dtype=np.int32)
+        _check(lib().pkv_seq_block_table(self._h, int(seq), out.ctypes.data_as(ctypes.c_void_p),
+                                         out.size, ctypes.byref(n)), "seq_block_table")
+        return out[:n.value]
+
+    def seq_len(self, seq: int) -> int:
+        n = ctypes.c_int()
+        _check(lib().pkv_seq_len(self._h, int(seq), ctypes.byref(n)), "seq_len")
+        return n.value
+
+    def refcount(self, block: int) -> int:
+        n = ctypes.c_int()
+        _check(lib().pkv_block_refcount(self._h, int(block), ctypes.byref(n)), "block_refcount")
+        return n.value
+
+    def stats(self):
+        f, u, s = ctypes.c_int(), ctypes.c_int(), ctypes.c_longlong()
+        _check(lib().pkv_alloc_stats(self._h, ctypes.byref(f), ctypes.byref(u), ctypes.byref(s)),
+               "alloc_stats")
+        return {"free_blocks": f.value, "used_blocks": u.value, "used_slots": s.value}
+
+    def block_tables(self, seqs, max_blocks: int) -> np.ndarray:
+        """int32 [len(seqs), max_blocks] padded with -1."""
+        out = np.full((len(seqs), max_blocks), -1, dtype=np.int32)
+        for i, s in enumerate(seqs):
+            t = self.block_table(s)
+            out[i, :len(t)] = t
+        return out

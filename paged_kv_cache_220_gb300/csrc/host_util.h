@@ -1,0 +1,48 @@
+// Host-side argument checks shared by the C entry points.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/pagedkv.h"
+
+namespace pkv {
+
+// Device error word registered with pkv_set_device_check (may be null).
+int* device_error_ptr();
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+inline int elem_bytes(int dtype) { return dtype == PKV_DTYPE_FP8_E4M3 ? 1 : 2; }
+
+// Shape checks common to every call that touches a pool.
+inline int check_cache_desc(const pkv_cache_desc& c) {
+  if (c.num_blocks <= 0 || c.num_kv_heads <= 0 || c.block_size <= 0 || c.head_dim <= 0)
+    return PKV_ERR_INVALID_ARG;
+  if (c.dtype != PKV_DTYPE_BF16 && c.dtype != PKV_DTYPE_FP8_E4M3) return PKV_ERR_INVALID_ARG;
+  if (c.block_size != 16 && c.block_size != 32) return PKV_ERR_UNSUPPORTED;
+  if (c.head_dim != 128 && c.head_dim != 256) return PKV_ERR_UNSUPPORTED;
+  if (c.num_kv_heads > 32) return PKV_ERR_UNSUPPORTED;
+  return PKV_OK;
+}
+
+inline int launch_status() {
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+// Raise a kernel's dynamic shared-memory limit once per device.
+template <typename Kernel>
+inline int ensure_smem(Kernel k, size_t bytes, bool* done_per_device, int max_devices) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
+  if (dev < max_devices && done_per_device[dev]) return PKV_OK;
+  if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(bytes)) != cudaSuccess)
+    return PKV_ERR_CUDA;
+  if (dev < max_devices) done_per_device[dev] = true;
+  return PKV_OK;
+}
+
+}  // namespace pkv

@@ -1,0 +1,203 @@
+"""Build the device state of a decode workload through the library itself.
+
+The allocator hands out slots (seeded random placement), the cache is filled
+with the history rows [0, ctx - 1) through ``kv_cache_write``, and the state
+for one decode step is kept ready: the new token's K/V rows and slots, the
+query, the block tables and context lengths. Layers share one block table
+(every layer's pool uses the same block ids) and have their own pools.
+
+Shared prefixes (``Workload.prefix_len > 0``): the first rollout of each prompt
+is created and filled with the prompt rows, the others are forks of it; then
+every rollout appends its first completion token in one step, which is where
+copy-on-write pairs appear (a prompt whose last block is partly filled); those
+pairs are executed with ``copy_blocks`` before the completion rows are
+written.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+from typing import List, Optional
+
+import numpy as np
+import torch
+
+import paged_kv_cache_220_gb300 as pkv
+from paged_kv_cache_220_gb300 import synth
+
+
+@dataclass
+class LayerState:
+    k_cache: torch.Tensor
+    v_cache: torch.Tensor
+    q: torch.Tensor                 # [S, Hq, D] bf16
+    k_new: torch.Tensor             # [S, Hk, D] bf16, row ctx-1 of each sequence
+    v_new: torch.Tensor
+    k_scale: Optional[torch.Tensor] = None
+    v_scale: Optional[torch.Tensor] = None
+
+
+@dataclass
+class PagedWorkload:
+    w: synth.Workload
+    alloc: pkv.BlockAllocator
+    seqs: List[int]
+    block_tables: torch.Tensor      # [S, MB] int32 (device)
+    context_lens: torch.Tensor      # [S] int32 (device)
+    slot_mapping: torch.Tensor      # [S] int64 (device): slot of row ctx-1
+    max_context: int
+    layers: List[LayerState] = field(default_factory=list)
+    cow_pairs: Optional[torch.Tensor] = None   # [n, 2] int32 from the divergence step
+    cow_pairs_host: Optional[np.ndarray] = None
+    tables_host: Optional[np.ndarray] = None
+    history_slots: Optional[List[np.ndarray]] = None
+
+    @property
+    def num_seqs(self):
+        return self.w.num_seqs
+
+
+def _write_rows(w, layer, st, seq, slots, t0, t1, device, k_scale, v_scale):
+    """Generate logical rows [t0, t1) of `seq` and store them at `slots`."""
+    if t1 <= t0:
+        return
+    k = w.rows(synth.KIND_K, layer, seq, t0, t1, device)
+    v = w.rows(synth.KIND_V, layer, seq, t0, t1, device)
+    sm = torch.as_tensor(np.ascontiguousarray(slots[: t1 - t0]), device=device)
+    pkv.kv_cache_write(k, v, sm, st.k_cache, st.v_cache, k_scale, v_scale)
+
+
+def fp8_scales(w: synth.Workload, layer: int, device) -> tuple:
+    """Per-KV-head scales amax_h / 448 (fp32) over every logical row of every
+    sequence (history and the new token) of the layer."""
+    Hk = w.num_kv_heads
+    amax = []
+    for kind in (synth.KIND_K, synth.KIND_V):
+        m = torch.zeros(Hk, dtype=torch.float32, device=device)
+        for s in range(w.num_seqs):
+            r = w.rows(kind, layer, s, 0, w.ctx[s], device).float().abs()
+            m = torch.maximum(m, r.amax(dim=(0, 2)))
+        amax.append(m)
+    return amax[0] / 448.0, amax[1] / 448.0
+
+
+def build(w: synth.Workload, device="cuda", layers: Optional[int] = None,
+          alloc_seed: Optional[int] = None, share_prefix: bool = True) -> PagedWorkload:
+    """share_prefix=False gives every rollout a private copy of its prompt
+    (same logical rows, no shared blocks), for aliasing comparisons."""
+    device = torch.device(device)
+    L = w.layers if layers is None else layers
+    B = w.block_size
+    nb = w.pool_blocks()
+    if w.prefix_len > 0 and not share_prefix:
+        nb = sum(-(-c // B) for c in w.ctx) + w.slack_blocks
+    alloc = pkv.BlockAllocator(nb, B, seed=w.seed if alloc_seed is None else alloc_seed)
+    S = w.num_seqs
+    Hk, D = w.num_kv_heads, w.head_dim
+    cache_dtype = torch.uint8 if w.fp8 else torch.bfloat16
+    states = []
+    for layer in range(L):
+        kc = torch.zeros(alloc.num_blocks, Hk, B, D, dtype=cache_dtype, device=device)
+        vc = torch.zeros_like(kc)
+        ks = vs = None
+        if w.fp8:
+            ks, vs = fp8_scales(w, layer, device)
+        states.append(LayerState(kc, vc, w.q(layer, device), None, None, ks, vs))
+
+    seqs: List[int] = []
+    hist_slots: List[Optional[np.ndarray]] = [None] * S
+    cow_pairs = np.zeros((0, 2), dtype=np.int32)
+    if w.prefix_len > 0 and not share_prefix:
+        for s in range(S):
+            sid = alloc.new_seq()
+            seqs.append(sid)
+            slots, _ = alloc.append(sid, w.ctx[s])
+            for layer in range(L):
+                _write_rows(w, layer, states[layer], s, slots, 0, w.ctx[s] - 1, device,
+                            states[layer].k_scale, states[layer].v_scale)
+    elif w.prefix_len > 0:
+        G, P = w.group, w.prefix_len
+        n_prompt = S // G
+        seqs = [0] * S
+        slot_parts = [[] for _ in range(S)]
+        for p in range(n_prompt):
+            s0 = alloc.new_seq()
+            slots, _ = alloc.append(s0, P)
+            for layer in range(L):
+                _write_rows(w, layer, states[layer], p * G, slots, 0, P, device,
+                            states[layer].k_scale, states[layer].v_scale)
+            ids = [s0] + [alloc.fork(s0) for _ in range(G - 1)]
+            for r in range(G):
+                seqs[p * G + r] = ids[r]
+                slot_parts[p * G + r].append(slots)
+        # divergence: every rollout appends its first completion token; the
+        # first G-1 rollouts of a prompt clone a partly filled last block
+        pairs = []
+        first = [None] * S
+        order = []
+        for p in range(n_prompt):
+            order += [p * G + r for r in range(1, G)] + [p * G]
+        for s in order:
+            sl, pr = alloc.append(seqs[s], 1)
+            first[s] = sl
+            pairs += [tuple(x) for x in pr.tolist()]
+        cow_pairs = np.array(pairs, dtype=np.int32).reshape(-1, 2)
+        if len(pairs):
+            cp = torch.as_tensor(cow_pairs, device=device)
+            for st in states:
+                pkv.copy_blocks(st.k_cache, st.v_cache, cp)
+        for s in range(S):
+            rest = w.ctx[s] - P - 1                      # further tokens after the first
+            more, pr = alloc.append(seqs[s], rest) if rest > 0 else (np.zeros(0, np.int64), [])
+            assert len(pr) == 0
+            full = np.concatenate(slot_parts[s] + [first[s], more])
+            hist_slots[s] = full
+            for layer in range(L):
+                _write_rows(w, layer, states[layer], s, full[P:], P, w.ctx[s] - 1, device,
+                            states[layer].k_scale, states[layer].v_scale)
+    else:
+        for s in range(S):
+            sid = alloc.new_seq()
+            seqs.append(sid)
+            slots, _ = alloc.append(sid, w.ctx[s])
+            hist_slots[s] = slots
+            for layer in range(L):
+                _write_rows(w, layer, states[layer], s, slots, 0, w.ctx[s] - 1, device,
+                            states[layer].k_scale, states[layer].v_scale)
+
+    MB = max(1, max(-(-c // B) for c in w.ctx))
+    tables = alloc.block_tables(seqs, MB)
+    # final slot of every logical position, read off the final block tables
+    # (a cloned block moves the positions it holds)
+    for s in range(S):
+        pos = np.arange(w.ctx[s], dtype=np.int64)
+        hist_slots[s] = tables[s][pos // B].astype(np.int64) * B + pos % B
+    slot_new = np.array([hist_slots[s][w.ctx[s] - 1] for s in range(S)], dtype=np.int64)
+    for layer, st in enumerate(states):
+        st.k_new = torch.stack([w.rows(synth.KIND_K, layer, s, w.ctx[s] - 1, w.ctx[s], device)[0]
+                                for s in range(S)])
+        st.v_new = torch.stack([w.rows(synth.KIND_V, layer, s, w.ctx[s] - 1, w.ctx[s], device)[0]
+                                for s in range(S)])
+    pw = PagedWorkload(
+        w=w, alloc=alloc, seqs=seqs,
+        block_tables=torch.as_tensor(tables, device=device),
+        context_lens=torch.as_tensor(np.array(w.ctx, dtype=np.int32), device=device),
+        slot_mapping=torch.as_tensor(slot_new, device=device),
+        max_context=w.max_context, layers=states,
+        cow_pairs=torch.as_tensor(cow_pairs, device=device) if len(cow_pairs) else None,
+        cow_pairs_host=cow_pairs, tables_host=tables, history_slots=hist_slots)
+    return pw
+
+
+def step(pw: PagedWorkload, out: List[torch.Tensor], workspace: Optional[torch.Tensor],
+         partition_size: Optional[int] = None, stream=None) -> None:
+    """One decode step over every layer: write the new token, attend, merge."""
+    P = pw.w.partition_size if partition_size is None else partition_size
+    for layer, st in enumerate(pw.layers):
+        pkv.kv_cache_write(st.k_new, st.v_new, pw.slot_mapping, st.k_cache, st.v_cache,
+                           st.k_scale, st.v_scale, stream)
+        pkv.paged_attention_decode(out[layer], st.q, st.k_cache, st.v_cache, pw.block_tables,
+                                   pw.context_lens, pw.w.scale, pw.max_context, P, workspace,
+                                   st.k_scale, st.v_scale, stream)
+        if P > 0:
+            pkv.paged_attention_reduce(out[layer], workspace, pw.context_lens, pw.max_context, P,
+                                       stream)

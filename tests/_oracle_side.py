@@ -1,0 +1,98 @@
+"""Oracle-side inputs and comparisons for the GPU parity tests.
+
+Everything here is computed on the host from the seeded generator (the same
+element streams the device side generates) and the oracle; nothing is read
+back from the CUDA library except the outputs under test.
+"""
+import numpy as np
+import torch
+
+import oracle
+from paged_kv_cache_220_gb300 import synth
+
+# Tolerances for bf16 attention outputs (and FP8-KV outputs against the
+# oracle on the same FP8 codes): maximum absolute error and relative L2 error.
+MAX_ABS = 1e-2
+REL_L2 = 5e-3
+
+
+def bits16(t: torch.Tensor) -> np.ndarray:
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def bf16_to_f64(bits: np.ndarray) -> np.ndarray:
+    return (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def host_rows(w: synth.Workload, layer: int, s: int, t1: int = None):
+    t1 = w.ctx[s] if t1 is None else t1
+    return (w.rows(synth.KIND_K, layer, s, 0, t1, "cpu"),
+            w.rows(synth.KIND_V, layer, s, 0, t1, "cpu"))
+
+
+_ALL_BF16 = (np.arange(65536, dtype=np.uint32) << 16).view(np.float32)
+
+
+def quantize(rows_bf16: torch.Tensor, scale: np.ndarray) -> np.ndarray:
+    """E4M3 codes of x / scale[h] (fp32 quotient) with the oracle's encoder.
+    The encoder is a pure function of the bf16 input and the head's scale, so
+    it is evaluated once on all 65,536 bf16 patterns per head and looked up."""
+    bits = bits16(rows_bf16)
+    out = np.empty(bits.shape, dtype=np.uint8)
+    for h in range(bits.shape[1]):
+        with np.errstate(over="ignore", invalid="ignore"):
+            y = (_ALL_BF16 / np.float32(scale[h])).astype(np.float32)
+        lut = oracle.e4m3_encode(y)
+        out[:, h, :] = lut[bits[:, h, :]]
+    return out
+
+
+def expected(w: synth.Workload, layer: int, seqs, k_scale=None, v_scale=None) -> np.ndarray:
+    """fp64 oracle output [len(seqs), Hq, D] for the given sequences."""
+    q = bits16(w.q(layer, "cpu"))[list(seqs)]
+    ks, vs = [], []
+    for s in seqs:
+        K, V = host_rows(w, layer, s)
+        if w.fp8:
+            ks.append(quantize(K, k_scale))
+            vs.append(quantize(V, v_scale))
+        else:
+            ks.append(bits16(K))
+            vs.append(bits16(V))
+    if w.fp8:
+        return oracle.decode(q, ks, vs, w.scale, k_scale.astype(np.float64),
+                             v_scale.astype(np.float64))
+    return oracle.decode(q, ks, vs, w.scale)
+
+
+def expected_pool(w: synth.Workload, layer: int, num_blocks: int, slots_per_seq,
+                  k_scale=None, v_scale=None):
+    """Pool images (K, V) after every logical row of every sequence has been
+    written to its slot: the block-table definition applied by the oracle."""
+    dt = np.uint8 if w.fp8 else np.uint16
+    shape = (num_blocks, w.num_kv_heads, w.block_size, w.head_dim)
+    pk, pv = np.zeros(shape, dtype=dt), np.zeros(shape, dtype=dt)
+    for s in range(w.num_seqs):
+        K, V = host_rows(w, layer, s)
+        if w.fp8:
+            k, v = quantize(K, k_scale), quantize(V, v_scale)
+        else:
+            k, v = bits16(K), bits16(V)
+        oracle.scatter_rows_fast(pk, k, slots_per_seq[s])
+        oracle.scatter_rows_fast(pv, v, slots_per_seq[s])
+    return pk, pv
+
+
+def errors(got_bf16: torch.Tensor, ref: np.ndarray):
+    g = bf16_to_f64(bits16(got_bf16))
+    diff = g - ref
+    max_abs = float(np.max(np.abs(diff))) if diff.size else 0.0
+    den = float(np.linalg.norm(ref))
+    rel = float(np.linalg.norm(diff)) / den if den > 0 else float(np.linalg.norm(diff))
+    return max_abs, rel
+
+
+def assert_close(got_bf16, ref, what=""):
+    ma, rl = errors(got_bf16, ref)
+    assert ma <= MAX_ABS and rl <= REL_L2, "%s: max_abs=%.3e rel_l2=%.3e" % (what, ma, rl)
+    return ma, rl

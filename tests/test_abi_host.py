@@ -1,0 +1,102 @@
+"""The C-ABI library loads without a GPU, exports every function the header
+declares, and rejects bad arguments before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import paged_kv_cache_220_gb300 as pkv
+from paged_kv_cache_220_gb300 import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "pagedkv.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(pkv_[a-z0-9_]+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return pkv.lib()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared()
+    assert len(names) >= 18
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(pkv.SIGNATURES), set(names) ^ set(pkv.SIGNATURES)
+
+
+def test_version_and_status_strings(lib):
+    assert lib.pkv_version() >= 100
+    for code in range(-6, 1):
+        assert pkv.status_string(code) not in ("", "unknown status")
+    assert pkv.status_string(-99) == "unknown status"
+
+
+def _desc(nb=8, bs=16, hk=2, d=128, dt=0):
+    return pkv.CacheDesc(nb, bs, hk, d, dt)
+
+
+FAKE = ctypes.c_void_p(0x10000)      # never dereferenced: validation fails first
+
+
+def test_cache_write_validation(lib):
+    f = lib.pkv_kv_cache_write
+    assert f(FAKE, FAKE, FAKE, 0, FAKE, FAKE, _desc(), None, None, None) == pkv.PKV_OK
+    assert f(FAKE, FAKE, FAKE, -1, FAKE, FAKE, _desc(), None, None, None) == pkv.PKV_ERR_INVALID_ARG
+    assert f(None, FAKE, FAKE, 4, FAKE, FAKE, _desc(), None, None, None) == pkv.PKV_ERR_INVALID_ARG
+    assert f(FAKE, FAKE, FAKE, 4, FAKE, FAKE, _desc(bs=8), None, None, None) == pkv.PKV_ERR_UNSUPPORTED
+    assert f(FAKE, FAKE, FAKE, 4, FAKE, FAKE, _desc(d=64), None, None, None) == pkv.PKV_ERR_UNSUPPORTED
+    assert f(FAKE, FAKE, FAKE, 4, FAKE, FAKE, _desc(dt=1), None, None, None) == pkv.PKV_ERR_INVALID_ARG
+    odd = ctypes.c_void_p(0x10008)
+    assert f(odd, FAKE, FAKE, 4, FAKE, FAKE, _desc(), None, None, None) == pkv.PKV_ERR_INVALID_ARG
+
+
+def test_decode_validation(lib):
+    f = lib.pkv_paged_attention_decode
+    args = lambda **kw: [kw.get("out", FAKE), FAKE, FAKE, FAKE, kw.get("desc", _desc()), None, None,
+                         FAKE, kw.get("mb", 64), FAKE, kw.get("S", 4), kw.get("Hq", 8),
+                         kw.get("maxc", 1024), kw.get("scale", 0.088), kw.get("P", 0),
+                         kw.get("ws", None), kw.get("wsb", 0), None]
+    assert f(*args(S=0)) == pkv.PKV_OK
+    assert f(*args(Hq=7)) == pkv.PKV_ERR_INVALID_ARG           # not a multiple of Hk
+    assert f(*args(Hq=18)) == pkv.PKV_ERR_UNSUPPORTED          # group 9
+    assert f(*args(maxc=1025)) == pkv.PKV_ERR_INVALID_ARG      # beyond the table
+    assert f(*args(P=24)) == pkv.PKV_ERR_INVALID_ARG           # not a multiple of B
+    assert f(*args(P=512)) == pkv.PKV_ERR_INVALID_ARG          # no workspace
+    assert f(*args(P=512, ws=FAKE, wsb=16)) == pkv.PKV_ERR_INVALID_ARG  # too small
+    assert f(*args(out=None)) == pkv.PKV_ERR_INVALID_ARG
+    assert f(*args(scale=float("nan"))) == pkv.PKV_ERR_INVALID_ARG
+    assert f(*args(desc=_desc(dt=1))) == pkv.PKV_ERR_INVALID_ARG  # fp8 without scales
+
+
+def test_workspace_size(lib):
+    # [S][Hq][NP] partial outputs of D floats plus max and sum
+    n = pkv.decode_workspace_bytes(8, 24, 256, 131072, 512)
+    assert n == 8 * 24 * 256 * (256 + 2) * 4
+    assert pkv.decode_workspace_bytes(8, 24, 256, 131072, 0) == 0
+
+
+def test_reduce_and_copy_validation(lib):
+    r = lib.pkv_paged_attention_reduce
+    assert r(FAKE, None, 0, FAKE, 4, 8, 128, 100, 0, None) == pkv.PKV_ERR_INVALID_ARG
+    assert r(FAKE, None, 0, FAKE, 4, 8, 96, 100, 64, None) == pkv.PKV_ERR_UNSUPPORTED
+    assert r(FAKE, None, 0, FAKE, 4, 8, 128, 100, 64, None) == pkv.PKV_ERR_INVALID_ARG
+    c = lib.pkv_copy_blocks
+    assert c(FAKE, FAKE, _desc(), FAKE, 0, None) == pkv.PKV_OK
+    assert c(FAKE, FAKE, _desc(), None, 3, None) == pkv.PKV_ERR_INVALID_ARG
+    assert c(FAKE, FAKE, _desc(), FAKE, -1, None) == pkv.PKV_ERR_INVALID_ARG
+
+
+def test_binding_fails_loudly_without_cuda_tensors(lib):
+    import torch
+    k = torch.zeros(4, 2, 128, dtype=torch.bfloat16)
+    cache = torch.zeros(8, 2, 16, 128, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        pkv.kv_cache_write(k, k, torch.zeros(4, dtype=torch.int64), cache, cache)
