@@ -194,6 +194,45 @@ int pkv_paged_attention_reduce(void* out, const void* workspace,
 int pkv_copy_blocks(void* k_cache, void* v_cache, pkv_cache_desc cache,
                     const int32_t* block_pairs, int num_pairs, void* stream);
 
+/* ------------------------------------------------------------------------ *
+ * paged_attention_decode_noalloc: split decode + merge that allocates
+ * nothing. (The pages have no counterpart; this is a service for callers.)
+ *
+ * For callers that cannot call cudaMalloc or provide a workspace: code
+ * running inside a framework that owns the whole device-memory budget and
+ * forbids allocations outside its arena, C callers without a device
+ * allocator, and latency-critical paths where an allocation (which can
+ * synchronise the device) is not acceptable. The per-partition partials go
+ * to a fixed array of PKV_NOALLOC_SCRATCH_BYTES bytes of device memory that
+ * belongs to the library; every GPU that loads this part of the library
+ * holds that array until the process exits.
+ *
+ * Arguments and result are those of pkv_paged_attention_decode with
+ * partition_size > 0 followed by pkv_paged_attention_reduce: `out` receives
+ * the merged bf16 output. The caller still passes every input and output.
+ *   - Returns PKV_ERR_UNSUPPORTED when the partials,
+ *     pkv_decode_workspace_bytes(num_seqs, num_heads, head_dim, max_context,
+ *     partition_size), exceed PKV_NOALLOC_SCRATCH_BYTES (use a larger
+ *     partition_size or the workspace form), PKV_ERR_INVALID_ARG for
+ *     partition_size <= 0, and every error of the two calls it makes.
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current) and caches it; make that first call before any
+ *     stream capture.
+ *   - All calls in the process share the one array and it keeps the last
+ *     call's contents; nothing in it needs to start at zero. Calls whose
+ *     kernels may overlap on the GPU (other streams, other host threads)
+ *     race on it: serialise them.
+ * ------------------------------------------------------------------------ */
+#define PKV_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+
+int pkv_paged_attention_decode_noalloc(void* out, const void* q, const void* k_cache,
+                                       const void* v_cache, pkv_cache_desc cache,
+                                       const float* k_scale, const float* v_scale,
+                                       const int32_t* block_tables, int max_blocks_per_seq,
+                                       const int32_t* context_lens, int num_seqs,
+                                       int num_heads, int max_context, float scale,
+                                       int partition_size, void* stream);
+
 /* Register a device int32 that kernels write a PKV_DEVERR_* code into (first
  * error wins; the caller clears it). NULL switches reporting off; the kernels
  * still skip out-of-range ids. Process-wide; returns PKV_OK. */

@@ -66,6 +66,8 @@ SIGNATURES = {
     "pkv_paged_attention_decode": (_I, [_P, _P, _P, _P, CacheDesc, _P, _P, _P, _I, _P, _I, _I,
                                         _I, ctypes.c_float, _I, _P, ctypes.c_size_t, _P]),
     "pkv_paged_attention_reduce": (_I, [_P, _P, ctypes.c_size_t, _P, _I, _I, _I, _I, _I, _P]),
+    "pkv_paged_attention_decode_noalloc": (_I, [_P, _P, _P, _P, CacheDesc, _P, _P, _P, _I, _P,
+                                                _I, _I, _I, ctypes.c_float, _I, _P]),
     "pkv_copy_blocks": (_I, [_P, _P, CacheDesc, _P, _I, _P]),
     "pkv_set_device_check": (_I, [_P]),
     "pkv_status_string": (ctypes.c_char_p, [_I]),
@@ -226,6 +228,27 @@ def paged_attention(q, k_cache, v_cache, block_tables, context_lens, scale, max_
     if partition_size > 0:
         paged_attention_reduce(out, workspace, context_lens, max_context, partition_size, stream)
     return out
+
+
+NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
+
+
+def paged_attention_decode_noalloc(out, q, k_cache, v_cache, block_tables, context_lens, scale,
+                                   max_context, partition_size, k_scale=None, v_scale=None,
+                                   stream=None) -> None:
+    """Split decode + merge into `out` with the library's own fixed scratch
+    (no workspace, no allocation). For callers that cannot allocate device
+    memory; calls that may overlap on the GPU share the scratch and race."""
+    desc = cache_desc(k_cache)
+    S, Hq, D = q.shape
+    rc = lib().pkv_paged_attention_decode_noalloc(
+        _dev_ptr(out, "out", torch.bfloat16), _dev_ptr(q, "q", torch.bfloat16),
+        _dev_ptr(k_cache, "k_cache"), _dev_ptr(v_cache, "v_cache"), desc,
+        _dev_ptr(k_scale, "k_scale", torch.float32), _dev_ptr(v_scale, "v_scale", torch.float32),
+        _dev_ptr(block_tables, "block_tables", torch.int32), int(block_tables.shape[1]),
+        _dev_ptr(context_lens, "context_lens", torch.int32), S, Hq, int(max_context),
+        float(scale), int(partition_size), _stream(stream))
+    _check(rc, "paged_attention_decode_noalloc")
 
 
 def copy_blocks(k_cache, v_cache, block_pairs, stream=None) -> None:

@@ -24,7 +24,7 @@ ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CUFLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2",
            "--expt-relaxed-constexpr", "-I" + INCLUDE]
 SOURCES = ["api.cu", "kv_cache_write.cu", "copy_blocks.cu", "decode.cu", "reduce.cu",
-           "allocator.cpp"]
+           "decode_noalloc.cu", "allocator.cpp"]
 
 
 def nvcc() -> str:
