@@ -227,6 +227,12 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="override the layer count (profiling of a smaller case)")
+    ap.add_argument("--seqs", type=int, default=0,
+                    help="override the number of sequences (profiling of a smaller case)")
+    ap.add_argument("--partition", type=int, default=-1,
+                    help="override the partition size (0 = one pass)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -234,6 +240,13 @@ def main():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     w = workload_for(args.config)
+    import dataclasses
+    if args.layers > 0:
+        w = dataclasses.replace(w, layers=args.layers)
+    if args.seqs > 0:
+        w = dataclasses.replace(w, ctx=w.ctx[:args.seqs])
+    if args.partition >= 0:
+        w = dataclasses.replace(w, partition_size=args.partition)
 
     if args.impl == "reference":
         if rank != 0:
@@ -270,7 +283,6 @@ def main():
     pkv.lib()
 
     # weak scaling: every rank runs its own batch of the workload
-    import dataclasses
     if world > 1:
         w = dataclasses.replace(w, seed=w.seed + 100 * rank)
     pw = workload.build(w)

@@ -29,6 +29,7 @@
 #include <cmath>
 
 #include "common.cuh"
+#include "decode_params.h"
 #include "host_util.h"
 
 namespace pkv {
@@ -39,28 +40,7 @@ constexpr int kBarrierBytes = 256;  // room for 2 * 16 mbarriers
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
-struct DecodeParams {
-  const uint16_t* q;  // [S][Hq][D] bf16 bits
-  const uint8_t* k_cache;
-  const uint8_t* v_cache;
-  const float* k_scale;
-  const float* v_scale;
-  const int32_t* block_tables;
-  const int32_t* context_lens;
-  uint16_t* out;       // [S][Hq][D] (one pass)
-  float* tmp_out;      // [S][Hq][NPmax][D] (split)
-  float* max_logits;   // [S][Hq][NPmax]
-  float* exp_sums;     // [S][Hq][NPmax]
-  int* err;
-  int num_blocks;
-  int num_kv_heads;
-  int num_heads;
-  int group;
-  int max_blocks_per_seq;
-  int partition_blocks;  // 0 = whole context in one CTA
-  int np_max;
-  float qscale;          // scale * log2(e)
-};
+
 
 template <int D, int BS, bool FP8>
 struct PageGeom {
@@ -409,6 +389,12 @@ extern "C" int pkv_paged_attention_decode(void* out, const void* q, const void* 
   }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int D = cache.head_dim, BS = cache.block_size;
+  if (!fp8) {
+    // bf16 pools: tensor-core kernel with TMA tensor loads (decode_tc.cu)
+    if (static_cast<int64_t>(cache.num_blocks) * cache.num_kv_heads * BS >= (int64_t{1} << 31))
+      return PKV_ERR_UNSUPPORTED;
+    return launch_decode_tc(p, k_cache, v_cache, D, BS, grid, st);
+  }
   if (D == 128 && BS == 16) return dispatch_dtype<128, 16>(p, fp8, grid, st);
   if (D == 128 && BS == 32) return dispatch_dtype<128, 32>(p, fp8, grid, st);
   if (D == 256 && BS == 16) return dispatch_dtype<256, 16>(p, fp8, grid, st);

@@ -1,0 +1,440 @@
+// Tensor-core paged decode for bf16 pools.
+//
+// Same computation as the SIMT decode (decode.cu): one query token per
+// sequence, the GQA group of g <= 8 query heads against the pages of one KV
+// head, fp32 online softmax, per-partition partials in the split form. The
+// kernel walks the block table and gathers the scattered pages ("Dissecting
+// vLLM: How PagedAttention and Continuous Batching Maximize Throughput",
+// section "PagedAttention: Virtual Memory for KV Cache").
+//
+// Data movement (the part that sets the speed, decode being bound by HBM):
+// - a producer warp reads the block table and loads every (block, head) page
+//   of K and V with TMA tensor copies (cp.async.bulk.tensor, one 128-byte x B
+//   box per 64 head-dim columns, 128-byte swizzle) into a ring of shared
+//   memory stages; an mbarrier per stage counts the bytes in;
+// - the swizzle makes the row-strided fragment loads below bank-conflict
+//   free although a page row is 256 or 512 bytes long.
+//
+// Arithmetic, per 16-token slice of a page (one consumer warp per page):
+// - S^T[16 tokens x 8] = K_slice[16 x D] . Q^T[D x 8] with mma.m16n8k16
+//   (bf16 in, fp32 out); tokens are the M side, the padded query group the N
+//   side, Q's fragments stay in registers for the whole CTA;
+// - online softmax on the accumulator fragment (base 2, logit scale applied
+//   in fp32); per-query maxima across the 16 tokens by three xor shuffles;
+// - the probabilities are split into a bf16 high part and a bf16 remainder
+//   (P = P_hi + P_lo to ~16 bits), turned into the B operand of the next
+//   product with movmatrix (an 8x8 transpose in registers);
+// - O^T[D x 8] += V_slice^T[D x 16] . P^T[16 x 8] with mma.m16n8k16, V^T's
+//   fragments read by ldmatrix.trans from the swizzled page.
+// At the end the consumer warps' states are merged in a fixed order, so the
+// result depends on logical positions only.
+#include <cmath>
+#include <cudaTypedefs.h>
+#include <mutex>
+
+#include "common.cuh"
+#include "decode_params.h"
+#include "host_util.h"
+
+namespace pkv {
+
+constexpr float kLn2Tc = 0.6931471805599453f;
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                          uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+__device__ __forceinline__ uint32_t movm_t(uint32_t a) {
+  uint32_t d;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+  return d;
+}
+
+// D += A(16x16, row) * B(16x8, col); bf16 inputs, fp32 accumulators.
+__device__ __forceinline__ void mma_bf16(float* d, uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);  // .x = lo (low 16 bits)
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Byte address of element (row, col) of a page stored as [D/64][B][128 B]
+// with the 128-byte swizzle (16-byte unit index xor row % 8). The page base
+// is 1024-byte aligned, so the xor term equals ((addr >> 7) & 7).
+template <int BS>
+__device__ __forceinline__ uint32_t swz(uint32_t page, int row, int col) {
+  const uint32_t a = page + (col >> 6) * (BS * 128) + row * 128 + (col & 63) * 2;
+  return a ^ (((a >> 7) & 7u) << 4);
+}
+
+// NST is a multiple of NW: page `it` goes to consumer warp it % NW and to
+// stage it % NST, so every stage belongs to one warp. A warp therefore waits
+// on a stage's phase k only after it released phase k-1 itself, and the
+// parity test of the wait cannot alias an older phase.
+template <int D, int BS, int NW, int NST>
+struct TcGeom {
+  static_assert(NST % NW == 0, "stages must be private to a consumer warp");
+  static constexpr int kPage = BS * D * 2;
+  static constexpr int kStage = 2 * kPage;
+  static constexpr int kRing = NST * kStage;
+  static constexpr int kMerge = NW * 8 * D * 4 + 2 * NW * 8 * 4;
+  static constexpr int kSmem = 1024 /*barriers*/ + 1024 /*alignment*/ +
+                               (kRing > kMerge ? kRing : kMerge);
+  static constexpr int kThreads = (NW + 1) * 32;
+};
+
+template <int D, int BS, int NW, int NST>
+__global__ void __launch_bounds__(TcGeom<D, BS, NW, NST>::kThreads)
+    decode_tc_kernel(const __grid_constant__ CUtensorMap tmk,
+                     const __grid_constant__ CUtensorMap tmv, const DecodeParams p) {
+  using G = TcGeom<D, BS, NW, NST>;
+  constexpr int PAGE = G::kPage;
+  constexpr int KT = D / 16;  // k-steps of Q.K^T == 16-row tiles of O^T
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_addr(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* sbase = smem_raw + (base - raw);
+  uint64_t* full = reinterpret_cast<uint64_t*>(sbase);
+  uint64_t* empty = full + NST;
+  const uint32_t ring = base + 1024;
+  float* ring_f = reinterpret_cast<float*>(sbase + 1024);
+
+  const int part = blockIdx.x;
+  const int h = blockIdx.y;
+  const int s = blockIdx.z;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int g = p.group;
+
+  int ctx = p.context_lens[s];
+  const int cap = p.max_blocks_per_seq * BS;
+  if (ctx < 0 || ctx > cap) {
+    if (threadIdx.x == 0 && part == 0 && h == 0) report_error(p.err, PKV_DEVERR_CONTEXT);
+    ctx = ctx < 0 ? 0 : cap;
+  }
+  int blk_begin = 0;
+  int blk_end = (ctx + BS - 1) / BS;
+  if (p.partition_blocks > 0) {
+    blk_begin = part * p.partition_blocks;
+    if (blk_begin >= blk_end) return;  // partition past the end: nothing to store
+    blk_end = min(blk_end, blk_begin + p.partition_blocks);
+  }
+  const int nblk = blk_end - blk_begin;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < NST; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  int issued = 0;  // producer lane 0 only
+  // per-thread softmax state for queries q0 = 2*(lane%4), q1 = q0 + 1
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+  float o[KT][4];
+
+  if (warp == NW) {
+    // ---------------- producer: block table walk, TMA tensor copies
+    if (lane == 0) {
+      const int32_t* bt = p.block_tables + static_cast<int64_t>(s) * p.max_blocks_per_seq;
+      for (int it = 0; it < nblk; ++it) {
+        const int st = it % NST;
+        if (it >= NST && !mbar_wait(&empty[st], ((it / NST) - 1) & 1, p.err)) break;
+        const int32_t pb = bt[blk_begin + it];
+        issued = it + 1;
+        if (pb < 0 || pb >= p.num_blocks) {
+          report_error(p.err, PKV_DEVERR_BLOCK_ID);
+          mbar_arrive(&full[st]);  // release the stage without data
+          continue;
+        }
+        const uint32_t kdst = ring + st * G::kStage;
+        const int y = (pb * p.num_kv_heads + h) * BS;
+        mbar_arrive_expect_tx(&full[st], 2 * PAGE);
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c) {
+          tma_load_2d(kdst + c * BS * 128, &tmk, c * 64, y, &full[st]);
+          tma_load_2d(kdst + PAGE + c * BS * 128, &tmv, c * 64, y, &full[st]);
+        }
+      }
+    }
+  } else {
+    // ---------------- consumers
+    // Q^T fragments (B operand of m16n8k16): b0 = Q[n][16k + 2(lane%4) + {0,1}],
+    // b1 = the same 8 columns further, n = lane/4 (zero for n >= g).
+    uint32_t bq[KT][2];
+    {
+      const int n = lane >> 2;
+      const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
+          p.q + (static_cast<int64_t>(s) * p.num_heads + h * g + n) * D);
+#pragma unroll
+      for (int k = 0; k < KT; ++k) {
+        bq[k][0] = n < g ? __ldg(qrow + (k * 16 + (lane & 3) * 2) / 2) : 0u;
+        bq[k][1] = n < g ? __ldg(qrow + (k * 16 + 8 + (lane & 3) * 2) / 2) : 0u;
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < KT; ++k) o[k][0] = o[k][1] = o[k][2] = o[k][3] = 0.f;
+    const float qs = p.qscale;
+
+    for (int it = warp; it < nblk; it += NW) {
+      const int st = it % NST;
+      if (!mbar_wait(&full[st], (it / NST) & 1, p.err)) break;
+      const uint32_t kp = ring + st * G::kStage;
+      const uint32_t vp = kp + PAGE;
+      const int ntok = min(BS, ctx - (blk_begin + it) * BS);
+      if (ntok < BS) {
+        // slots past the context hold whatever was there: zero their V rows so
+        // the zero probabilities cannot meet a NaN in the product
+        for (int r = ntok; r < BS; ++r)
+          for (int c = lane * 8; c < D; c += 256)
+            asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(swz<BS>(vp, r, c)), "r"(0u)
+                         : "memory");
+        __syncwarp();
+      }
+#pragma unroll 1
+      for (int r0 = 0; r0 < BS; r0 += 16) {
+        // ---- S^T = K_slice . Q^T (two accumulators halve the dependency chain)
+        float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+        const int arow = r0 + (lane & 7) + ((lane >> 3) & 1) * 8;
+        const int acol = (lane >> 4) * 8;
+#pragma unroll
+        for (int k = 0; k < KT; ++k) {
+          uint32_t a0, a1, a2, a3;
+          ldsm_x4(swz<BS>(kp, arow, k * 16 + acol), a0, a1, a2, a3);
+          mma_bf16((k & 1) ? sb : sa, a0, a1, a2, a3, bq[k][0], bq[k][1]);
+        }
+        // ---- online softmax on the fragment: rows = tokens, cols = queries
+        const int t0 = r0 + (lane >> 2), t1 = t0 + 8;
+        const float s00 = t0 < ntok ? (sa[0] + sb[0]) * qs : -INFINITY;
+        const float s01 = t0 < ntok ? (sa[1] + sb[1]) * qs : -INFINITY;
+        const float s10 = t1 < ntok ? (sa[2] + sb[2]) * qs : -INFINITY;
+        const float s11 = t1 < ntok ? (sa[3] + sb[3]) * qs : -INFINITY;
+        float mx0 = fmaxf(s00, s10), mx1 = fmaxf(s01, s11);
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+          mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+        }
+        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+        if (__any_sync(0xffffffffu, (mn0 > m0) || (mn1 > m1))) {
+          const float c0 = fast_exp2(m0 - mn0), c1 = fast_exp2(m1 - mn1);  // 0 when m was -inf
+          l0 *= c0;
+          l1 *= c1;
+#pragma unroll
+          for (int k = 0; k < KT; ++k) {
+            o[k][0] *= c0;
+            o[k][1] *= c1;
+            o[k][2] *= c0;
+            o[k][3] *= c1;
+          }
+          m0 = mn0;
+          m1 = mn1;
+        }
+        // every slice has a valid token in row 0 of the warp's first page, so
+        // m is finite from the first slice on and masked logits give p = 0
+        const float p00 = fast_exp2(s00 - m0), p01 = fast_exp2(s01 - m1);
+        const float p10 = fast_exp2(s10 - m0), p11 = fast_exp2(s11 - m1);
+        l0 += p00 + p10;
+        l1 += p01 + p11;
+        // ---- P = P_hi + P_lo in bf16, transposed into the B operand
+        const uint32_t hi_t = pack_bf16(p00, p01), hi_b = pack_bf16(p10, p11);
+        const __nv_bfloat162 ht = *reinterpret_cast<const __nv_bfloat162*>(&hi_t);
+        const __nv_bfloat162 hb = *reinterpret_cast<const __nv_bfloat162*>(&hi_b);
+        const uint32_t lo_t = pack_bf16(p00 - __low2float(ht), p01 - __high2float(ht));
+        const uint32_t lo_b = pack_bf16(p10 - __low2float(hb), p11 - __high2float(hb));
+        const uint32_t bh0 = movm_t(hi_t), bh1 = movm_t(hi_b);
+        const uint32_t bl0 = movm_t(lo_t), bl1 = movm_t(lo_b);
+        // ---- O^T += V_slice^T . P^T
+        const int vrow = r0 + (lane & 7) + ((lane >> 4) & 1) * 8;
+        const int vcol = ((lane >> 3) & 1) * 8;
+#pragma unroll
+        for (int k = 0; k < KT; ++k) {
+          uint32_t a0, a1, a2, a3;
+          ldsm_x4_t(swz<BS>(vp, vrow, k * 16 + vcol), a0, a1, a2, a3);
+          mma_bf16(o[k], a0, a1, a2, a3, bh0, bh1);
+          mma_bf16(o[k], a0, a1, a2, a3, bl0, bl1);
+        }
+      }
+      if (ntok < BS) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[st]);
+    }
+    // per-query sums over the 8 lanes that share a query pair
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+      l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+    }
+  }
+
+  __syncthreads();
+  if (warp == NW && lane == 0) {
+    // wait for every copy this CTA issued before the ring is reused
+    const int first = issued > NST ? issued - NST : 0;
+    for (int it = first; it < issued; ++it)
+      if (!mbar_wait(&full[it % NST], (it / NST) & 1, p.err)) break;
+  }
+  __syncthreads();
+
+  // ---------------- merge the warp states in a fixed order
+  float* mo = ring_f;                   // [NW][8][D]
+  float* mm = mo + NW * 8 * D;          // [NW][8]
+  float* ml = mm + NW * 8;              // [NW][8]
+  if (warp < NW) {
+    const int q0 = (lane & 3) * 2;
+    const int d0 = lane >> 2;
+#pragma unroll
+    for (int k = 0; k < KT; ++k) {
+      mo[(warp * 8 + q0) * D + k * 16 + d0] = o[k][0];
+      mo[(warp * 8 + q0 + 1) * D + k * 16 + d0] = o[k][1];
+      mo[(warp * 8 + q0) * D + k * 16 + d0 + 8] = o[k][2];
+      mo[(warp * 8 + q0 + 1) * D + k * 16 + d0 + 8] = o[k][3];
+    }
+    if (lane < 4) {
+      mm[warp * 8 + q0] = m0;
+      mm[warp * 8 + q0 + 1] = m1;
+      ml[warp * 8 + q0] = l0;
+      ml[warp * 8 + q0 + 1] = l1;
+    }
+  }
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < g * D; idx += G::kThreads) {
+    const int j = idx / D;
+    const int c = idx % D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) M = fmaxf(M, mm[w * 8 + j]);
+    float L = 0.f, O = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < NW; ++w) {
+        const float a = fast_exp2(mm[w * 8 + j] - M);
+        L = fmaf(ml[w * 8 + j], a, L);
+        O = fmaf(mo[(w * 8 + j) * D + c], a, O);
+      }
+    }
+    const float res = L > 0.f ? O / L : 0.f;
+    const int64_t hq = static_cast<int64_t>(s) * p.num_heads + h * g + j;
+    if (p.partition_blocks == 0) {
+      p.out[hq * D + c] = float_to_bf16_bits(res);
+    } else {
+      p.tmp_out[(hq * p.np_max + part) * D + c] = res;
+      if (c == 0) {
+        p.max_logits[hq * p.np_max + part] = M * kLn2Tc;
+        p.exp_sums[hq * p.np_max + part] = L;
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------- host side
+
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+// Tensor map of one pool viewed as a 2-D array [rows = NB*Hk*B][D] of bf16,
+// box = 64 columns x B rows, 128-byte swizzle. Encodings are cached.
+static int pool_tensor_map(CUtensorMap* out, const void* base, int64_t rows, int D, int BS) {
+  struct Entry {
+    const void* base;
+    int64_t rows;
+    int d, bs;
+    CUtensorMap map;
+  };
+  static std::mutex mu;
+  static Entry cache[32];
+  static int used = 0, next = 0;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < used; ++i)
+      if (cache[i].base == base && cache[i].rows == rows && cache[i].d == D && cache[i].bs == BS) {
+        *out = cache[i].map;
+        return PKV_OK;
+      }
+  }
+  auto enc = tensor_map_encoder();
+  if (!enc) return PKV_ERR_CUDA;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(D) * 2};
+  cuuint32_t box[2] = {64u, static_cast<cuuint32_t>(BS)};
+  cuuint32_t estr[2] = {1u, 1u};
+  CUtensorMap m;
+  CUresult r = enc(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
+                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return PKV_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(mu);
+  Entry& e = cache[next];
+  e = Entry{base, rows, D, BS, m};
+  next = (next + 1) % 32;
+  if (used < 32) ++used;
+  *out = m;
+  return PKV_OK;
+}
+
+template <int D, int BS, int NW, int NST>
+static int launch_tc(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
+                     dim3 grid, cudaStream_t st) {
+  using G = TcGeom<D, BS, NW, NST>;
+  static bool done[64] = {false};
+  auto kern = decode_tc_kernel<D, BS, NW, NST>;
+  int rc = ensure_smem(kern, G::kSmem, done, 64);
+  if (rc != PKV_OK) return rc;
+  kern<<<grid, G::kThreads, G::kSmem, st>>>(tk, tv, p);
+  return launch_status();
+}
+
+int launch_decode_tc(const DecodeParams& p, const void* k_cache, const void* v_cache,
+                     int head_dim, int block_size, dim3 grid, cudaStream_t st) {
+  const int64_t rows = static_cast<int64_t>(p.num_blocks) * p.num_kv_heads * block_size;
+  CUtensorMap tk, tv;
+  int rc = pool_tensor_map(&tk, k_cache, rows, head_dim, block_size);
+  if (rc != PKV_OK) return rc;
+  rc = pool_tensor_map(&tv, v_cache, rows, head_dim, block_size);
+  if (rc != PKV_OK) return rc;
+  if (head_dim == 256 && block_size == 16) return launch_tc<256, 16, 2, 4>(p, tk, tv, grid, st);
+  if (head_dim == 256 && block_size == 32) return launch_tc<256, 32, 2, 2>(p, tk, tv, grid, st);
+  if (head_dim == 128 && block_size == 16) return launch_tc<128, 16, 4, 8>(p, tk, tv, grid, st);
+  return launch_tc<128, 32, 2, 4>(p, tk, tv, grid, st);
+}
+
+}  // namespace pkv
