@@ -134,8 +134,10 @@ int pkv_kv_cache_write(const void* k, const void* v, const int64_t* slot_mapping
  *   context_lens : device int32 [num_seqs]; a context of 0 yields zeros
  *   max_context  : host upper bound of context_lens (sizes the grid)
  *   scale        : logit scale, normally 1/sqrt(head_dim)
- *   partition_size : 0 = one pass over the whole context, the result goes to
- *               `out`. Otherwise a multiple of block_size: the context is cut
+ *   partition_size : 0 = one pass: the result goes to `out` directly (the
+ *               library spreads each sequence over a thread-block cluster of up
+ *               to 8 CTAs and merges their softmax states on chip; no
+ *               workspace). Otherwise a multiple of block_size: the context is cut
  *               into partitions [p*P, (p+1)*P) starting at token 0, and each
  *               partition's (max, sum, normalised output) is written to
  *               `workspace`; pkv_paged_attention_reduce then merges them.

@@ -103,6 +103,25 @@ def e4m3_encode(x) -> np.ndarray:
     return out
 
 
+_ALL_BF16 = (np.arange(65536, dtype=np.uint32) << 16).view(np.float32)
+
+
+def e4m3_encode_bf16(bits: np.ndarray, scale) -> np.ndarray:
+    """E4M3 codes of x / scale[h] (fp32 quotient) for bf16 bit patterns
+    bits[..., h, :]. The encoder is a pure function of the bf16 input and the
+    head's scale, so it is evaluated once on all 65,536 bf16 patterns per
+    head and looked up."""
+    bits = np.asarray(bits, dtype=np.uint16)
+    scale = np.asarray(scale, dtype=np.float32)
+    out = np.empty(bits.shape, dtype=np.uint8)
+    for h in range(bits.shape[-2]):
+        with np.errstate(over="ignore", invalid="ignore"):
+            y = (_ALL_BF16 / np.float32(scale[h])).astype(np.float32)
+        lut = e4m3_encode(y)
+        out[..., h, :] = lut[bits[..., h, :]]
+    return out
+
+
 def e4m3_decode(codes) -> np.ndarray:
     """uint8 E4M3 codes -> float64 values."""
     c = np.ascontiguousarray(np.asarray(codes, dtype=np.uint8))

@@ -26,11 +26,12 @@ struct DecodeParams {
   int max_blocks_per_seq;
   int partition_blocks;  // 0 = whole context in one CTA
   int np_max;
+  int cluster;           // one pass: CTAs (a thread-block cluster) per (seq, KV head)
   float qscale;          // scale * log2(e)
 };
 
-// Tensor-core decode for bf16 pools (decode_tc.cu). Returns a pkv_status.
+// Tensor-core decode (decode_tc.cu) for bf16 or E4M3 pools. Returns a pkv_status.
 int launch_decode_tc(const DecodeParams& p, const void* k_cache, const void* v_cache,
-                     int head_dim, int block_size, dim3 grid, cudaStream_t st);
+                     int head_dim, int block_size, bool fp8, dim3 grid, cudaStream_t st);
 
 }  // namespace pkv

@@ -1,11 +1,10 @@
-// Tensor-core paged decode for bf16 pools.
+// Tensor-core paged decode for bf16 and FP8 (E4M3) pools.
 //
-// Same computation as the SIMT decode (decode.cu): one query token per
-// sequence, the GQA group of g <= 8 query heads against the pages of one KV
-// head, fp32 online softmax, per-partition partials in the split form. The
-// kernel walks the block table and gathers the scattered pages ("Dissecting
-// vLLM: How PagedAttention and Continuous Batching Maximize Throughput",
-// section "PagedAttention: Virtual Memory for KV Cache").
+// One query token per sequence, the GQA group of g <= 8 query heads against
+// the pages of one KV head, fp32 online softmax, per-partition partials in the
+// split form. The kernel walks the block table and gathers the scattered pages
+// ("Dissecting vLLM: How PagedAttention and Continuous Batching Maximize
+// Throughput", section "PagedAttention: Virtual Memory for KV Cache").
 //
 // Data movement (the part that sets the speed, decode being bound by HBM):
 // - a producer warp reads the block table and loads every (block, head) page
@@ -63,6 +62,22 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t&
                : "r"(addr));
 }
 
+// All threads of all CTAs of the cluster; release/acquire orders shared
+// memory writes before the barrier with reads after it, across the cluster.
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
+               ::: "memory");
+}
+
+// fp32 at shared address `addr` of cluster rank `rank` (same offset there).
+__device__ __forceinline__ float ld_dsmem(uint32_t addr, int rank) {
+  uint32_t ra;
+  float v;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(addr), "r"(rank));
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(ra) : "memory");
+  return v;
+}
+
 __device__ __forceinline__ uint32_t movm_t(uint32_t a) {
   uint32_t d;
   asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
@@ -84,12 +99,42 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-// Byte address of element (row, col) of a page stored as [D/64][B][128 B]
-// with the 128-byte swizzle (16-byte unit index xor row % 8). The page base
-// is 1024-byte aligned, so the xor term equals ((addr >> 7) & 7).
+__device__ __forceinline__ void mma_f16(float* d, uint32_t a0, uint32_t a1, uint32_t a2,
+                                        uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+  __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Two E4M3 codes (the low or the high 16 bits of w) -> f16x2, exact.
+__device__ __forceinline__ uint32_t e4m3x2_f16x2(uint32_t w, int hi) {
+  uint32_t d;
+  const uint16_t x = static_cast<uint16_t>(hi ? (w >> 16) : (w & 0xFFFFu));
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(d) : "h"(x));
+  return d;
+}
+
+// Row of the 16-row output tile that holds head-dimension offset `i` of the
+// FP8 product (see the PV step below): rows 0-7 hold offsets {0,1,4,5,8,9,12,13},
+// rows 8-15 hold {2,3,6,7,10,11,14,15}.
+__device__ __forceinline__ int fp8_row_offset(int row) {
+  const int j = row & 7;
+  return 4 * (j >> 1) + (j & 1) + (row >= 8 ? 2 : 0);
+}
+
+// A page is stored as [D*esz/128][B][128 B]: one TMA box per 128-byte column
+// chunk, 128-byte swizzle (16-byte unit index xor row % 8). Page bases are
+// 1024-byte aligned, so the xor term equals ((addr >> 7) & 7).
 template <int BS>
-__device__ __forceinline__ uint32_t swz(uint32_t page, int row, int col) {
-  const uint32_t a = page + (col >> 6) * (BS * 128) + row * 128 + (col & 63) * 2;
+__device__ __forceinline__ uint32_t swz_bytes(uint32_t page, int row, int byte_col) {
+  const uint32_t a = page + (byte_col >> 7) * (BS * 128) + row * 128 + (byte_col & 127);
   return a ^ (((a >> 7) & 7u) << 4);
 }
 
@@ -97,24 +142,29 @@ __device__ __forceinline__ uint32_t swz(uint32_t page, int row, int col) {
 // stage it % NST, so every stage belongs to one warp. A warp therefore waits
 // on a stage's phase k only after it released phase k-1 itself, and the
 // parity test of the wait cannot alias an older phase.
-template <int D, int BS, int NW, int NST>
+template <int D, int BS, bool FP8, int NW, int NST>
 struct TcGeom {
   static_assert(NST % NW == 0, "stages must be private to a consumer warp");
-  static constexpr int kPage = BS * D * 2;
+  static constexpr int kEsz = FP8 ? 1 : 2;
+  static constexpr int kPage = BS * D * kEsz;
+  static constexpr int kChunks = D * kEsz / 128;  // TMA boxes per page
+  static constexpr int kBoxCols = 128 / kEsz;     // elements per box row
   static constexpr int kStage = 2 * kPage;
   static constexpr int kRing = NST * kStage;
-  static constexpr int kMerge = NW * 8 * D * 4 + 2 * NW * 8 * 4;
+  // warp states [NW][8][D] + max/sum, then the CTA state [8][D] + max/sum
+  static constexpr int kMerge = NW * 8 * D * 4 + 2 * NW * 8 * 4 + 8 * D * 4 + 2 * 8 * 4;
   static constexpr int kSmem = 1024 /*barriers*/ + 1024 /*alignment*/ +
                                (kRing > kMerge ? kRing : kMerge);
   static constexpr int kThreads = (NW + 1) * 32;
 };
 
-template <int D, int BS, int NW, int NST>
-__global__ void __launch_bounds__(TcGeom<D, BS, NW, NST>::kThreads)
+template <int D, int BS, bool FP8, int NW, int NST>
+__global__ void __launch_bounds__(TcGeom<D, BS, FP8, NW, NST>::kThreads)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tmk,
                      const __grid_constant__ CUtensorMap tmv, const DecodeParams p) {
-  using G = TcGeom<D, BS, NW, NST>;
+  using G = TcGeom<D, BS, FP8, NW, NST>;
   constexpr int PAGE = G::kPage;
+  constexpr int ESZ = G::kEsz;
   constexpr int KT = D / 16;  // k-steps of Q.K^T == 16-row tiles of O^T
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
@@ -144,6 +194,12 @@ __global__ void __launch_bounds__(TcGeom<D, BS, NW, NST>::kThreads)
     blk_begin = part * p.partition_blocks;
     if (blk_begin >= blk_end) return;  // partition past the end: nothing to store
     blk_end = min(blk_end, blk_begin + p.partition_blocks);
+  } else if (p.cluster > 1) {
+    // one pass over a cluster: rank r takes an equal share of the pages (it may
+    // get none, but it still takes part in the cluster merge below)
+    const int share = (blk_end + p.cluster - 1) / p.cluster;
+    blk_begin = min(blk_end, part * share);
+    blk_end = min(blk_end, blk_begin + share);
   }
   const int nblk = blk_end - blk_begin;
 
@@ -179,16 +235,19 @@ __global__ void __launch_bounds__(TcGeom<D, BS, NW, NST>::kThreads)
         const int y = (pb * p.num_kv_heads + h) * BS;
         mbar_arrive_expect_tx(&full[st], 2 * PAGE);
 #pragma unroll
-        for (int c = 0; c < D / 64; ++c) {
-          tma_load_2d(kdst + c * BS * 128, &tmk, c * 64, y, &full[st]);
-          tma_load_2d(kdst + PAGE + c * BS * 128, &tmv, c * 64, y, &full[st]);
+        for (int c = 0; c < G::kChunks; ++c) {
+          tma_load_2d(kdst + c * BS * 128, &tmk, c * G::kBoxCols, y, &full[st]);
+          tma_load_2d(kdst + PAGE + c * BS * 128, &tmv, c * G::kBoxCols, y, &full[st]);
         }
       }
     }
   } else {
     // ---------------- consumers
-    // Q^T fragments (B operand of m16n8k16): b0 = Q[n][16k + 2(lane%4) + {0,1}],
-    // b1 = the same 8 columns further, n = lane/4 (zero for n >= g).
+    // Q^T fragments (B operand of m16n8k16), n = lane/4 (zero for n >= g).
+    // bf16: b0 = Q[n][16k + 2(lane%4) + {0,1}], b1 = the same 8 columns on.
+    // FP8 (f16 operands): the contraction index of k-step k is permuted so that
+    // plain ldmatrix rows of the FP8 page line up with it: b0 = Q[n][16k +
+    // 4(lane%4) + {0,1}], b1 = Q[n][16k + 4(lane%4) + {2,3}].
     uint32_t bq[KT][2];
     {
       const int n = lane >> 2;
@@ -196,13 +255,21 @@ __global__ void __launch_bounds__(TcGeom<D, BS, NW, NST>::kThreads)
           p.q + (static_cast<int64_t>(s) * p.num_heads + h * g + n) * D);
 #pragma unroll
       for (int k = 0; k < KT; ++k) {
-        bq[k][0] = n < g ? __ldg(qrow + (k * 16 + (lane & 3) * 2) / 2) : 0u;
-        bq[k][1] = n < g ? __ldg(qrow + (k * 16 + 8 + (lane & 3) * 2) / 2) : 0u;
+        if constexpr (!FP8) {
+          bq[k][0] = n < g ? __ldg(qrow + (k * 16 + (lane & 3) * 2) / 2) : 0u;
+          bq[k][1] = n < g ? __ldg(qrow + (k * 16 + 8 + (lane & 3) * 2) / 2) : 0u;
+        } else {
+          const uint32_t w0 = n < g ? __ldg(qrow + (k * 16 + (lane & 3) * 4) / 2) : 0u;
+          const uint32_t w1 = n < g ? __ldg(qrow + (k * 16 + (lane & 3) * 4 + 2) / 2) : 0u;
+          bq[k][0] = pack_f16(bf16lo(w0), bf16hi(w0));
+          bq[k][1] = pack_f16(bf16lo(w1), bf16hi(w1));
+        }
       }
     }
 #pragma unroll
     for (int k = 0; k < KT; ++k) o[k][0] = o[k][1] = o[k][2] = o[k][3] = 0.f;
-    const float qs = p.qscale;
+    float qs = p.qscale;
+    if constexpr (FP8) qs *= p.k_scale[h];
 
     for (int it = warp; it < nblk; it += NW) {
       const int st = it % NST;
@@ -214,8 +281,9 @@ __global__ void __launch_bounds__(TcGeom<D, BS, NW, NST>::kThreads)
         // slots past the context hold whatever was there: zero their V rows so
         // the zero probabilities cannot meet a NaN in the product
         for (int r = ntok; r < BS; ++r)
-          for (int c = lane * 8; c < D; c += 256)
-            asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(swz<BS>(vp, r, c)), "r"(0u)
+          for (int c = lane * 16; c < D * ESZ; c += 512)
+            asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(swz_bytes<BS>(vp, r, c)),
+                         "r"(0u)
                          : "memory");
         __syncwarp();
       }
@@ -224,12 +292,27 @@ __global__ void __launch_bounds__(TcGeom<D, BS, NW, NST>::kThreads)
         // ---- S^T = K_slice . Q^T (two accumulators halve the dependency chain)
         float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
         const int arow = r0 + (lane & 7) + ((lane >> 3) & 1) * 8;
-        const int acol = (lane >> 4) * 8;
+        if constexpr (!FP8) {
+          const int acol = (lane >> 4) * 16;  // bytes
 #pragma unroll
-        for (int k = 0; k < KT; ++k) {
-          uint32_t a0, a1, a2, a3;
-          ldsm_x4(swz<BS>(kp, arow, k * 16 + acol), a0, a1, a2, a3);
-          mma_bf16((k & 1) ? sb : sa, a0, a1, a2, a3, bq[k][0], bq[k][1]);
+          for (int k = 0; k < KT; ++k) {
+            uint32_t a0, a1, a2, a3;
+            ldsm_x4(swz_bytes<BS>(kp, arow, k * 32 + acol), a0, a1, a2, a3);
+            mma_bf16((k & 1) ? sb : sa, a0, a1, a2, a3, bq[k][0], bq[k][1]);
+          }
+        } else {
+          // one x4 load covers 16 rows x 32 codes = two k-steps; each b16 lane
+          // element holds two codes, converted exactly to f16
+          const int acol = (lane >> 4) * 16;
+#pragma unroll
+          for (int k = 0; k < KT; k += 2) {
+            uint32_t m0r, m1r, m2r, m3r;
+            ldsm_x4(swz_bytes<BS>(kp, arow, k * 16 + acol), m0r, m1r, m2r, m3r);
+            mma_f16(sa, e4m3x2_f16x2(m0r, 0), e4m3x2_f16x2(m1r, 0), e4m3x2_f16x2(m0r, 1),
+                    e4m3x2_f16x2(m1r, 1), bq[k][0], bq[k][1]);
+            mma_f16(sb, e4m3x2_f16x2(m2r, 0), e4m3x2_f16x2(m3r, 0), e4m3x2_f16x2(m2r, 1),
+                    e4m3x2_f16x2(m3r, 1), bq[k + 1][0], bq[k + 1][1]);
+          }
         }
         // ---- online softmax on the fragment: rows = tokens, cols = queries
         const int t0 = r0 + (lane >> 2), t1 = t0 + 8;
@@ -264,23 +347,45 @@ __global__ void __launch_bounds__(TcGeom<D, BS, NW, NST>::kThreads)
         const float p10 = fast_exp2(s10 - m0), p11 = fast_exp2(s11 - m1);
         l0 += p00 + p10;
         l1 += p01 + p11;
-        // ---- P = P_hi + P_lo in bf16, transposed into the B operand
-        const uint32_t hi_t = pack_bf16(p00, p01), hi_b = pack_bf16(p10, p11);
-        const __nv_bfloat162 ht = *reinterpret_cast<const __nv_bfloat162*>(&hi_t);
-        const __nv_bfloat162 hb = *reinterpret_cast<const __nv_bfloat162*>(&hi_b);
-        const uint32_t lo_t = pack_bf16(p00 - __low2float(ht), p01 - __high2float(ht));
-        const uint32_t lo_b = pack_bf16(p10 - __low2float(hb), p11 - __high2float(hb));
-        const uint32_t bh0 = movm_t(hi_t), bh1 = movm_t(hi_b);
-        const uint32_t bl0 = movm_t(lo_t), bl1 = movm_t(lo_b);
-        // ---- O^T += V_slice^T . P^T
         const int vrow = r0 + (lane & 7) + ((lane >> 4) & 1) * 8;
-        const int vcol = ((lane >> 3) & 1) * 8;
+        if constexpr (!FP8) {
+          // ---- P = P_hi + P_lo in bf16, transposed into the B operand
+          const uint32_t hi_t = pack_bf16(p00, p01), hi_b = pack_bf16(p10, p11);
+          const __nv_bfloat162 ht = *reinterpret_cast<const __nv_bfloat162*>(&hi_t);
+          const __nv_bfloat162 hb = *reinterpret_cast<const __nv_bfloat162*>(&hi_b);
+          const uint32_t lo_t = pack_bf16(p00 - __low2float(ht), p01 - __high2float(ht));
+          const uint32_t lo_b = pack_bf16(p10 - __low2float(hb), p11 - __high2float(hb));
+          const uint32_t bh0 = movm_t(hi_t), bh1 = movm_t(hi_b);
+          const uint32_t bl0 = movm_t(lo_t), bl1 = movm_t(lo_b);
+          // ---- O^T += V_slice^T . P^T, V^T fragments by ldmatrix.trans
+          const int vcol = ((lane >> 3) & 1) * 16;  // bytes
 #pragma unroll
-        for (int k = 0; k < KT; ++k) {
-          uint32_t a0, a1, a2, a3;
-          ldsm_x4_t(swz<BS>(vp, vrow, k * 16 + vcol), a0, a1, a2, a3);
-          mma_bf16(o[k], a0, a1, a2, a3, bh0, bh1);
-          mma_bf16(o[k], a0, a1, a2, a3, bl0, bl1);
+          for (int k = 0; k < KT; ++k) {
+            uint32_t a0, a1, a2, a3;
+            ldsm_x4_t(swz_bytes<BS>(vp, vrow, k * 32 + vcol), a0, a1, a2, a3);
+            mma_bf16(o[k], a0, a1, a2, a3, bh0, bh1);
+            mma_bf16(o[k], a0, a1, a2, a3, bl0, bl1);
+          }
+        } else {
+          // ---- P in f16 (11-bit mantissa), transposed into the B operand
+          const uint32_t b0 = movm_t(pack_f16(p00, p01)), b1 = movm_t(pack_f16(p10, p11));
+          // ---- O^T += V_slice^T . P^T. A plain x4 load gives rows = tokens,
+          // 16 codes per 8x8 b16 matrix (tokens 0-7 / 8-15, columns 16m / 16m+16);
+          // converting a lane's 4 codes gives two 8x8 f16 fragments (columns
+          // 4c+{0,1} and 4c+{2,3}); movmatrix transposes each into an A-operand
+          // piece whose rows are those head-dim offsets (see fp8_row_offset).
+          const int vrow2 = r0 + (lane & 7) + ((lane >> 3) & 1) * 8;
+          const int vcol = (lane >> 4) * 16;
+#pragma unroll
+          for (int k = 0; k < KT; k += 2) {
+            uint32_t m0r, m1r, m2r, m3r;
+            ldsm_x4(swz_bytes<BS>(vp, vrow2, k * 16 + vcol), m0r, m1r, m2r, m3r);
+            mma_f16(o[k], movm_t(e4m3x2_f16x2(m0r, 0)), movm_t(e4m3x2_f16x2(m0r, 1)),
+                    movm_t(e4m3x2_f16x2(m1r, 0)), movm_t(e4m3x2_f16x2(m1r, 1)), b0, b1);
+            mma_f16(o[k + 1], movm_t(e4m3x2_f16x2(m2r, 0)), movm_t(e4m3x2_f16x2(m2r, 1)),
+                    movm_t(e4m3x2_f16x2(m3r, 0)), movm_t(e4m3x2_f16x2(m3r, 1)), b0, b1);
+          }
+          (void)vrow;
         }
       }
       if (ntok < BS) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -310,13 +415,15 @@ __global__ void __launch_bounds__(TcGeom<D, BS, NW, NST>::kThreads)
   float* ml = mm + NW * 8;              // [NW][8]
   if (warp < NW) {
     const int q0 = (lane & 3) * 2;
-    const int d0 = lane >> 2;
+    // head-dim offsets of the two accumulator rows this lane holds
+    const int r_lo = FP8 ? fp8_row_offset(lane >> 2) : (lane >> 2);
+    const int r_hi = FP8 ? fp8_row_offset((lane >> 2) + 8) : (lane >> 2) + 8;
 #pragma unroll
     for (int k = 0; k < KT; ++k) {
-      mo[(warp * 8 + q0) * D + k * 16 + d0] = o[k][0];
-      mo[(warp * 8 + q0 + 1) * D + k * 16 + d0] = o[k][1];
-      mo[(warp * 8 + q0) * D + k * 16 + d0 + 8] = o[k][2];
-      mo[(warp * 8 + q0 + 1) * D + k * 16 + d0 + 8] = o[k][3];
+      mo[(warp * 8 + q0) * D + k * 16 + r_lo] = o[k][0];
+      mo[(warp * 8 + q0 + 1) * D + k * 16 + r_lo] = o[k][1];
+      mo[(warp * 8 + q0) * D + k * 16 + r_hi] = o[k][2];
+      mo[(warp * 8 + q0 + 1) * D + k * 16 + r_hi] = o[k][3];
     }
     if (lane < 4) {
       mm[warp * 8 + q0] = m0;
@@ -326,6 +433,60 @@ __global__ void __launch_bounds__(TcGeom<D, BS, NW, NST>::kThreads)
     }
   }
   __syncthreads();
+  const float vsc = FP8 ? p.v_scale[h] : 1.f;
+  if (p.cluster > 1) {
+    // ---- CTA state (max, sum, unnormalised output per query), then the
+    // cluster merges: rank r combines the head-dim slice [r*D/C, (r+1)*D/C)
+    // of every rank's state, read through distributed shared memory, in rank
+    // order.
+    float* cs_o = mm + 2 * NW * 8;  // [8][D]
+    float* cs_m = cs_o + 8 * D;     // [8]
+    float* cs_l = cs_m + 8;         // [8]
+    for (int idx = threadIdx.x; idx < g * D; idx += G::kThreads) {
+      const int j = idx / D;
+      const int c = idx % D;
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < NW; ++w) M = fmaxf(M, mm[w * 8 + j]);
+      float L = 0.f, O = 0.f;
+      if (M != -INFINITY) {
+#pragma unroll
+        for (int w = 0; w < NW; ++w) {
+          const float a = fast_exp2(mm[w * 8 + j] - M);
+          L = fmaf(ml[w * 8 + j], a, L);
+          O = fmaf(mo[(w * 8 + j) * D + c], a, O);
+        }
+      }
+      cs_o[j * D + c] = O;
+      if (c == 0) {
+        cs_m[j] = M;
+        cs_l[j] = L;
+      }
+    }
+    cluster_sync_all();
+    const int C = p.cluster;
+    const int SL = D / C;
+    const uint32_t o_addr = smem_addr(cs_o), m_addr = smem_addr(cs_m), l_addr = smem_addr(cs_l);
+    for (int idx = threadIdx.x; idx < g * SL; idx += G::kThreads) {
+      const int j = idx / SL;
+      const int c = part * SL + idx % SL;
+      float M = -INFINITY;
+      for (int r = 0; r < C; ++r) M = fmaxf(M, ld_dsmem(m_addr + 4 * j, r));
+      float L = 0.f, O = 0.f;
+      if (M != -INFINITY) {
+        for (int r = 0; r < C; ++r) {
+          const float a = fast_exp2(ld_dsmem(m_addr + 4 * j, r) - M);
+          L = fmaf(ld_dsmem(l_addr + 4 * j, r), a, L);
+          O = fmaf(ld_dsmem(o_addr + 4 * (j * D + c), r), a, O);
+        }
+      }
+      const float res = L > 0.f ? (O / L) * vsc : 0.f;
+      const int64_t hq = static_cast<int64_t>(s) * p.num_heads + h * g + j;
+      p.out[hq * D + c] = float_to_bf16_bits(res);
+    }
+    cluster_sync_all();  // keep this CTA's state alive until every rank has read it
+    return;
+  }
   for (int idx = threadIdx.x; idx < g * D; idx += G::kThreads) {
     const int j = idx / D;
     const int c = idx % D;
@@ -341,7 +502,7 @@ __global__ void __launch_bounds__(TcGeom<D, BS, NW, NST>::kThreads)
         O = fmaf(mo[(w * 8 + j) * D + c], a, O);
       }
     }
-    const float res = L > 0.f ? O / L : 0.f;
+    const float res = L > 0.f ? (O / L) * vsc : 0.f;
     const int64_t hq = static_cast<int64_t>(s) * p.num_heads + h * g + j;
     if (p.partition_blocks == 0) {
       p.out[hq * D + c] = float_to_bf16_bits(res);
@@ -371,13 +532,16 @@ static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-// Tensor map of one pool viewed as a 2-D array [rows = NB*Hk*B][D] of bf16,
-// box = 64 columns x B rows, 128-byte swizzle. Encodings are cached.
-static int pool_tensor_map(CUtensorMap* out, const void* base, int64_t rows, int D, int BS) {
+// Tensor map of one pool viewed as a 2-D array [rows = NB*Hk*B][D] of bf16
+// or bytes (E4M3), box = 128 bytes x B rows, 128-byte swizzle. Encodings are
+// cached per (pointer, shape).
+static int pool_tensor_map(CUtensorMap* out, const void* base, int64_t rows, int D, int BS,
+                           bool fp8) {
   struct Entry {
     const void* base;
     int64_t rows;
     int d, bs;
+    bool fp8;
     CUtensorMap map;
   };
   static std::mutex mu;
@@ -386,55 +550,107 @@ static int pool_tensor_map(CUtensorMap* out, const void* base, int64_t rows, int
   {
     std::lock_guard<std::mutex> lock(mu);
     for (int i = 0; i < used; ++i)
-      if (cache[i].base == base && cache[i].rows == rows && cache[i].d == D && cache[i].bs == BS) {
+      if (cache[i].base == base && cache[i].rows == rows && cache[i].d == D &&
+          cache[i].bs == BS && cache[i].fp8 == fp8) {
         *out = cache[i].map;
         return PKV_OK;
       }
   }
   auto enc = tensor_map_encoder();
   if (!enc) return PKV_ERR_CUDA;
+  const int esz = fp8 ? 1 : 2;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(rows)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(D) * 2};
-  cuuint32_t box[2] = {64u, static_cast<cuuint32_t>(BS)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(D) * esz};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / esz), static_cast<cuuint32_t>(BS)};
   cuuint32_t estr[2] = {1u, 1u};
   CUtensorMap m;
-  CUresult r = enc(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
-                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+  CUresult r = enc(&m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                   const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return PKV_ERR_CUDA;
   std::lock_guard<std::mutex> lock(mu);
   Entry& e = cache[next];
-  e = Entry{base, rows, D, BS, m};
+  e = Entry{base, rows, D, BS, fp8, m};
   next = (next + 1) % 32;
   if (used < 32) ++used;
   *out = m;
   return PKV_OK;
 }
 
-template <int D, int BS, int NW, int NST>
-static int launch_tc(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
+template <int D, int BS, bool FP8, int NW, int NST>
+static int launch_tc(const DecodeParams& p_in, const CUtensorMap& tk, const CUtensorMap& tv,
                      dim3 grid, cudaStream_t st) {
-  using G = TcGeom<D, BS, NW, NST>;
+  using G = TcGeom<D, BS, FP8, NW, NST>;
   static bool done[64] = {false};
-  auto kern = decode_tc_kernel<D, BS, NW, NST>;
+  auto kern = decode_tc_kernel<D, BS, FP8, NW, NST>;
   int rc = ensure_smem(kern, G::kSmem, done, 64);
   if (rc != PKV_OK) return rc;
-  kern<<<grid, G::kThreads, G::kSmem, st>>>(tk, tv, p);
+  DecodeParams p = p_in;
+  if (p.partition_blocks > 0 || p.cluster <= 1) {
+    p.cluster = 1;
+    kern<<<grid, G::kThreads, G::kSmem, st>>>(tk, tv, p);
+    return launch_status();
+  }
+  // One pass: a cluster of C CTAs per (KV head, sequence), C a power of two
+  // <= 16; shrink C if the device cannot co-schedule clusters that large.
+  static bool nonportable[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && !nonportable[dev]) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+        cudaSuccess)
+      return PKV_ERR_CUDA;
+    nonportable[dev] = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cfg.blockDim = dim3(G::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = G::kSmem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  for (int C = p.cluster; C >= 2; C >>= 1) {
+    attr[0].val.clusterDim.x = C;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(C, grid.y, grid.z);
+    int nclusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&nclusters, kern, &cfg) != cudaSuccess) {
+      (void)cudaGetLastError();
+      nclusters = 0;
+    }
+    if (nclusters < 1) continue;
+    p.cluster = C;
+    if (cudaLaunchKernelEx(&cfg, kern, tk, tv, p) != cudaSuccess) return PKV_ERR_CUDA;
+    return launch_status();
+  }
+  p.cluster = 1;
+  kern<<<dim3(1, grid.y, grid.z), G::kThreads, G::kSmem, st>>>(tk, tv, p);
   return launch_status();
 }
 
+template <bool FP8>
+static int dispatch_tc(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
+                       int head_dim, int block_size, dim3 grid, cudaStream_t st) {
+  // (consumer warps, ring stages): about 64-128 KB of stages per CTA
+  if (head_dim == 256 && block_size == 16) return launch_tc<256, 16, FP8, 2, 4>(p, tk, tv, grid, st);
+  if (head_dim == 256 && block_size == 32) return launch_tc<256, 32, FP8, 2, FP8 ? 4 : 2>(p, tk, tv, grid, st);
+  if (head_dim == 128 && block_size == 16) return launch_tc<128, 16, FP8, 4, 8>(p, tk, tv, grid, st);
+  return launch_tc<128, 32, FP8, 2, 4>(p, tk, tv, grid, st);
+}
+
 int launch_decode_tc(const DecodeParams& p, const void* k_cache, const void* v_cache,
-                     int head_dim, int block_size, dim3 grid, cudaStream_t st) {
+                     int head_dim, int block_size, bool fp8, dim3 grid, cudaStream_t st) {
   const int64_t rows = static_cast<int64_t>(p.num_blocks) * p.num_kv_heads * block_size;
   CUtensorMap tk, tv;
-  int rc = pool_tensor_map(&tk, k_cache, rows, head_dim, block_size);
+  int rc = pool_tensor_map(&tk, k_cache, rows, head_dim, block_size, fp8);
   if (rc != PKV_OK) return rc;
-  rc = pool_tensor_map(&tv, v_cache, rows, head_dim, block_size);
+  rc = pool_tensor_map(&tv, v_cache, rows, head_dim, block_size, fp8);
   if (rc != PKV_OK) return rc;
-  if (head_dim == 256 && block_size == 16) return launch_tc<256, 16, 2, 4>(p, tk, tv, grid, st);
-  if (head_dim == 256 && block_size == 32) return launch_tc<256, 32, 2, 2>(p, tk, tv, grid, st);
-  if (head_dim == 128 && block_size == 16) return launch_tc<128, 16, 4, 8>(p, tk, tv, grid, st);
-  return launch_tc<128, 32, 2, 4>(p, tk, tv, grid, st);
+  return fp8 ? dispatch_tc<true>(p, tk, tv, head_dim, block_size, grid, st)
+             : dispatch_tc<false>(p, tk, tv, head_dim, block_size, grid, st);
 }
 
 }  // namespace pkv

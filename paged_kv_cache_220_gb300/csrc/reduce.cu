@@ -2,28 +2,38 @@
 //
 // With m_p, l_p, o_p the partition's max logit, exp-sum and normalised output,
 // M = max_p m_p and w_p = l_p * exp(m_p - M), the full softmax output is
-// sum_p (w_p / sum_q w_q) o_p. One CTA per (query head, sequence); thread c4
-// owns four consecutive output elements and reads the partials with 16-byte
-// loads. The weights are computed once per CTA into shared memory.
+// sum_p (w_p / sum_q w_q) o_p.
+//
+// One CTA of 16 warps per (query head, sequence). The weights are computed
+// once into shared memory (block-wide max and sum in a fixed tree order), then
+// warp w accumulates the partitions p = w, w + 16, ... with 16-byte loads,
+// four partitions in flight per lane, and the 16 warp sums are added in warp
+// order. Normalising the weights before the products makes a single partition
+// reproduce its output exactly. The work is HBM-bound: (d + 2) * 4 bytes per
+// partition read, d * 2 bytes written.
 #include "common.cuh"
 #include "host_util.h"
 
 namespace pkv {
 
 constexpr float kLog2eR = 1.4426950408889634f;
+constexpr int kReduceWarps = 16;
+constexpr int kReduceThreads = kReduceWarps * 32;
 
 template <int D>
-__global__ void __launch_bounds__(D / 4) reduce_kernel(
+__global__ void __launch_bounds__(kReduceThreads) reduce_kernel(
     uint16_t* __restrict__ out, const float* __restrict__ tmp_out,
     const float* __restrict__ max_logits, const float* __restrict__ exp_sums,
     const int32_t* __restrict__ context_lens, int num_heads, int np_max, int partition_size,
     int* err) {
-  extern __shared__ float wsh[];  // [np_max] weights
-  __shared__ float red[D / 4];
+  constexpr int V4 = D / 128;  // float4 per lane per partition row
+  extern __shared__ float wsh[];  // [np_max] normalised weights
+  __shared__ float red[kReduceWarps];
+  __shared__ float4 acc_sh[kReduceWarps][D / 4];
   const int j = blockIdx.x;
   const int s = blockIdx.y;
   const int tid = threadIdx.x;
-  constexpr int NT = D / 4;
+  const int warp = tid >> 5, lane = tid & 31;
   int ctx = context_lens[s];
   int np = ctx > 0 ? (ctx + partition_size - 1) / partition_size : 0;
   if (np > np_max) {
@@ -31,51 +41,98 @@ __global__ void __launch_bounds__(D / 4) reduce_kernel(
     np = np_max;
   }
   const int64_t row = static_cast<int64_t>(s) * num_heads + j;
-  uint2* dst = reinterpret_cast<uint2*>(out + row * D) + tid;
   if (np == 0) {
-    *dst = make_uint2(0u, 0u);
+    if (tid < D / 4) reinterpret_cast<uint2*>(out + row * D)[tid] = make_uint2(0u, 0u);
     return;
   }
   const float* ml = max_logits + row * np_max;
   const float* es = exp_sums + row * np_max;
-  // M = max over partitions (block reduction)
+
+  // M = max_p m_p
   float M = -INFINITY;
-  for (int i = tid; i < np; i += NT) M = fmaxf(M, ml[i]);
-  red[tid] = M;
+  for (int i = tid; i < np; i += kReduceThreads) M = fmaxf(M, ml[i]);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  if (lane == 0) red[warp] = M;
   __syncthreads();
-  for (int w = NT / 2; w > 0; w >>= 1) {
-    if (tid < w) red[tid] = fmaxf(red[tid], red[tid + w]);
-    __syncthreads();
-  }
   M = red[0];
+#pragma unroll
+  for (int w = 1; w < kReduceWarps; ++w) M = fmaxf(M, red[w]);
   __syncthreads();
+  // W = sum_p w_p (fixed tree: lanes by xor, then warps in order)
   float W = 0.f;
-  for (int i = tid; i < np; i += NT) {
+  for (int i = tid; i < np; i += kReduceThreads) {
     const float w = es[i] * fast_exp2((ml[i] - M) * kLog2eR);
     wsh[i] = w;
     W += w;
   }
-  red[tid] = W;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) W += __shfl_xor_sync(0xffffffffu, W, off);
+  if (lane == 0) red[warp] = W;
   __syncthreads();
-  // fixed-shape tree: the sum does not depend on timing
-  for (int w = NT / 2; w > 0; w >>= 1) {
-    if (tid < w) red[tid] += red[tid + w];
-    __syncthreads();
+  W = 0.f;
+#pragma unroll
+  for (int w = 0; w < kReduceWarps; ++w) W += red[w];
+  for (int i = tid; i < np; i += kReduceThreads) wsh[i] = wsh[i] / W;
+  __syncthreads();
+
+  // sum_p r_p o_p: warp w takes p = w, w + 16, ...; lane owns float4 columns
+  // lane + 32 v (v < V4)
+  const float4* src = reinterpret_cast<const float4*>(tmp_out + row * np_max * D);
+  float4 acc[V4];
+#pragma unroll
+  for (int v = 0; v < V4; ++v) acc[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+  constexpr int U = 4;
+  int i = warp;
+  for (; i + (U - 1) * kReduceWarps < np; i += U * kReduceWarps) {
+    float4 x[U][V4];
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+#pragma unroll
+      for (int v = 0; v < V4; ++v)
+        x[u][v] = src[static_cast<int64_t>(i + u * kReduceWarps) * (D / 4) + lane + 32 * v];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const float r = wsh[i + u * kReduceWarps];
+#pragma unroll
+      for (int v = 0; v < V4; ++v) {
+        acc[v].x = fmaf(r, x[u][v].x, acc[v].x);
+        acc[v].y = fmaf(r, x[u][v].y, acc[v].y);
+        acc[v].z = fmaf(r, x[u][v].z, acc[v].z);
+        acc[v].w = fmaf(r, x[u][v].w, acc[v].w);
+      }
+    }
   }
-  W = red[0];
-  const float4* src = reinterpret_cast<const float4*>(tmp_out + row * np_max * D) + tid;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int i = 0; i < np; ++i) {
-    const float r = wsh[i] / W;
-    const float4 v = src[static_cast<int64_t>(i) * (D / 4)];
-    acc.x = fmaf(r, v.x, acc.x);
-    acc.y = fmaf(r, v.y, acc.y);
-    acc.z = fmaf(r, v.z, acc.z);
-    acc.w = fmaf(r, v.w, acc.w);
+  for (; i < np; i += kReduceWarps) {
+    const float r = wsh[i];
+#pragma unroll
+    for (int v = 0; v < V4; ++v) {
+      const float4 x = src[static_cast<int64_t>(i) * (D / 4) + lane + 32 * v];
+      acc[v].x = fmaf(r, x.x, acc[v].x);
+      acc[v].y = fmaf(r, x.y, acc[v].y);
+      acc[v].z = fmaf(r, x.z, acc[v].z);
+      acc[v].w = fmaf(r, x.w, acc[v].w);
+    }
   }
-  const uint32_t lo = float_to_bf16_bits(acc.x) | (static_cast<uint32_t>(float_to_bf16_bits(acc.y)) << 16);
-  const uint32_t hi = float_to_bf16_bits(acc.z) | (static_cast<uint32_t>(float_to_bf16_bits(acc.w)) << 16);
-  *dst = make_uint2(lo, hi);
+#pragma unroll
+  for (int v = 0; v < V4; ++v) acc_sh[warp][lane + 32 * v] = acc[v];
+  __syncthreads();
+  if (tid < D / 4) {
+    float4 a = acc_sh[0][tid];
+#pragma unroll
+    for (int w = 1; w < kReduceWarps; ++w) {
+      const float4 b = acc_sh[w][tid];
+      a.x += b.x;
+      a.y += b.y;
+      a.z += b.z;
+      a.w += b.w;
+    }
+    const uint32_t lo = float_to_bf16_bits(a.x) |
+                        (static_cast<uint32_t>(float_to_bf16_bits(a.y)) << 16);
+    const uint32_t hi = float_to_bf16_bits(a.z) |
+                        (static_cast<uint32_t>(float_to_bf16_bits(a.w)) << 16);
+    reinterpret_cast<uint2*>(out + row * D)[tid] = make_uint2(lo, hi);
+  }
 }
 
 }  // namespace pkv
@@ -98,7 +155,7 @@ extern "C" int pkv_paged_attention_reduce(void* out, const void* workspace,
   if (max_context > 0 && (!workspace || !aligned16(workspace) || workspace_bytes < need))
     return PKV_ERR_INVALID_ARG;
   const size_t smem = static_cast<size_t>(np) * sizeof(float);
-  constexpr size_t kMaxSmem = 200 * 1024;
+  constexpr size_t kMaxSmem = 160 * 1024;  // plus the static accumulators
   if (smem > kMaxSmem) return PKV_ERR_UNSUPPORTED;
   // With every context empty no partial is read (np_max = 0 makes the kernel
   // write zeros), so the workspace may be absent.
@@ -114,16 +171,16 @@ extern "C" int pkv_paged_attention_reduce(void* out, const void* workspace,
     static bool done[64] = {false};
     int rc = ensure_smem(reduce_kernel<128>, kMaxSmem, done, 64);
     if (rc != PKV_OK) return rc;
-    reduce_kernel<128><<<grid, 32, smem, st>>>(static_cast<uint16_t*>(out), tmp, ml, es,
-                                               context_lens, num_heads, np_arg, partition_size,
-                                               device_error_ptr());
+    reduce_kernel<128><<<grid, kReduceThreads, smem, st>>>(
+        static_cast<uint16_t*>(out), tmp, ml, es, context_lens, num_heads, np_arg,
+        partition_size, device_error_ptr());
   } else {
     static bool done[64] = {false};
     int rc = ensure_smem(reduce_kernel<256>, kMaxSmem, done, 64);
     if (rc != PKV_OK) return rc;
-    reduce_kernel<256><<<grid, 64, smem, st>>>(static_cast<uint16_t*>(out), tmp, ml, es,
-                                               context_lens, num_heads, np_arg, partition_size,
-                                               device_error_ptr());
+    reduce_kernel<256><<<grid, kReduceThreads, smem, st>>>(
+        static_cast<uint16_t*>(out), tmp, ml, es, context_lens, num_heads, np_arg,
+        partition_size, device_error_ptr());
   }
   return launch_status();
 }

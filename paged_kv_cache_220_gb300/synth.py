@@ -205,9 +205,10 @@ def tiny(seed: int = 1001) -> Workload:
 
 
 def qwen_like(seed: int = 1002, layers: int = 16, num_seqs: int = 64,
-              ctx: int = 8192, partition_size: int = 512) -> Workload:
+              ctx: int = 8192, partition_size: int = 1024) -> Workload:
     """16 layers back to back, 64 sequences at 8192 tokens, 24 query / 4 KV
-    heads, d=256, B=16, pool exactly fits (0.5 GiB of KV per sequence)."""
+    heads, d=256, B=16, pool exactly fits (0.5 GiB of KV per sequence).
+    Split decode in 1024-token partitions (2048 CTAs per layer)."""
     return Workload("qwen_like_gqa_decode", seed, 24, 4, 256, 16, [ctx] * num_seqs,
                     layers=layers, partition_size=partition_size)
 

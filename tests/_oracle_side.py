@@ -30,21 +30,9 @@ def host_rows(w: synth.Workload, layer: int, s: int, t1: int = None):
             w.rows(synth.KIND_V, layer, s, 0, t1, "cpu"))
 
 
-_ALL_BF16 = (np.arange(65536, dtype=np.uint32) << 16).view(np.float32)
-
-
 def quantize(rows_bf16: torch.Tensor, scale: np.ndarray) -> np.ndarray:
-    """E4M3 codes of x / scale[h] (fp32 quotient) with the oracle's encoder.
-    The encoder is a pure function of the bf16 input and the head's scale, so
-    it is evaluated once on all 65,536 bf16 patterns per head and looked up."""
-    bits = bits16(rows_bf16)
-    out = np.empty(bits.shape, dtype=np.uint8)
-    for h in range(bits.shape[1]):
-        with np.errstate(over="ignore", invalid="ignore"):
-            y = (_ALL_BF16 / np.float32(scale[h])).astype(np.float32)
-        lut = oracle.e4m3_encode(y)
-        out[:, h, :] = lut[bits[:, h, :]]
-    return out
+    """E4M3 codes of x / scale[h] (fp32 quotient) with the oracle's encoder."""
+    return oracle.e4m3_encode_bf16(bits16(rows_bf16), scale)
 
 
 def expected(w: synth.Workload, layer: int, seqs, k_scale=None, v_scale=None) -> np.ndarray:

@@ -352,3 +352,16 @@ def test_planted_oracle_mistakes_are_caught(mutation):
     finally:
         oracle.set_mutation(0)
     assert any(caught), "planted mistake %d slipped through every pin" % mutation
+
+
+def test_e4m3_table_encoder_equals_direct_encoder():
+    """The per-head lookup form of the encoder is the same function."""
+    rng = np.random.default_rng(21)
+    bits = rng.integers(0, 65536, (50, 3, 16)).astype(np.uint16)
+    x = (bits.astype(np.uint32) << 16).view(np.float32)
+    bits[~np.isfinite(x)] = 0
+    x = (bits.astype(np.uint32) << 16).view(np.float32)
+    sc = np.array([0.013, 1.0, 7.5], dtype=np.float32)
+    with np.errstate(over="ignore"):
+        direct = oracle.e4m3_encode((x / sc[None, :, None]).astype(np.float32))
+    assert np.array_equal(oracle.e4m3_encode_bf16(bits, sc), direct)
