@@ -235,6 +235,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--graph", type=int, default=1,
+                    help="1: the timed steps replay a CUDA graph of the step (default)")
     ap.add_argument("--layers", type=int, default=0,
                     help="override the layer count (profiling of a smaller case)")
     ap.add_argument("--seqs", type=int, default=0,
@@ -307,8 +309,6 @@ def main():
 
     def one_step(ev=None):
         for layer, st in enumerate(pw.layers):
-            if cow is not None:
-                pkv.copy_blocks(st.k_cache, st.v_cache, cow)
             pkv.kv_cache_write(st.k_new, st.v_new, pw.slot_mapping, st.k_cache, st.v_cache,
                                st.k_scale, st.v_scale)
             if ev is not None:
@@ -321,7 +321,7 @@ def main():
             if P:
                 pkv.paged_attention_reduce(out[layer], ws, pw.context_lens, pw.max_context, P)
 
-    launches_per_step = L * (2 + (1 if P else 0) + (1 if cow is not None else 0))
+    launches_per_step = L * (2 + (1 if P else 0))
     for _ in range(args.warmup):
         one_step()
     torch.cuda.synchronize()
@@ -330,6 +330,28 @@ def main():
     evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(L)]
            for _ in range(K)]
     step_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+    # (1) eager steps with events around every decode launch: the roofline of
+    # the decode kernel, measured live on the launching stream
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    for i in range(K):
+        if flush is not None:
+            flush.fill_(i & 0xFF)
+        step_ev[i][0].record(stream)
+        one_step(evs[i])
+        step_ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    eager_ms = sum(a.elapsed_time(b) for a, b in step_ev)
+    dec_ms = [evs[i][l][0].elapsed_time(evs[i][l][1]) for i in range(K) for l in range(L)]
+    dec_avg_ms = sum(dec_ms) / len(dec_ms)
+    # (2) the timed steps: replays of a CUDA graph of the whole step (one host
+    # dispatch per step), or eager launches with --graph 0
+    graph = None
+    if args.graph:
+        graph = workload.capture_step(pw, out, ws, P)
+        for _ in range(args.warmup):
+            graph.replay()
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
@@ -338,21 +360,29 @@ def main():
             if flush is not None:
                 flush.fill_(i & 0xFF)
             step_ev[i][0].record(stream)
-            one_step(evs[i])
+            if graph is not None:
+                graph.replay()
+            else:
+                one_step()
             step_ev[i][1].record(stream)
         torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()
     step_ms = [a.elapsed_time(b) for a, b in step_ev]
     total_ms = sum(step_ms)
-    dec_ms = [evs[i][l][0].elapsed_time(evs[i][l][1]) for i in range(K) for l in range(L)]
-    dec_avg_ms = sum(dec_ms) / len(dec_ms)
     if dist is not None:
         t = torch.tensor([total_ms], device="cuda")
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         total_ms = float(t.item())
     ms_per_step = total_ms / K
     value = per_step_bytes * world / (ms_per_step / 1e3) / 1e9
+
+    # copy-on-write copies of the divergence iteration, timed on a scratch
+    # pool with the same block geometry (replaying them on the live pool would
+    # overwrite the tokens the clones received after the divergence)
+    cow_copy = None
+    if cow is not None and len(pw.cow_pairs_host):
+        cow_copy = time_copy_blocks(pw, args)
 
     # end to end through the public API with host buffers
     e2e = None
@@ -387,7 +417,9 @@ def main():
             "l2": "flushed before every step" if flush is not None else
                   "inputs larger than L2 (%.1f GB of K/V per step)" % (per_step_bytes / 1e9),
             "parallelism": "replicas/weak: each GPU its own batch" if world > 1 else "1 GPU",
+            "cuda_graph": bool(graph is not None),
         },
+        "eager_ms_per_step": round(eager_ms / K, 4),
         "pct_of_peak": round(100 * value / world / peak, 2),
         "tokens_per_s_per_layer": round(tok_per_s_layer, 1),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
@@ -395,7 +427,7 @@ def main():
                      "peak_kind": peak_kind, "kernel": "paged_attention_decode",
                      "bytes_per_launch": dec_bytes, "launch_ms": round(dec_avg_ms, 5),
                      "traffic": traffic},
-        "cpu_baseline": cpu, "e2e": e2e,
+        "cpu_baseline": cpu, "e2e": e2e, "copy_blocks": cow_copy,
         "gpu_launches": launches_per_step * K,
         "clocks": clk.summary(),
     }
@@ -405,6 +437,37 @@ def main():
     if dist is not None:
         dist.destroy_process_group()
     return 0
+
+
+def time_copy_blocks(pw, args):
+    """copy_blocks over the workload's divergence pairs (e.g. 480 for the
+    2040-token prompts), remapped into a scratch pool of 2 x pairs blocks."""
+    import torch
+    import paged_kv_cache_220_gb300 as pkv
+    n = len(pw.cow_pairs_host)
+    st = pw.layers[0]
+    shape = (2 * n,) + tuple(st.k_cache.shape[1:])
+    kc = torch.empty(shape, dtype=st.k_cache.dtype, device="cuda")
+    vc = torch.empty_like(kc)
+    kc.view(torch.uint8).random_(0, 255)
+    vc.view(torch.uint8).random_(0, 255)
+    perm = torch.randperm(2 * n, generator=torch.Generator().manual_seed(5))
+    pairs = torch.stack([perm[:n], perm[n:]], dim=1).to(torch.int32).cuda()
+    for _ in range(3):
+        pkv.copy_blocks(kc, vc, pairs)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    K = max(10, args.steps)
+    torch.cuda.synchronize()
+    a.record()
+    for _ in range(K):
+        pkv.copy_blocks(kc, vc, pairs)
+    b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / K
+    block_bytes = kc[0].numel() * kc.element_size()
+    moved = n * block_bytes * 2 * 2          # K and V, read + write
+    return {"pairs": n, "ms": round(ms, 5), "bytes": moved,
+            "gbs": round(moved / (ms / 1e3) / 1e9, 1), "layers": 1}
 
 
 def run_e2e(args, pw, w, out, ws, P, per_step_bytes, world, dist):

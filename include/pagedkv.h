@@ -235,6 +235,30 @@ int pkv_paged_attention_decode_noalloc(void* out, const void* q, const void* k_c
                                        int num_heads, int max_context, float scale,
                                        int partition_size, void* stream);
 
+/* ------------------------------------------------------------------------ *
+ * swap_out / swap_in: move whole blocks (K and V, all heads) between a pool
+ * and a packed buffer, for preemption by swapping ([Dissect] "Continuous
+ * Batching: Breaking the Sequence Barrier" and "FAQ": a running sequence's
+ * blocks go to CPU RAM, the device blocks are freed, and they come back
+ * later).
+ *
+ *   blocks  : int32 [n] block ids, readable by the device (device memory or
+ *             pinned host memory)
+ *   k_buf, v_buf : [n][num_kv_heads*block_size*head_dim*esz] bytes, block i of
+ *             the list at row i; device memory or pinned host memory the device
+ *             can address (the kernel reads/writes it directly)
+ * swap_out: buf[i] = pool[blocks[i]]; swap_in: pool[blocks[i]] = buf[i]
+ * (byte for byte). The allocator side (freeing a sequence, re-creating it
+ * with fresh blocks on the way back) is the caller's.
+ * Errors: PKV_ERR_INVALID_ARG, PKV_ERR_UNSUPPORTED, PKV_ERR_CUDA; n == 0 is a
+ * no-op. Out-of-range ids are skipped and reported.
+ * ------------------------------------------------------------------------ */
+int pkv_swap_out(const void* k_cache, const void* v_cache, pkv_cache_desc cache,
+                 const int32_t* blocks, int num_blocks_to_move, void* k_buf, void* v_buf,
+                 void* stream);
+int pkv_swap_in(void* k_cache, void* v_cache, pkv_cache_desc cache, const int32_t* blocks,
+                int num_blocks_to_move, const void* k_buf, const void* v_buf, void* stream);
+
 /* Register a device int32 that kernels write a PKV_DEVERR_* code into (first
  * error wins; the caller clears it). NULL switches reporting off; the kernels
  * still skip out-of-range ids. Process-wide; returns PKV_OK. */
@@ -301,6 +325,55 @@ int pkv_block_refcount(const pkv_allocator* a, int block, int* refcount);
  * counted once per physical slot (shared slots count once). */
 int pkv_alloc_stats(const pkv_allocator* a, int* free_blocks, int* used_blocks,
                     long long* used_slots);
+
+/* ------------------------------------------------------------------------ *
+ * Iteration-level (continuous) batching scheduler over an allocator
+ * ([HowVLLM] "Continuous batching removes straggler bubbles"; [Dissect]
+ * "Continuous Batching: Breaking the Sequence Barrier"; [ArchBench]
+ * "Continuous batching and the straggler problem").
+ *
+ * A request is (id, prompt length, token budget); it ends (EOS) when it has
+ * produced max_new_tokens tokens. pkv_sched_step runs one iteration:
+ *   1. eject the requests that produced their last token in the previous
+ *      iteration; their blocks return to the free list at once;
+ *   2. admit waiting requests in arrival order while the batch has fewer than
+ *      max_num_seqs requests and the free blocks cover the prompt and its first
+ *      new token on top of what the running requests need this iteration
+ *      (the prompt slots are reported: the caller stores the prompt's K/V);
+ *   3. give every running request one slot for this iteration's token; if the
+ *      pool runs dry, the most recently admitted request is preempted (freed
+ *      and put back at the head of the queue, to be recomputed).
+ * After a step, the running batch (admission order) is read with
+ * pkv_sched_running / pkv_sched_block_tables; context_len counts the token of
+ * this iteration. The scheduler uses the allocator through its public calls;
+ * neither is thread-safe.
+ * ------------------------------------------------------------------------ */
+typedef struct pkv_scheduler pkv_scheduler;
+
+int pkv_sched_create(pkv_allocator* alloc, int block_size, int max_num_seqs,
+                     pkv_scheduler** out);
+void pkv_sched_destroy(pkv_scheduler* s);
+int pkv_sched_add_request(pkv_scheduler* s, int64_t request_id, int prompt_len,
+                          int max_new_tokens);
+/* One iteration; reports the batch size, the requests admitted in it and
+ * those ejected at its start. */
+int pkv_sched_step(pkv_scheduler* s, int* num_running, int* num_admitted,
+                   int* num_finished);
+/* Running batch: request ids, context lengths and the slot of this
+ * iteration's token, each [cap >= num_running] (any may be NULL). */
+int pkv_sched_running(const pkv_scheduler* s, int64_t* request_ids,
+                      int32_t* context_lens, int64_t* new_slots, int cap);
+/* Block tables of the running batch, [rows >= num_running][max_blocks],
+ * padded with -1. PKV_ERR_INVALID_ARG if a table is longer than max_blocks. */
+int pkv_sched_block_tables(const pkv_scheduler* s, int32_t* tables, int max_blocks,
+                           int rows);
+/* Prompt slots of a request admitted in the last step (n = prompt length). */
+int pkv_sched_prompt_slots(const pkv_scheduler* s, int64_t request_id,
+                           int64_t* slots, int cap, int* n);
+/* Ids of the last step's events: kind 0 admitted, 1 finished, 2 preempted. */
+int pkv_sched_events(const pkv_scheduler* s, int kind, int64_t* ids, int cap, int* n);
+int pkv_sched_counts(const pkv_scheduler* s, int* waiting, int* running,
+                     long long* steps);
 
 #ifdef __cplusplus
 }

@@ -69,6 +69,8 @@ SIGNATURES = {
     "pkv_paged_attention_decode_noalloc": (_I, [_P, _P, _P, _P, CacheDesc, _P, _P, _P, _I, _P,
                                                 _I, _I, _I, ctypes.c_float, _I, _P]),
     "pkv_copy_blocks": (_I, [_P, _P, CacheDesc, _P, _I, _P]),
+    "pkv_swap_out": (_I, [_P, _P, CacheDesc, _P, _I, _P, _P, _P]),
+    "pkv_swap_in": (_I, [_P, _P, CacheDesc, _P, _I, _P, _P, _P]),
     "pkv_set_device_check": (_I, [_P]),
     "pkv_status_string": (ctypes.c_char_p, [_I]),
     "pkv_version": (_I, []),
@@ -83,6 +85,16 @@ SIGNATURES = {
     "pkv_block_refcount": (_I, [_P, _I, ctypes.POINTER(_I)]),
     "pkv_alloc_stats": (_I, [_P, ctypes.POINTER(_I), ctypes.POINTER(_I),
                              ctypes.POINTER(ctypes.c_longlong)]),
+    "pkv_sched_create": (_I, [_P, _I, _I, ctypes.POINTER(_P)]),
+    "pkv_sched_destroy": (None, [_P]),
+    "pkv_sched_add_request": (_I, [_P, ctypes.c_int64, _I, _I]),
+    "pkv_sched_step": (_I, [_P, ctypes.POINTER(_I), ctypes.POINTER(_I), ctypes.POINTER(_I)]),
+    "pkv_sched_running": (_I, [_P, _P, _P, _P, _I]),
+    "pkv_sched_block_tables": (_I, [_P, _P, _I, _I]),
+    "pkv_sched_prompt_slots": (_I, [_P, ctypes.c_int64, _P, _I, ctypes.POINTER(_I)]),
+    "pkv_sched_events": (_I, [_P, _I, _P, _I, ctypes.POINTER(_I)]),
+    "pkv_sched_counts": (_I, [_P, ctypes.POINTER(_I), ctypes.POINTER(_I),
+                              ctypes.POINTER(ctypes.c_longlong)]),
 }
 
 
@@ -264,6 +276,44 @@ def copy_blocks(k_cache, v_cache, block_pairs, stream=None) -> None:
     _check(rc, "copy_blocks")
 
 
+def _any_ptr(t, name):
+    """Pointer of a device tensor or of pinned host memory the device can address."""
+    if not isinstance(t, torch.Tensor) or not t.is_contiguous():
+        raise ValueError("%s must be a contiguous tensor" % name)
+    if not t.is_cuda and not t.is_pinned():
+        raise ValueError("%s must be a CUDA tensor or pinned host memory" % name)
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def swap_out(k_cache, v_cache, blocks, k_buf, v_buf, stream=None) -> None:
+    """k_buf[i] = k_cache[blocks[i]] (and V); buffers device or pinned host,
+    [n, Hk, B, D] like the pool."""
+    desc = cache_desc(k_cache)
+    n = int(blocks.shape[0])
+    if n == 0:
+        return
+    if blocks.dtype != torch.int32 or k_buf.shape[0] < n or k_buf.shape[1:] != k_cache.shape[1:]:
+        raise ValueError("blocks int32 [n]; buffers [>=n, Hk, B, D]")
+    rc = lib().pkv_swap_out(_dev_ptr(k_cache, "k_cache"), _dev_ptr(v_cache, "v_cache"), desc,
+                            _any_ptr(blocks, "blocks"), n, _any_ptr(k_buf, "k_buf"),
+                            _any_ptr(v_buf, "v_buf"), _stream(stream))
+    _check(rc, "swap_out")
+
+
+def swap_in(k_cache, v_cache, blocks, k_buf, v_buf, stream=None) -> None:
+    """k_cache[blocks[i]] = k_buf[i] (and V)."""
+    desc = cache_desc(k_cache)
+    n = int(blocks.shape[0])
+    if n == 0:
+        return
+    if blocks.dtype != torch.int32 or k_buf.shape[0] < n or k_buf.shape[1:] != k_cache.shape[1:]:
+        raise ValueError("blocks int32 [n]; buffers [>=n, Hk, B, D]")
+    rc = lib().pkv_swap_in(_dev_ptr(k_cache, "k_cache"), _dev_ptr(v_cache, "v_cache"), desc,
+                           _any_ptr(blocks, "blocks"), n, _any_ptr(k_buf, "k_buf"),
+                           _any_ptr(v_buf, "v_buf"), _stream(stream))
+    _check(rc, "swap_in")
+
+
 def set_device_check(flag) -> None:
     """Register a 1-element int32 CUDA tensor as the device error word
     (None switches reporting off). Keep the tensor alive while registered."""
@@ -350,3 +400,80 @@ class BlockAllocator:
             t = self.block_table(s)
             out[i, :len(t)] = t
         return out
+
+
+class Scheduler:
+    """Iteration-level batching over a BlockAllocator (see pkv_sched_step)."""
+
+    def __init__(self, alloc: "BlockAllocator", max_num_seqs: int):
+        h = ctypes.c_void_p()
+        _check(lib().pkv_sched_create(alloc._h, alloc.block_size, int(max_num_seqs),
+                                      ctypes.byref(h)), "sched_create")
+        self._h = h
+        self.alloc = alloc  # keeps the allocator alive
+
+    def close(self) -> None:
+        if getattr(self, "_h", None):
+            lib().pkv_sched_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def add_request(self, request_id: int, prompt_len: int, max_new_tokens: int) -> None:
+        _check(lib().pkv_sched_add_request(self._h, int(request_id), int(prompt_len),
+                                           int(max_new_tokens)), "sched_add_request")
+
+    def step(self):
+        """One iteration; returns (num_running, num_admitted, num_finished)."""
+        r, a, f = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+        _check(lib().pkv_sched_step(self._h, ctypes.byref(r), ctypes.byref(a), ctypes.byref(f)),
+               "sched_step")
+        return r.value, a.value, f.value
+
+    def running(self):
+        """(request_ids int64, context_lens int32, new_slots int64) of the batch."""
+        n = self.counts()["running"]
+        ids = np.empty(max(n, 1), np.int64)
+        cl = np.empty(max(n, 1), np.int32)
+        sl = np.empty(max(n, 1), np.int64)
+        _check(lib().pkv_sched_running(self._h, ids.ctypes.data_as(ctypes.c_void_p),
+                                       cl.ctypes.data_as(ctypes.c_void_p),
+                                       sl.ctypes.data_as(ctypes.c_void_p), max(n, 1)),
+               "sched_running")
+        return ids[:n], cl[:n], sl[:n]
+
+    def block_tables(self, max_blocks: int) -> np.ndarray:
+        n = self.counts()["running"]
+        t = np.empty((max(n, 1), max_blocks), np.int32)
+        _check(lib().pkv_sched_block_tables(self._h, t.ctypes.data_as(ctypes.c_void_p),
+                                            int(max_blocks), max(n, 1)), "sched_block_tables")
+        return t[:n]
+
+    def prompt_slots(self, request_id: int) -> np.ndarray:
+        n = ctypes.c_int()
+        rc = lib().pkv_sched_prompt_slots(self._h, int(request_id), None, 0, ctypes.byref(n))
+        if rc not in (PKV_OK, PKV_ERR_INVALID_ARG):
+            _check(rc, "sched_prompt_slots")
+        out = np.empty(max(n.value, 1), np.int64)
+        _check(lib().pkv_sched_prompt_slots(self._h, int(request_id),
+                                            out.ctypes.data_as(ctypes.c_void_p), out.size,
+                                            ctypes.byref(n)), "sched_prompt_slots")
+        return out[:n.value]
+
+    def events(self, kind: int) -> np.ndarray:
+        """kind 0: admitted, 1: finished, 2: preempted (in the last step)."""
+        n = ctypes.c_int()
+        buf = np.empty(4096, np.int64)
+        _check(lib().pkv_sched_events(self._h, int(kind), buf.ctypes.data_as(ctypes.c_void_p),
+                                      buf.size, ctypes.byref(n)), "sched_events")
+        return buf[:n.value].copy()
+
+    def counts(self):
+        w, r, s = ctypes.c_int(), ctypes.c_int(), ctypes.c_longlong()
+        _check(lib().pkv_sched_counts(self._h, ctypes.byref(w), ctypes.byref(r), ctypes.byref(s)),
+               "sched_counts")
+        return {"waiting": w.value, "running": r.value, "steps": s.value}

@@ -611,17 +611,27 @@ static int launch_tc(const DecodeParams& p_in, const CUtensorMap& tk, const CUte
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   attr[0].id = cudaLaunchAttributeClusterDimension;
+  // Largest cluster size <= the requested one that the device can co-schedule
+  // with this kernel's resources, asked once per device and size (so calls
+  // made during stream capture do no occupancy queries).
+  static int8_t fits[64][5] = {};  // 0 unknown, 1 yes, -1 no; index log2(C)
   for (int C = p.cluster; C >= 2; C >>= 1) {
+    int lg = 0;
+    while ((1 << lg) < C) ++lg;
     attr[0].val.clusterDim.x = C;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.gridDim = dim3(C, grid.y, grid.z);
-    int nclusters = 0;
-    if (cudaOccupancyMaxActiveClusters(&nclusters, kern, &cfg) != cudaSuccess) {
-      (void)cudaGetLastError();
-      nclusters = 0;
+    if (dev >= 64 || lg > 4) continue;
+    if (fits[dev][lg] == 0) {
+      int nclusters = 0;
+      if (cudaOccupancyMaxActiveClusters(&nclusters, kern, &cfg) != cudaSuccess) {
+        (void)cudaGetLastError();
+        nclusters = 0;
+      }
+      fits[dev][lg] = nclusters >= 1 ? 1 : -1;
     }
-    if (nclusters < 1) continue;
+    if (fits[dev][lg] < 0) continue;
     p.cluster = C;
     if (cudaLaunchKernelEx(&cfg, kern, tk, tv, p) != cudaSuccess) return PKV_ERR_CUDA;
     return launch_status();

@@ -1,0 +1,257 @@
+// Iteration-level (continuous) batching over the block allocator.
+//
+// Sources: "How vLLM gets real throughput on H100s ...", section "Continuous
+// batching removes straggler bubbles" (scheduling at every forward pass; a
+// sequence that ends returns its blocks at once and a queued request takes
+// its place on the next iteration); "Dissecting vLLM ...", section
+// "Continuous Batching: Breaking the Sequence Barrier" (after each iteration:
+// eject finished sequences, admit waiting requests into the freed room,
+// preempt under memory pressure); "vLLM architecture, memory and benchmarks
+// deep dive", section "Continuous batching and the straggler problem".
+//
+// One call of pkv_sched_step is one iteration:
+//   1. eject: running requests that produced their last token in the previous
+//      iteration are finished and their sequences freed (blocks back to the
+//      free list);
+//   2. admit: waiting requests, first come first served, while the batch has
+//      room (max_num_seqs) and the free blocks cover the prompt plus its first
+//      new token on top of the blocks the running sequences need this
+//      iteration; an admitted request's prompt slots are reported so the
+//      caller can store its K/V (the prefill, outside this library);
+//   3. grow: every running request takes one slot for this iteration's token.
+//      If the pool cannot supply a block, the most recently admitted running
+//      request is preempted: its sequence is freed and it goes back to the
+//      front of the queue to be recomputed from its prompt later.
+// EOS is a request's own token budget (max_new_tokens), known up front.
+#include <algorithm>
+#include <cstdint>
+#include <deque>
+#include <new>
+#include <vector>
+
+#include "../../include/pagedkv.h"
+
+namespace {
+
+struct Req {
+  int64_t id;
+  int prompt_len;
+  int max_new;
+  int generated;  // tokens produced so far (the one of this iteration included)
+  int seq;        // allocator sequence id while running
+  std::vector<int64_t> prompt_slots;  // reported in the admitting iteration
+};
+
+}  // namespace
+
+struct pkv_scheduler {
+  pkv_allocator* alloc = nullptr;
+  int block_size = 0;
+  int max_num_seqs = 0;
+  std::deque<Req> waiting;
+  std::vector<Req> running;                 // admission order
+  std::vector<int64_t> finished;            // ejected in the last step
+  std::vector<int64_t> preempted;           // preempted in the last step
+  std::vector<int64_t> admitted;            // ids admitted in the last step
+  std::vector<int64_t> new_slots;           // per running request, last step
+  int64_t steps = 0;
+};
+
+extern "C" int pkv_sched_create(pkv_allocator* alloc, int block_size, int max_num_seqs,
+                                pkv_scheduler** out) {
+  if (!alloc || !out || block_size <= 0 || max_num_seqs <= 0) return PKV_ERR_INVALID_ARG;
+  pkv_scheduler* s = new (std::nothrow) pkv_scheduler();
+  if (!s) return PKV_ERR_OUT_OF_BLOCKS;
+  s->alloc = alloc;
+  s->block_size = block_size;
+  s->max_num_seqs = max_num_seqs;
+  *out = s;
+  return PKV_OK;
+}
+
+extern "C" void pkv_sched_destroy(pkv_scheduler* s) { delete s; }
+
+extern "C" int pkv_sched_add_request(pkv_scheduler* s, int64_t request_id, int prompt_len,
+                                     int max_new_tokens) {
+  if (!s || prompt_len < 0 || max_new_tokens <= 0) return PKV_ERR_INVALID_ARG;
+  try {
+    s->waiting.push_back(Req{request_id, prompt_len, max_new_tokens, 0, -1, {}});
+  } catch (...) {
+    return PKV_ERR_OUT_OF_BLOCKS;
+  }
+  return PKV_OK;
+}
+
+namespace {
+
+int blocks_for(int64_t tokens, int B) { return static_cast<int>((tokens + B - 1) / B); }
+
+int free_blocks(const pkv_scheduler* s) {
+  int f = 0;
+  pkv_alloc_stats(s->alloc, &f, nullptr, nullptr);
+  return f;
+}
+
+// Blocks the running requests need to grow by one token each.
+int growth_blocks(const pkv_scheduler* s) {
+  int n = 0;
+  for (const Req& r : s->running) {
+    const int64_t len = static_cast<int64_t>(r.prompt_len) + r.generated;
+    if (len % s->block_size == 0) ++n;
+  }
+  return n;
+}
+
+void preempt_last(pkv_scheduler* s) {
+  Req r = std::move(s->running.back());
+  s->running.pop_back();
+  pkv_seq_free(s->alloc, r.seq);
+  s->preempted.push_back(r.id);
+  r.seq = -1;
+  r.generated = 0;  // recomputed from the prompt when it is admitted again
+  r.prompt_slots.clear();
+  s->waiting.push_front(std::move(r));
+}
+
+}  // namespace
+
+extern "C" int pkv_sched_step(pkv_scheduler* s, int* num_running, int* num_admitted,
+                              int* num_finished) {
+  if (!s) return PKV_ERR_INVALID_ARG;
+  try {
+    s->finished.clear();
+    s->preempted.clear();
+    s->admitted.clear();
+    // 1. eject
+    std::vector<Req> keep;
+    keep.reserve(s->running.size());
+    for (Req& r : s->running) {
+      if (r.generated >= r.max_new) {
+        pkv_seq_free(s->alloc, r.seq);
+        s->finished.push_back(r.id);
+      } else {
+        r.prompt_slots.clear();
+        keep.push_back(std::move(r));
+      }
+    }
+    s->running.swap(keep);
+    // 2. admit
+    while (!s->waiting.empty() && static_cast<int>(s->running.size()) < s->max_num_seqs) {
+      Req& w = s->waiting.front();
+      const int need = blocks_for(static_cast<int64_t>(w.prompt_len) + 1, s->block_size);
+      if (need + growth_blocks(s) > free_blocks(s)) break;
+      Req r = std::move(w);
+      s->waiting.pop_front();
+      int sid = -1;
+      int rc = pkv_seq_new(s->alloc, &sid);
+      if (rc != PKV_OK) return rc;
+      r.seq = sid;
+      r.generated = 0;
+      r.prompt_slots.assign(r.prompt_len, -1);
+      if (r.prompt_len > 0) {
+        rc = pkv_seq_append(s->alloc, sid, r.prompt_len, r.prompt_slots.data(), nullptr, nullptr);
+        if (rc != PKV_OK) {
+          pkv_seq_free(s->alloc, sid);
+          return rc;
+        }
+      }
+      s->admitted.push_back(r.id);
+      s->running.push_back(std::move(r));
+    }
+    // 3. grow by one token each; preempt the newest on exhaustion
+    s->new_slots.clear();
+    for (size_t i = 0; i < s->running.size();) {
+      Req& r = s->running[i];
+      int64_t slot = -1;
+      const int rc = pkv_seq_append(s->alloc, r.seq, 1, &slot, nullptr, nullptr);
+      if (rc == PKV_OK) {
+        ++r.generated;
+        s->new_slots.push_back(slot);
+        ++i;
+        continue;
+      }
+      if (rc != PKV_ERR_OUT_OF_BLOCKS) return rc;
+      // the request being grown may itself be the newest one
+      const bool self = (i + 1 == s->running.size());
+      preempt_last(s);
+      if (self) break;
+    }
+    // a preempted request may have been admitted in this very step
+    std::vector<int64_t> adm;
+    for (int64_t id : s->admitted)
+      for (const Req& r : s->running)
+        if (r.id == id) adm.push_back(id);
+    s->admitted.swap(adm);
+  } catch (...) {
+    return PKV_ERR_OUT_OF_BLOCKS;
+  }
+  ++s->steps;
+  if (num_running) *num_running = static_cast<int>(s->running.size());
+  if (num_admitted) *num_admitted = static_cast<int>(s->admitted.size());
+  if (num_finished) *num_finished = static_cast<int>(s->finished.size());
+  return PKV_OK;
+}
+
+extern "C" int pkv_sched_running(const pkv_scheduler* s, int64_t* request_ids,
+                                 int32_t* context_lens, int64_t* new_slots, int cap) {
+  if (!s) return PKV_ERR_INVALID_ARG;
+  const int n = static_cast<int>(s->running.size());
+  if (cap < n) return PKV_ERR_INVALID_ARG;
+  for (int i = 0; i < n; ++i) {
+    const Req& r = s->running[i];
+    if (request_ids) request_ids[i] = r.id;
+    if (context_lens) context_lens[i] = r.prompt_len + r.generated;
+    if (new_slots) new_slots[i] = s->new_slots[i];
+  }
+  return PKV_OK;
+}
+
+extern "C" int pkv_sched_block_tables(const pkv_scheduler* s, int32_t* tables, int max_blocks,
+                                      int rows) {
+  if (!s || !tables || max_blocks <= 0) return PKV_ERR_INVALID_ARG;
+  const int n = static_cast<int>(s->running.size());
+  if (rows < n) return PKV_ERR_INVALID_ARG;
+  for (int i = 0; i < n; ++i) {
+    int32_t* row = tables + static_cast<int64_t>(i) * max_blocks;
+    int nb = 0;
+    const int rc = pkv_seq_block_table(s->alloc, s->running[i].seq, row, max_blocks, &nb);
+    if (rc != PKV_OK) return rc;
+    std::fill(row + nb, row + max_blocks, -1);
+  }
+  return PKV_OK;
+}
+
+extern "C" int pkv_sched_prompt_slots(const pkv_scheduler* s, int64_t request_id,
+                                      int64_t* slots, int cap, int* n) {
+  if (!s || !n) return PKV_ERR_INVALID_ARG;
+  for (const Req& r : s->running) {
+    if (r.id != request_id) continue;
+    *n = static_cast<int>(r.prompt_slots.size());
+    if (cap < *n || (*n > 0 && !slots)) return PKV_ERR_INVALID_ARG;
+    std::copy(r.prompt_slots.begin(), r.prompt_slots.end(), slots);
+    return PKV_OK;
+  }
+  return PKV_ERR_NOT_FOUND;
+}
+
+extern "C" int pkv_sched_events(const pkv_scheduler* s, int kind, int64_t* ids, int cap,
+                                int* n) {
+  if (!s || !n) return PKV_ERR_INVALID_ARG;
+  const std::vector<int64_t>* v = kind == 0 ? &s->admitted
+                                  : kind == 1 ? &s->finished
+                                  : kind == 2 ? &s->preempted : nullptr;
+  if (!v) return PKV_ERR_INVALID_ARG;
+  *n = static_cast<int>(v->size());
+  if (cap < *n || (*n > 0 && !ids)) return PKV_ERR_INVALID_ARG;
+  std::copy(v->begin(), v->end(), ids);
+  return PKV_OK;
+}
+
+extern "C" int pkv_sched_counts(const pkv_scheduler* s, int* waiting, int* running,
+                                long long* steps) {
+  if (!s) return PKV_ERR_INVALID_ARG;
+  if (waiting) *waiting = static_cast<int>(s->waiting.size());
+  if (running) *running = static_cast<int>(s->running.size());
+  if (steps) *steps = s->steps;
+  return PKV_OK;
+}

@@ -244,3 +244,29 @@ def long_fp8(seed: int = 1005, num_seqs: int = 8, ctx: int = 131072) -> Workload
 
 ALL = {"tiny": tiny, "qwen_like": qwen_like, "mixed": mixed, "cow": cow,
        "long_fp8": long_fp8}
+
+
+# ---- request streams (continuous batching): a request's K/V row at position
+# t and its query at position t are fixed by (seed, layer, request id, t), so
+# any iteration can be regenerated on the host.
+def request_rows(seed: int, kind: int, layer: int, request_id: int, t0: int, t1: int,
+                 num_kv_heads: int, head_dim: int, device="cpu") -> torch.Tensor:
+    per = num_kv_heads * head_dim
+    key = stream_key(seed, kind, layer, (1 << 18) + request_id)
+    return normal_bf16(key, (t1 - t0) * per, t0 * per, device).view(t1 - t0, num_kv_heads,
+                                                                    head_dim)
+
+
+def request_query(seed: int, layer: int, request_id: int, pos: int, num_heads: int,
+                  head_dim: int, device="cpu") -> torch.Tensor:
+    per = num_heads * head_dim
+    key = stream_key(seed, KIND_Q, layer, (1 << 18) + request_id)
+    return normal_bf16(key, per, pos * per, device).view(num_heads, head_dim)
+
+
+def request_mix(seed: int, n: int, prompt_lo: int = 16, prompt_hi: int = 4096,
+                gen_lo: int = 8, gen_hi: int = 512):
+    """n requests (id, prompt length log-uniform, token budget log-uniform)."""
+    p = _loguniform_lengths(seed, n, prompt_lo, prompt_hi)
+    g = _loguniform_lengths(seed + 1, n, gen_lo, gen_hi)
+    return [(i, p[i], g[i]) for i in range(n)]

@@ -201,3 +201,120 @@ def step(pw: PagedWorkload, out: List[torch.Tensor], workspace: Optional[torch.T
         if P > 0:
             pkv.paged_attention_reduce(out[layer], workspace, pw.context_lens, pw.max_context, P,
                                        stream)
+
+
+def capture_step(pw: PagedWorkload, out: List[torch.Tensor], workspace: Optional[torch.Tensor],
+                 partition_size: Optional[int] = None, copy_pairs: bool = False):
+    """Record one decode step (every layer's cache write, decode and merge;
+    with copy_pairs also the copy-on-write block copies) as a CUDA graph, so a
+    step is replayed with one launch from the host instead of 3-4 per layer
+    ("vLLM architecture, memory and benchmarks deep dive", section
+    "Hardware-level optimizations": per-kernel dispatch cost on the CPU
+    exceeds small kernels' run time; a recorded graph replays the whole
+    sequence in one dispatch).
+
+    The graph reads the tensors it was recorded with: update q, the new K/V,
+    slots, block tables and context lengths in place, then replay().
+    copy_pairs records the copy-on-write copies too; that is only right for
+    the divergence iteration itself, since a clone later also holds tokens
+    written after the copy.
+    Every kernel is run once eagerly first (on the capture stream), so the
+    library's one-time per-device set-up happens outside the capture."""
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        if copy_pairs and pw.cow_pairs is not None:
+            for st in pw.layers:
+                pkv.copy_blocks(st.k_cache, st.v_cache, pw.cow_pairs)
+        step(pw, out, workspace, partition_size)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        if copy_pairs and pw.cow_pairs is not None:
+            for st in pw.layers:
+                pkv.copy_blocks(st.k_cache, st.v_cache, pw.cow_pairs)
+        step(pw, out, workspace, partition_size)
+    return g
+
+
+class ContinuousBatch:
+    """Decode iterations driven by the continuous-batching scheduler.
+
+    Every iteration: the scheduler ejects finished requests (their blocks go
+    back to the pool), admits waiting ones (their prompt K/V rows are written
+    to the prompt slots, standing in for the prefill) and gives each running
+    request the slot of this iteration's token; then the new K/V rows are
+    written and the split decode + merge runs over the running batch. K/V rows
+    and queries come from per-request streams (synth.request_rows /
+    request_query), so any iteration can be checked on the host."""
+
+    def __init__(self, seed, requests, num_blocks, block_size=32, num_heads=24,
+                 num_kv_heads=4, head_dim=256, max_num_seqs=64, partition_size=512,
+                 device="cuda", alloc_seed=None):
+        self.seed = seed
+        self.B = block_size
+        self.Hq, self.Hk, self.D = num_heads, num_kv_heads, head_dim
+        self.P = partition_size
+        self.device = torch.device(device)
+        self.alloc = pkv.BlockAllocator(num_blocks, block_size,
+                                        seed=seed if alloc_seed is None else alloc_seed)
+        self.sched = pkv.Scheduler(self.alloc, max_num_seqs)
+        self.max_num_seqs = max_num_seqs
+        self.max_context = max(p + g for _, p, g in requests)
+        self.max_blocks = -(-self.max_context // block_size)
+        for rid, p, g in requests:
+            self.sched.add_request(rid, p, g)
+        self.k_cache = torch.zeros(num_blocks, num_kv_heads, block_size, head_dim,
+                                   dtype=torch.bfloat16, device=self.device)
+        self.v_cache = torch.zeros_like(self.k_cache)
+        self.out = torch.empty(max_num_seqs, num_heads, head_dim, dtype=torch.bfloat16,
+                               device=self.device)
+        self.ws = pkv.alloc_workspace(max_num_seqs, num_heads, head_dim, self.max_context,
+                                      partition_size, device=self.device) \
+            if partition_size else None
+        self.scale = float(torch.tensor(1.0 / (head_dim ** 0.5), dtype=torch.float32))
+        self.tokens = 0
+
+    def done(self) -> bool:
+        c = self.sched.counts()
+        return c["running"] == 0 and c["waiting"] == 0
+
+    def step(self):
+        """One iteration; returns (request_ids, context_lens, out[:n]) or None
+        when nothing is running."""
+        n, na, _ = self.sched.step()
+        if n == 0:
+            return None
+        dev = self.device
+        for rid in self.sched.events(0):
+            slots = self.sched.prompt_slots(int(rid))
+            if len(slots) == 0:
+                continue
+            k = synth.request_rows(self.seed, synth.KIND_K, 0, int(rid), 0, len(slots),
+                                   self.Hk, self.D, dev)
+            v = synth.request_rows(self.seed, synth.KIND_V, 0, int(rid), 0, len(slots),
+                                   self.Hk, self.D, dev)
+            pkv.kv_cache_write(k, v, torch.as_tensor(slots, device=dev), self.k_cache,
+                               self.v_cache)
+        ids, ctx, slots = self.sched.running()
+        k_new = torch.stack([synth.request_rows(self.seed, synth.KIND_K, 0, int(r), int(c) - 1,
+                                                int(c), self.Hk, self.D, dev)[0]
+                             for r, c in zip(ids, ctx)])
+        v_new = torch.stack([synth.request_rows(self.seed, synth.KIND_V, 0, int(r), int(c) - 1,
+                                                int(c), self.Hk, self.D, dev)[0]
+                             for r, c in zip(ids, ctx)])
+        q = torch.stack([synth.request_query(self.seed, 0, int(r), int(c) - 1, self.Hq, self.D,
+                                             dev) for r, c in zip(ids, ctx)])
+        pkv.kv_cache_write(k_new, v_new, torch.as_tensor(slots, device=dev), self.k_cache,
+                           self.v_cache)
+        bt = torch.as_tensor(self.sched.block_tables(self.max_blocks), device=dev)
+        cl = torch.as_tensor(ctx, device=dev)
+        out = self.out[:n]
+        mc = int(ctx.max())
+        pkv.paged_attention_decode(out, q, self.k_cache, self.v_cache, bt, cl, self.scale, mc,
+                                   self.P, self.ws)
+        if self.P:
+            pkv.paged_attention_reduce(out, self.ws, cl, mc, self.P)
+        self.tokens += n
+        return ids, ctx, out

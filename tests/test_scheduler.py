@@ -1,0 +1,119 @@
+"""Continuous-batching scheduler on the host: iteration-level admission and
+ejection, blocks returned at EOS, invariants, preemption under pressure."""
+import numpy as np
+import pytest
+
+import paged_kv_cache_220_gb300 as pkv
+from paged_kv_cache_220_gb300 import build, synth
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    build.build()
+
+
+def _check(alloc, sched, B):
+    ids, ctx, slots = sched.running()
+    tables = sched.block_tables(4096)
+    assert len(set(slots.tolist())) == len(slots)
+    for i in range(len(ids)):
+        nb = int((tables[i] >= 0).sum())
+        assert nb == -(-int(ctx[i]) // B)
+        pos = int(ctx[i]) - 1
+        assert int(slots[i]) == int(tables[i][pos // B]) * B + pos % B
+    st = alloc.stats()
+    assert st["free_blocks"] + st["used_blocks"] == alloc.num_blocks
+    assert st["used_slots"] == int(ctx.sum())
+
+
+def test_iteration_level_eject_and_admit():
+    """The pages' straggler example: budgets 50, 120, 240 and 1024 tokens with
+    room for two at a time. A finished request's slot is taken by the next
+    waiting request in the very next iteration."""
+    B = 16
+    alloc = pkv.BlockAllocator(1024, B, seed=1)
+    sched = pkv.Scheduler(alloc, max_num_seqs=2)
+    budgets = [50, 120, 240, 1024]
+    for i, g in enumerate(budgets):
+        sched.add_request(i, 10, g)
+    admitted_at, finished_at = {}, {}
+    step = 0
+    while True:
+        n, na, nf = sched.step()
+        step += 1
+        for r in sched.events(0):
+            admitted_at[int(r)] = step
+        for r in sched.events(1):
+            finished_at[int(r)] = step
+        if n == 0 and sched.counts()["waiting"] == 0:
+            break
+        _check(alloc, sched, B)
+        assert n <= 2
+    assert admitted_at == {0: 1, 1: 1, 2: 51, 3: 121}
+    assert finished_at == {0: 51, 1: 121, 2: 291, 3: 1145}
+    assert alloc.stats()["used_blocks"] == 0 and alloc.stats()["free_blocks"] == 1024
+
+
+def test_context_grows_one_token_per_iteration():
+    alloc = pkv.BlockAllocator(64, 4, seed=2)
+    sched = pkv.Scheduler(alloc, max_num_seqs=8)
+    for i, (p, g) in enumerate([(3, 2), (5, 1), (2, 3)]):
+        sched.add_request(i, p, g)
+    sched.step()
+    ids, ctx, _ = sched.running()
+    assert ids.tolist() == [0, 1, 2] and ctx.tolist() == [4, 6, 3]
+    for i in ids:
+        assert len(sched.prompt_slots(int(i))) == [3, 5, 2][int(i)]
+    sched.step()
+    ids, ctx, _ = sched.running()
+    assert ids.tolist() == [0, 2] and ctx.tolist() == [5, 4]
+    assert sched.events(1).tolist() == [1]
+    sched.step()
+    ids, ctx, _ = sched.running()
+    assert ids.tolist() == [2] and ctx.tolist() == [5]
+    n, _, nf = sched.step()
+    assert n == 0 and nf == 1
+    assert alloc.stats()["used_blocks"] == 0
+
+
+def test_admission_waits_for_free_blocks():
+    B = 16
+    alloc = pkv.BlockAllocator(10, B, seed=3)
+    sched = pkv.Scheduler(alloc, max_num_seqs=16)
+    sched.add_request(0, 100, 5)     # 7 blocks with its first token
+    sched.add_request(1, 60, 5)      # needs 4 more: waits
+    n, na, _ = sched.step()
+    assert (n, na) == (1, 1)
+    for _ in range(5):
+        sched.step()
+    assert 1 in sched.events(0).tolist()
+
+
+def test_preemption_requeues_and_everything_finishes():
+    B = 16
+    alloc = pkv.BlockAllocator(40, B, seed=4)
+    sched = pkv.Scheduler(alloc, max_num_seqs=8)
+    reqs = synth.request_mix(7, 24, prompt_lo=16, prompt_hi=200, gen_lo=16, gen_hi=300)
+    for rid, p, g in reqs:
+        sched.add_request(rid, p, g)
+    done, preempted = set(), 0
+    for _ in range(20000):
+        n, _, _ = sched.step()
+        done |= set(sched.events(1).tolist())
+        preempted += len(sched.events(2))
+        if n:
+            _check(alloc, sched, B)
+        if n == 0 and sched.counts()["waiting"] == 0:
+            break
+    assert done == set(range(24))
+    assert preempted > 0
+    assert alloc.stats()["free_blocks"] == 40
+
+
+def test_bad_arguments():
+    alloc = pkv.BlockAllocator(8, 16)
+    sched = pkv.Scheduler(alloc, 4)
+    with pytest.raises(pkv.PagedKVError):
+        sched.add_request(0, 10, 0)
+    with pytest.raises(pkv.PagedKVError):
+        sched.prompt_slots(5)
