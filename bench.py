@@ -235,6 +235,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--shared-prefix", type=int, default=1,
+                    help="1: workloads with shared prompts use the shared-prefix decode")
     ap.add_argument("--graph", type=int, default=1,
                     help="1: the timed steps replay a CUDA graph of the step (default)")
     ap.add_argument("--layers", type=int, default=0,
@@ -307,12 +309,26 @@ def main():
     stream = torch.cuda.current_stream()
     cow = pw.cow_pairs
 
+    cascade = None
+    if w.prefix_len > 0 and args.shared_prefix and P and not w.fp8:
+        cascade = workload.prefix_groups(pw)
+        ws = pkv.shared_prefix_workspace(w.num_seqs, w.num_heads, w.head_dim, pw.max_context,
+                                         cascade[2] * w.block_size, P)
+
     def one_step(ev=None):
         for layer, st in enumerate(pw.layers):
             pkv.kv_cache_write(st.k_new, st.v_new, pw.slot_mapping, st.k_cache, st.v_cache,
                                st.k_scale, st.v_scale)
             if ev is not None:
                 ev[layer][0].record(stream)
+            if cascade is not None:
+                pkv.paged_attention_shared_prefix(st.q, st.k_cache, st.v_cache, pw.block_tables,
+                                                  pw.context_lens, w.scale, pw.max_context,
+                                                  cascade[0], cascade[1], cascade[2], P,
+                                                  out=out[layer], workspace=ws)
+                if ev is not None:
+                    ev[layer][1].record(stream)
+                continue
             pkv.paged_attention_decode(out[layer], st.q, st.k_cache, st.v_cache, pw.block_tables,
                                        pw.context_lens, w.scale, pw.max_context, P, ws,
                                        st.k_scale, st.v_scale)
@@ -321,7 +337,7 @@ def main():
             if P:
                 pkv.paged_attention_reduce(out[layer], ws, pw.context_lens, pw.max_context, P)
 
-    launches_per_step = L * (2 + (1 if P else 0))
+    launches_per_step = L * ((4 if cascade is not None else 2) + (1 if P and cascade is None else 0))
     for _ in range(args.warmup):
         one_step()
     torch.cuda.synchronize()
@@ -349,7 +365,10 @@ def main():
     # dispatch per step), or eager launches with --graph 0
     graph = None
     if args.graph:
-        graph = workload.capture_step(pw, out, ws, P)
+        if cascade is not None:
+            graph = capture(one_step)
+        else:
+            graph = workload.capture_step(pw, out, ws, P)
         for _ in range(args.warmup):
             graph.replay()
     if dist is not None:
@@ -395,7 +414,7 @@ def main():
         return 0
 
     peak, peak_kind = peaks()
-    dec_bytes = decode_bytes(w)
+    dec_bytes = decode_bytes(w) if cascade is None else unique_decode_bytes(w)
     achieved = dec_bytes / (dec_avg_ms / 1e3) / 1e9
     traffic, traffic_note = ncu_traffic(args.config)
     cpu = None
@@ -424,7 +443,9 @@ def main():
         "tokens_per_s_per_layer": round(tok_per_s_layer, 1),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "peak_kind": peak_kind, "kernel": "paged_attention_decode",
+                     "peak_kind": peak_kind,
+                     "kernel": "paged_attention_decode" if cascade is None else
+                               "paged_attention_decode_shared_prefix (3 kernels, unique bytes)",
                      "bytes_per_launch": dec_bytes, "launch_ms": round(dec_avg_ms, 5),
                      "traffic": traffic},
         "cpu_baseline": cpu, "e2e": e2e, "copy_blocks": cow_copy,
@@ -437,6 +458,21 @@ def main():
     if dist is not None:
         dist.destroy_process_group()
     return 0
+
+
+def capture(fn):
+    """CUDA graph of fn() (run once eagerly on the capture stream first)."""
+    import torch
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        fn()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        fn()
+    return g
 
 
 def time_copy_blocks(pw, args):

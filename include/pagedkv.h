@@ -179,6 +179,41 @@ int pkv_paged_attention_reduce(void* out, const void* workspace,
                                int partition_size, void* stream);
 
 /* ------------------------------------------------------------------------ *
+ * paged_attention_decode_shared_prefix: decode for groups of sequences that
+ * share a prompt's physical blocks (rollouts forked from one prompt,
+ * [HowVLLM] "PagedAttention borrows from operating systems"; [Dissect]
+ * "PagedAttention: Virtual Memory for KV Cache"). The result is the same
+ * attention as pkv_paged_attention_decode; the shared pages are read once per
+ * group instead of once per member.
+ *
+ *   group_start   : device int32 [num_groups + 1]; group i is the sequences
+ *                   [group_start[i], group_start[i+1]) of the batch (at most
+ *                   128 / g members); sequences outside every group are fine
+ *   prefix_blocks : device int32 [num_seqs]; the number of leading blocks of
+ *                   each sequence that are its group's shared prefix: the same
+ *                   value and the same physical ids for every member, full
+ *                   blocks only, prefix_blocks[s]*block_size <= context_lens[s];
+ *                   0 for a sequence outside every group
+ *   max_prefix_blocks : host upper bound of prefix_blocks
+ *   partition_size: split size for both parts (multiple of block_size)
+ *   workspace     : at least pkv_shared_prefix_workspace_bytes(...) bytes
+ * Per group and KV head, a kernel computes partials of every member's query
+ * heads over the shared pages (the members' queries form the rows of one
+ * tensor-core product); each member's own blocks go through the split decode;
+ * the merge combines both. bf16 pools only (PKV_ERR_UNSUPPORTED otherwise).
+ * ------------------------------------------------------------------------ */
+size_t pkv_shared_prefix_workspace_bytes(int num_seqs, int num_heads, int head_dim,
+                                         int max_context, int max_prefix_tokens,
+                                         int partition_size);
+int pkv_paged_attention_decode_shared_prefix(
+    void* out, const void* q, const void* k_cache, const void* v_cache,
+    pkv_cache_desc cache, const int32_t* block_tables, int max_blocks_per_seq,
+    const int32_t* context_lens, int num_seqs, int num_heads, int max_context,
+    float scale, const int32_t* group_start, int num_groups,
+    const int32_t* prefix_blocks, int max_prefix_blocks, int partition_size,
+    void* workspace, size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------ *
  * copy_blocks: copy-on-write duplication. Sequences forked from one prompt
  * share its physical blocks; a block is cloned only when a sibling is about
  * to write into it ([HowVLLM] "PagedAttention borrows from operating

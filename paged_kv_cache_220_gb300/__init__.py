@@ -68,6 +68,10 @@ SIGNATURES = {
     "pkv_paged_attention_reduce": (_I, [_P, _P, ctypes.c_size_t, _P, _I, _I, _I, _I, _I, _P]),
     "pkv_paged_attention_decode_noalloc": (_I, [_P, _P, _P, _P, CacheDesc, _P, _P, _P, _I, _P,
                                                 _I, _I, _I, ctypes.c_float, _I, _P]),
+    "pkv_shared_prefix_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I, _I, _I, _I]),
+    "pkv_paged_attention_decode_shared_prefix": (_I, [_P, _P, _P, _P, CacheDesc, _P, _I, _P, _I,
+                                                      _I, _I, ctypes.c_float, _P, _I, _P, _I,
+                                                      _I, _P, ctypes.c_size_t, _P]),
     "pkv_copy_blocks": (_I, [_P, _P, CacheDesc, _P, _I, _P]),
     "pkv_swap_out": (_I, [_P, _P, CacheDesc, _P, _I, _P, _P, _P]),
     "pkv_swap_in": (_I, [_P, _P, CacheDesc, _P, _I, _P, _P, _P]),
@@ -261,6 +265,41 @@ def paged_attention_decode_noalloc(out, q, k_cache, v_cache, block_tables, conte
         _dev_ptr(context_lens, "context_lens", torch.int32), S, Hq, int(max_context),
         float(scale), int(partition_size), _stream(stream))
     _check(rc, "paged_attention_decode_noalloc")
+
+
+def shared_prefix_workspace(num_seqs, num_heads, head_dim, max_context, max_prefix_tokens,
+                            partition_size, device=None) -> torch.Tensor:
+    n = int(lib().pkv_shared_prefix_workspace_bytes(num_seqs, num_heads, head_dim, max_context,
+                                                    max_prefix_tokens, partition_size))
+    return torch.empty(max(n, 16), dtype=torch.uint8, device=device or "cuda")
+
+
+def paged_attention_shared_prefix(q, k_cache, v_cache, block_tables, context_lens, scale,
+                                  max_context, group_start, prefix_blocks, max_prefix_blocks,
+                                  partition_size, out=None, workspace=None,
+                                  stream=None) -> torch.Tensor:
+    """Decode of groups sharing prompt blocks (see the C header): shared pages
+    are read once per group. group_start int32 [G+1], prefix_blocks int32 [S]."""
+    desc = cache_desc(k_cache)
+    S, Hq, D = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    if workspace is None:
+        workspace = shared_prefix_workspace(S, Hq, D, max(int(max_context), 1),
+                                            int(max_prefix_blocks) * desc.block_size,
+                                            partition_size, q.device)
+    G = int(group_start.shape[0]) - 1
+    rc = lib().pkv_paged_attention_decode_shared_prefix(
+        _dev_ptr(out, "out", torch.bfloat16), _dev_ptr(q, "q", torch.bfloat16),
+        _dev_ptr(k_cache, "k_cache"), _dev_ptr(v_cache, "v_cache"), desc,
+        _dev_ptr(block_tables, "block_tables", torch.int32), int(block_tables.shape[1]),
+        _dev_ptr(context_lens, "context_lens", torch.int32), S, Hq, int(max_context),
+        float(scale), _dev_ptr(group_start, "group_start", torch.int32), G,
+        _dev_ptr(prefix_blocks, "prefix_blocks", torch.int32), int(max_prefix_blocks),
+        int(partition_size), _dev_ptr(workspace, "workspace"),
+        workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(rc, "paged_attention_decode_shared_prefix")
+    return out
 
 
 def copy_blocks(k_cache, v_cache, block_pairs, stream=None) -> None:

@@ -27,11 +27,22 @@ struct DecodeParams {
   int partition_blocks;  // 0 = whole context in one CTA
   int np_max;
   int cluster;           // one pass: CTAs (a thread-block cluster) per (seq, KV head)
+  const int32_t* block_offset;  // split form: first logical block per sequence (NULL = 0)
+  int slot_offset;              // split form: partial p is stored at slot slot_offset + p
   float qscale;          // scale * log2(e)
 };
 
 // Tensor-core decode (decode_tc.cu) for bf16 or E4M3 pools. Returns a pkv_status.
 int launch_decode_tc(const DecodeParams& p, const void* k_cache, const void* v_cache,
                      int head_dim, int block_size, bool fp8, dim3 grid, cudaStream_t st);
+
+// Merge of split partials (reduce.cu). With prefix_blocks == NULL the slots of
+// sequence s are [0, ceil(ctx/P)); otherwise [0, npre) and [slot_split,
+// slot_split + nsuf) with npre = ceil(prefix_blocks[s]*B/P) and nsuf =
+// ceil((ctx - prefix_blocks[s]*B)/P).
+int launch_reduce(void* out, const float* tmp, const float* ml, const float* es,
+                  const int32_t* context_lens, int num_seqs, int num_heads, int head_dim,
+                  int np_max, int partition_size, const int32_t* prefix_blocks, int block_size,
+                  int slot_split, cudaStream_t st);
 
 }  // namespace pkv

@@ -12,6 +12,7 @@
 // reproduce its output exactly. The work is HBM-bound: (d + 2) * 4 bytes per
 // partition read, d * 2 bytes written.
 #include "common.cuh"
+#include "decode_params.h"
 #include "host_util.h"
 
 namespace pkv {
@@ -25,7 +26,7 @@ __global__ void __launch_bounds__(kReduceThreads) reduce_kernel(
     uint16_t* __restrict__ out, const float* __restrict__ tmp_out,
     const float* __restrict__ max_logits, const float* __restrict__ exp_sums,
     const int32_t* __restrict__ context_lens, int num_heads, int np_max, int partition_size,
-    int* err) {
+    const int32_t* __restrict__ prefix_blocks, int block_size, int slot_split, int* err) {
   constexpr int V4 = D / 128;  // float4 per lane per partition row
   extern __shared__ float wsh[];  // [np_max] normalised weights
   __shared__ float red[kReduceWarps];
@@ -34,12 +35,20 @@ __global__ void __launch_bounds__(kReduceThreads) reduce_kernel(
   const int s = blockIdx.y;
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
-  int ctx = context_lens[s];
-  int np = ctx > 0 ? (ctx + partition_size - 1) / partition_size : 0;
-  if (np > np_max) {
-    if (tid == 0) report_error(err, PKV_DEVERR_CONTEXT);
-    np = np_max;
+  const int ctx = context_lens[s];
+  // slots of this sequence: [0, npre) and [slot_split, slot_split + nsuf)
+  int npre = 0, nsuf = ctx > 0 ? (ctx + partition_size - 1) / partition_size : 0;
+  if (prefix_blocks != nullptr) {
+    const int ptok = prefix_blocks[s] * block_size;
+    npre = (ptok + partition_size - 1) / partition_size;
+    nsuf = ctx > ptok ? (ctx - ptok + partition_size - 1) / partition_size : 0;
   }
+  if (slot_split + nsuf > np_max || npre > slot_split) {
+    if (tid == 0) report_error(err, PKV_DEVERR_CONTEXT);
+    npre = min(npre, slot_split);
+    nsuf = max(0, min(nsuf, np_max - slot_split));
+  }
+  const int np = npre + nsuf;
   const int64_t row = static_cast<int64_t>(s) * num_heads + j;
   if (np == 0) {
     if (tid < D / 4) reinterpret_cast<uint2*>(out + row * D)[tid] = make_uint2(0u, 0u);
@@ -50,7 +59,8 @@ __global__ void __launch_bounds__(kReduceThreads) reduce_kernel(
 
   // M = max_p m_p
   float M = -INFINITY;
-  for (int i = tid; i < np; i += kReduceThreads) M = fmaxf(M, ml[i]);
+  auto slot_of = [&](int v) { return v < npre ? v : slot_split + (v - npre); };
+  for (int i = tid; i < np; i += kReduceThreads) M = fmaxf(M, ml[slot_of(i)]);
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
   if (lane == 0) red[warp] = M;
@@ -62,7 +72,7 @@ __global__ void __launch_bounds__(kReduceThreads) reduce_kernel(
   // W = sum_p w_p (fixed tree: lanes by xor, then warps in order)
   float W = 0.f;
   for (int i = tid; i < np; i += kReduceThreads) {
-    const float w = es[i] * fast_exp2((ml[i] - M) * kLog2eR);
+    const float w = es[slot_of(i)] * fast_exp2((ml[slot_of(i)] - M) * kLog2eR);
     wsh[i] = w;
     W += w;
   }
@@ -90,7 +100,7 @@ __global__ void __launch_bounds__(kReduceThreads) reduce_kernel(
     for (int u = 0; u < U; ++u)
 #pragma unroll
       for (int v = 0; v < V4; ++v)
-        x[u][v] = src[static_cast<int64_t>(i + u * kReduceWarps) * (D / 4) + lane + 32 * v];
+        x[u][v] = src[static_cast<int64_t>(slot_of(i + u * kReduceWarps)) * (D / 4) + lane + 32 * v];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const float r = wsh[i + u * kReduceWarps];
@@ -107,7 +117,7 @@ __global__ void __launch_bounds__(kReduceThreads) reduce_kernel(
     const float r = wsh[i];
 #pragma unroll
     for (int v = 0; v < V4; ++v) {
-      const float4 x = src[static_cast<int64_t>(i) * (D / 4) + lane + 32 * v];
+      const float4 x = src[static_cast<int64_t>(slot_of(i)) * (D / 4) + lane + 32 * v];
       acc[v].x = fmaf(r, x.x, acc[v].x);
       acc[v].y = fmaf(r, x.y, acc[v].y);
       acc[v].z = fmaf(r, x.z, acc[v].z);
@@ -137,6 +147,36 @@ __global__ void __launch_bounds__(kReduceThreads) reduce_kernel(
 
 }  // namespace pkv
 
+namespace pkv {
+
+int launch_reduce(void* out, const float* tmp, const float* ml, const float* es,
+                  const int32_t* context_lens, int num_seqs, int num_heads, int head_dim,
+                  int np_max, int partition_size, const int32_t* prefix_blocks, int block_size,
+                  int slot_split, cudaStream_t st) {
+  const size_t smem = static_cast<size_t>(np_max > 0 ? np_max : 1) * sizeof(float);
+  constexpr size_t kMaxSmem = 160 * 1024;  // plus the static accumulators
+  if (smem > kMaxSmem) return PKV_ERR_UNSUPPORTED;
+  dim3 grid(num_heads, num_seqs);
+  if (head_dim == 128) {
+    static bool done[64] = {false};
+    int rc = ensure_smem(reduce_kernel<128>, kMaxSmem, done, 64);
+    if (rc != PKV_OK) return rc;
+    reduce_kernel<128><<<grid, kReduceThreads, smem, st>>>(
+        static_cast<uint16_t*>(out), tmp, ml, es, context_lens, num_heads, np_max,
+        partition_size, prefix_blocks, block_size, slot_split, device_error_ptr());
+  } else {
+    static bool done[64] = {false};
+    int rc = ensure_smem(reduce_kernel<256>, kMaxSmem, done, 64);
+    if (rc != PKV_OK) return rc;
+    reduce_kernel<256><<<grid, kReduceThreads, smem, st>>>(
+        static_cast<uint16_t*>(out), tmp, ml, es, context_lens, num_heads, np_max,
+        partition_size, prefix_blocks, block_size, slot_split, device_error_ptr());
+  }
+  return launch_status();
+}
+
+}  // namespace pkv
+
 extern "C" int pkv_paged_attention_reduce(void* out, const void* workspace,
                                           size_t workspace_bytes,
                                           const int32_t* context_lens, int num_seqs,
@@ -154,9 +194,6 @@ extern "C" int pkv_paged_attention_reduce(void* out, const void* workspace,
                                                  max_context > 0 ? max_context : 1, partition_size);
   if (max_context > 0 && (!workspace || !aligned16(workspace) || workspace_bytes < need))
     return PKV_ERR_INVALID_ARG;
-  const size_t smem = static_cast<size_t>(np) * sizeof(float);
-  constexpr size_t kMaxSmem = 160 * 1024;  // plus the static accumulators
-  if (smem > kMaxSmem) return PKV_ERR_UNSUPPORTED;
   // With every context empty no partial is read (np_max = 0 makes the kernel
   // write zeros), so the workspace may be absent.
   const int np_arg = max_context > 0 ? np : 0;
@@ -165,22 +202,6 @@ extern "C" int pkv_paged_attention_reduce(void* out, const void* workspace,
   const float* tmp = ws;
   const float* ml = ws ? ws + rows * head_dim : nullptr;
   const float* es = ws ? ml + rows : nullptr;
-  dim3 grid(num_heads, num_seqs);
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (head_dim == 128) {
-    static bool done[64] = {false};
-    int rc = ensure_smem(reduce_kernel<128>, kMaxSmem, done, 64);
-    if (rc != PKV_OK) return rc;
-    reduce_kernel<128><<<grid, kReduceThreads, smem, st>>>(
-        static_cast<uint16_t*>(out), tmp, ml, es, context_lens, num_heads, np_arg,
-        partition_size, device_error_ptr());
-  } else {
-    static bool done[64] = {false};
-    int rc = ensure_smem(reduce_kernel<256>, kMaxSmem, done, 64);
-    if (rc != PKV_OK) return rc;
-    reduce_kernel<256><<<grid, kReduceThreads, smem, st>>>(
-        static_cast<uint16_t*>(out), tmp, ml, es, context_lens, num_heads, np_arg,
-        partition_size, device_error_ptr());
-  }
-  return launch_status();
+  return launch_reduce(out, tmp, ml, es, context_lens, num_seqs, num_heads, head_dim, np_arg,
+                       partition_size, nullptr, 1, 0, static_cast<cudaStream_t>(stream));
 }

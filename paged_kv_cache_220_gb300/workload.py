@@ -318,3 +318,44 @@ class ContinuousBatch:
             pkv.paged_attention_reduce(out, self.ws, cl, mc, self.P)
         self.tokens += n
         return ids, ctx, out
+
+
+def prefix_groups(pw: PagedWorkload, device="cuda"):
+    """Group metadata of a shared-prefix workload: (group_start int32 [G+1],
+    prefix_blocks int32 [S], max_prefix_blocks). The shared prefix of a group
+    is the run of leading full blocks whose physical ids every member's table
+    has in common (a partly filled prompt block is cloned on divergence and
+    so is private)."""
+    w = pw.w
+    S = w.num_seqs
+    if w.prefix_len <= 0:
+        return (torch.zeros(1, dtype=torch.int32, device=device),
+                torch.zeros(S, dtype=torch.int32, device=device), 0)
+    G = w.group
+    n_prompt = S // G
+    tables = pw.tables_host
+    pre = np.zeros(S, dtype=np.int32)
+    for p in range(n_prompt):
+        rows = tables[p * G:(p + 1) * G]
+        full = w.prefix_len // w.block_size
+        k = 0
+        while k < full and np.all(rows[:, k] == rows[0, k]):
+            k += 1
+        pre[p * G:(p + 1) * G] = k
+    starts = np.arange(0, n_prompt * G + 1, G, dtype=np.int32)
+    return (torch.as_tensor(starts, device=device), torch.as_tensor(pre, device=device),
+            int(pre.max()) if S else 0)
+
+
+def step_shared_prefix(pw: PagedWorkload, out: List[torch.Tensor], groups, workspace,
+                       partition_size: Optional[int] = None, stream=None) -> None:
+    """One decode step over every layer with the shared-prefix decode."""
+    P = pw.w.partition_size if partition_size is None else partition_size
+    gs, pre, maxpre = groups
+    for layer, st in enumerate(pw.layers):
+        pkv.kv_cache_write(st.k_new, st.v_new, pw.slot_mapping, st.k_cache, st.v_cache,
+                           st.k_scale, st.v_scale, stream)
+        pkv.paged_attention_shared_prefix(st.q, st.k_cache, st.v_cache, pw.block_tables,
+                                          pw.context_lens, pw.w.scale, pw.max_context, gs, pre,
+                                          maxpre, P, out=out[layer], workspace=workspace,
+                                          stream=stream)

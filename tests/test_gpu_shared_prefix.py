@@ -1,0 +1,72 @@
+"""Shared-prefix decode: rollouts of one prompt read the prompt's pages once
+per group; the output matches the oracle and the plain split decode."""
+import dataclasses
+
+import pytest
+import torch
+
+import paged_kv_cache_220_gb300 as pkv
+from paged_kv_cache_220_gb300 import build as pkv_build
+from paged_kv_cache_220_gb300 import synth, workload
+from _oracle_side import MAX_ABS, REL_L2, assert_close, errors, expected
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    pkv_build.build()
+    flag = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pkv.set_device_check(flag)
+    yield flag
+    pkv.set_device_check(None)
+
+
+@pytest.mark.parametrize("prompt,B,P,rollouts", [(40, 16, 32, 4), (48, 16, 16, 16),
+                                                  (2040, 16, 512, 16), (200, 32, 64, 3),
+                                                  (100, 16, 512, 21)])
+def test_shared_prefix_matches_oracle(prompt, B, P, rollouts, _lib):
+    w = synth.cow(prompt_len=prompt, prompts=2, rollouts=rollouts)
+    comp = w.extra["completion"][:2 * rollouts]
+    w = dataclasses.replace(w, block_size=B, ctx=[prompt + (c % 300) + 1 for c in comp],
+                            slack_blocks=64)
+    if rollouts * w.num_heads // w.num_kv_heads > 128:
+        pytest.skip("group larger than one prefix CTA")
+    pw = workload.build(w)
+    groups = workload.prefix_groups(pw)
+    assert groups[2] == prompt // B
+    out = [torch.empty_like(pw.layers[0].q)]
+    workload.step_shared_prefix(pw, out, groups, None, P)
+    torch.cuda.synchronize()
+    ref = expected(w, 0, range(w.num_seqs))
+    assert_close(out[0].cpu(), ref, "shared prefix %d" % prompt)
+    # the plain split decode over the same state agrees within tolerance
+    ws = pkv.alloc_workspace(w.num_seqs, w.num_heads, w.head_dim, pw.max_context, P)
+    plain = torch.empty_like(out[0])
+    st = pw.layers[0]
+    pkv.paged_attention(st.q, st.k_cache, st.v_cache, pw.block_tables, pw.context_lens, w.scale,
+                        pw.max_context, P, out=plain, workspace=ws)
+    torch.cuda.synchronize()
+    ma, rl = errors(out[0].cpu(), plain.cpu().double().numpy())
+    assert ma <= MAX_ABS and rl <= REL_L2
+    assert int(_lib.item()) == 0
+
+
+def test_shared_prefix_mixed_with_ungrouped_and_exact_prefix(_lib):
+    """Groups of one, a member whose context ends right at the prefix."""
+    w = synth.cow(prompt_len=64, prompts=2, rollouts=4)
+    w = dataclasses.replace(w, ctx=[65, 66, 90, 65, 70, 71, 72, 200])
+    pw = workload.build(w)
+    gs, pre, mp = workload.prefix_groups(pw)
+    # split the second prompt's group into singletons without a shared prefix
+    gs2 = torch.tensor([0, 4], dtype=torch.int32, device="cuda")
+    pre2 = pre.clone()
+    pre2[4:] = 0
+    st = pw.layers[0]
+    pkv.kv_cache_write(st.k_new, st.v_new, pw.slot_mapping, st.k_cache, st.v_cache)
+    out = pkv.paged_attention_shared_prefix(pw.layers[0].q, pw.layers[0].k_cache,
+                                            pw.layers[0].v_cache, pw.block_tables,
+                                            pw.context_lens, w.scale, pw.max_context, gs2, pre2,
+                                            mp, 32)
+    torch.cuda.synchronize()
+    assert_close(out.cpu(), expected(w, 0, range(w.num_seqs)), "mixed groups")
