@@ -295,8 +295,7 @@ def main():
     pkv.lib()
 
     # weak scaling: every rank runs its own batch of the workload
-    if world > 1:
-        w = dataclasses.replace(w, seed=w.seed + 100 * rank)
+    w = workload.rank_workload(w, rank, world)
     pw = workload.build(w)
     L = len(pw.layers)
     P = w.partition_size
@@ -389,12 +388,9 @@ def main():
         dist.barrier()
     step_ms = [a.elapsed_time(b) for a, b in step_ev]
     total_ms = sum(step_ms)
-    if dist is not None:
-        t = torch.tensor([total_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = workload.max_over_ranks(total_ms, dist, "cuda")
     ms_per_step = total_ms / K
-    value = per_step_bytes * world / (ms_per_step / 1e3) / 1e9
+    value = workload.job_throughput(per_step_bytes, world, ms_per_step)
 
     # copy-on-write copies of the divergence iteration, timed on a scratch
     # pool with the same block geometry (replaying them on the live pool would

@@ -299,6 +299,13 @@ int pkv_swap_in(void* k_cache, void* v_cache, pkv_cache_desc cache, const int32_
  * still skip out-of-range ids. Process-wide; returns PKV_OK. */
 int pkv_set_device_check(int* dev_error_flag);
 
+/* Failure-detection self-test: launches one kernel whose barrier wait can never
+ * complete; the bounded wait gives up after limit_us microseconds (1..2e6),
+ * writes PKV_DEVERR_WAIT_TIMEOUT into *dev_error_flag (device int32, first
+ * error wins) and the kernel returns, leaving the context usable. Every wait
+ * in the library's kernels is bounded the same way (2 s). */
+int pkv_selftest_wait_timeout(int* dev_error_flag, int limit_us, void* stream);
+
 /* Static description of a status code. Never NULL. */
 const char* pkv_status_string(int status);
 

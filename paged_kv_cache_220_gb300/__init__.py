@@ -76,6 +76,7 @@ SIGNATURES = {
     "pkv_swap_out": (_I, [_P, _P, CacheDesc, _P, _I, _P, _P, _P]),
     "pkv_swap_in": (_I, [_P, _P, CacheDesc, _P, _I, _P, _P, _P]),
     "pkv_set_device_check": (_I, [_P]),
+    "pkv_selftest_wait_timeout": (_I, [_P, _I, _P]),
     "pkv_status_string": (ctypes.c_char_p, [_I]),
     "pkv_version": (_I, []),
     "pkv_alloc_create": (_I, [_I, _I, ctypes.c_uint64, ctypes.POINTER(_P)]),
@@ -351,6 +352,13 @@ def swap_in(k_cache, v_cache, blocks, k_buf, v_buf, stream=None) -> None:
                            _any_ptr(blocks, "blocks"), n, _any_ptr(k_buf, "k_buf"),
                            _any_ptr(v_buf, "v_buf"), _stream(stream))
     _check(rc, "swap_in")
+
+
+def selftest_wait_timeout(flag, limit_us: int = 50000, stream=None) -> None:
+    """Run the bounded-wait self-test; `flag` (int32 CUDA tensor) receives
+    DEVERR_WAIT_TIMEOUT."""
+    _check(lib().pkv_selftest_wait_timeout(_dev_ptr(flag, "flag", torch.int32), int(limit_us),
+                                           _stream(stream)), "selftest_wait_timeout")
 
 
 def set_device_check(flag) -> None:

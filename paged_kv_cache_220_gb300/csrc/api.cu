@@ -1,6 +1,8 @@
-// Library-wide C entry points: error word registration, status strings.
+// Library-wide C entry points: error word registration, status strings, the
+// bounded-wait self-test.
 #include <atomic>
 
+#include "common.cuh"
 #include "host_util.h"
 
 namespace pkv {
@@ -27,3 +29,26 @@ extern "C" const char* pkv_status_string(int status) {
 }
 
 extern "C" int pkv_version(void) { return 100; }
+
+namespace pkv {
+
+// An mbarrier that expects one arrival nobody makes: the bounded wait gives up
+// after limit_ns, records PKV_DEVERR_WAIT_TIMEOUT and the kernel returns.
+__global__ void wait_timeout_selftest_kernel(int* err, unsigned long long limit_ns) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) (void)mbar_wait(&bar, 0, err, limit_ns);
+}
+
+}  // namespace pkv
+
+extern "C" int pkv_selftest_wait_timeout(int* dev_error_flag, int limit_us, void* stream) {
+  if (!dev_error_flag || limit_us <= 0 || limit_us > 2000000) return PKV_ERR_INVALID_ARG;
+  pkv::wait_timeout_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+      dev_error_flag, static_cast<unsigned long long>(limit_us) * 1000ull);
+  return pkv::launch_status();
+}

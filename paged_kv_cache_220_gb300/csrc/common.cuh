@@ -1,11 +1,10 @@
 // Device helpers shared by the paged-cache kernels (sm_103a).
 //
-// - bounded mbarrier waits: every wait gives up after a wall-clock limit,
-//   records PKV_DEVERR_WAIT_TIMEOUT in the registered error word and lets the
-//   caller return, so no kernel of this library can spin forever;
-// - 1-D bulk copies (cp.async.bulk, the non-tensor TMA form) from global to
-//   shared memory, completing on an mbarrier with a byte count;
-// - bf16 / fp8 unpacking and the fast base-2 exponential.
+// - mbarrier set-up, arrivals with a transaction byte count, and bounded
+//   waits: every wait gives up after a wall-clock limit, records
+//   PKV_DEVERR_WAIT_TIMEOUT in the registered error word and lets the caller
+//   return, so no kernel of this library can spin forever;
+// - bf16 unpacking, bf16 rounding and the fast base-2 exponential.
 #pragma once
 
 #include <cstdint>
@@ -67,50 +66,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Wait for the phase with the given parity to complete. Returns false (and
-// records the timeout) if it has not completed within kWaitLimitNs.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err) {
+// records the timeout) if it has not completed within limit_ns.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err,
+                                          unsigned long long limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = global_ns();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 255u) == 0 && global_ns() - t0 > kWaitLimitNs) {
+    if ((i & 255u) == 0 && global_ns() - t0 > limit_ns) {
       report_error(err, PKV_DEVERR_WAIT_TIMEOUT);
       return false;
     }
   }
-}
-
-// 1-D bulk copy global -> shared, completion counted on `bar` in bytes.
-// Both addresses 16-byte aligned, bytes a multiple of 16.
-__device__ __forceinline__ void bulk_g2s(void* dst_smem, const void* src_gmem, uint32_t bytes,
-                                         uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          smem_addr(dst_smem)),
-      "l"(src_gmem), "r"(bytes), "r"(smem_addr(bar))
-      : "memory");
-}
-
-// Same, with an L2 eviction-priority policy (createpolicy result).
-__device__ __forceinline__ void bulk_g2s_hint(void* dst_smem, const void* src_gmem,
-                                              uint32_t bytes, uint64_t* bar, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], "
-      "[%1], %2, [%3], %4;" ::"r"(smem_addr(dst_smem)),
-      "l"(src_gmem), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
-      : "memory");
-}
-
-__device__ __forceinline__ uint64_t policy_evict_first() {
-  uint64_t p;
-  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
-  return p;
-}
-
-__device__ __forceinline__ uint64_t policy_evict_last() {
-  uint64_t p;
-  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
-  return p;
 }
 
 // 2^x on the special-function unit.
@@ -123,13 +90,6 @@ __device__ __forceinline__ float fast_exp2(float x) {
 // Two bf16 packed in a 32-bit word -> (low, high) as float (exact).
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
-
-// Two E4M3 codes packed in 16 bits -> float2 (exact, via the hardware
-// e4m3x2 -> f16x2 conversion).
-__device__ __forceinline__ float2 e4m3x2_to_float2(uint16_t w) {
-  __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w), __NV_E4M3);
-  return __half22float2(*reinterpret_cast<__half2*>(&h));
-}
 
 __device__ __forceinline__ uint16_t float_to_bf16_bits(float x) {
   __nv_bfloat16 b = __float2bfloat16_rn(x);

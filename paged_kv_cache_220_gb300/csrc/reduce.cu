@@ -4,11 +4,11 @@
 // M = max_p m_p and w_p = l_p * exp(m_p - M), the full softmax output is
 // sum_p (w_p / sum_q w_q) o_p.
 //
-// One CTA of 16 warps per (query head, sequence). The weights are computed
-// once into shared memory (block-wide max and sum in a fixed tree order), then
-// warp w accumulates the partitions p = w, w + 16, ... with 16-byte loads,
-// four partitions in flight per lane, and the 16 warp sums are added in warp
-// order. Normalising the weights before the products makes a single partition
+// One CTA per (query head, sequence), RW warps (16 when rows hold many
+// partitions, 4 otherwise). The weights are computed once into shared memory
+// (block-wide max and sum in a fixed tree order), then warp w accumulates the
+// partitions p = w, w + RW, ... with 16-byte loads, four partitions in flight
+// per lane, and the RW warp sums are added in warp order. Normalising the weights before the products makes a single partition
 // reproduce its output exactly. The work is HBM-bound: (d + 2) * 4 bytes per
 // partition read, d * 2 bytes written.
 #include "common.cuh"
@@ -18,15 +18,13 @@
 namespace pkv {
 
 constexpr float kLog2eR = 1.4426950408889634f;
-constexpr int kReduceWarps = 16;
-constexpr int kReduceThreads = kReduceWarps * 32;
-
-template <int D>
-__global__ void __launch_bounds__(kReduceThreads) reduce_kernel(
+template <int D, int kReduceWarps>
+__global__ void __launch_bounds__(kReduceWarps * 32) reduce_kernel(
     uint16_t* __restrict__ out, const float* __restrict__ tmp_out,
     const float* __restrict__ max_logits, const float* __restrict__ exp_sums,
     const int32_t* __restrict__ context_lens, int num_heads, int np_max, int partition_size,
     const int32_t* __restrict__ prefix_blocks, int block_size, int slot_split, int* err) {
+  constexpr int kReduceThreads = kReduceWarps * 32;
   constexpr int V4 = D / 128;  // float4 per lane per partition row
   extern __shared__ float wsh[];  // [np_max] normalised weights
   __shared__ float red[kReduceWarps];
@@ -157,20 +155,39 @@ int launch_reduce(void* out, const float* tmp, const float* ml, const float* es,
   constexpr size_t kMaxSmem = 160 * 1024;  // plus the static accumulators
   if (smem > kMaxSmem) return PKV_ERR_UNSUPPORTED;
   dim3 grid(num_heads, num_seqs);
+  const bool wide = np_max > 32;
   if (head_dim == 128) {
-    static bool done[64] = {false};
-    int rc = ensure_smem(reduce_kernel<128>, kMaxSmem, done, 64);
-    if (rc != PKV_OK) return rc;
-    reduce_kernel<128><<<grid, kReduceThreads, smem, st>>>(
-        static_cast<uint16_t*>(out), tmp, ml, es, context_lens, num_heads, np_max,
-        partition_size, prefix_blocks, block_size, slot_split, device_error_ptr());
+    if (wide) {
+      static bool done[64] = {false};
+      int rc = ensure_smem(reduce_kernel<128, 16>, kMaxSmem, done, 64);
+      if (rc != PKV_OK) return rc;
+      reduce_kernel<128, 16><<<grid, 16 * 32, smem, st>>>(
+          static_cast<uint16_t*>(out), tmp, ml, es, context_lens, num_heads, np_max,
+          partition_size, prefix_blocks, block_size, slot_split, device_error_ptr());
+    } else {
+      static bool done[64] = {false};
+      int rc = ensure_smem(reduce_kernel<128, 4>, kMaxSmem, done, 64);
+      if (rc != PKV_OK) return rc;
+      reduce_kernel<128, 4><<<grid, 4 * 32, smem, st>>>(
+          static_cast<uint16_t*>(out), tmp, ml, es, context_lens, num_heads, np_max,
+          partition_size, prefix_blocks, block_size, slot_split, device_error_ptr());
+    }
   } else {
-    static bool done[64] = {false};
-    int rc = ensure_smem(reduce_kernel<256>, kMaxSmem, done, 64);
-    if (rc != PKV_OK) return rc;
-    reduce_kernel<256><<<grid, kReduceThreads, smem, st>>>(
-        static_cast<uint16_t*>(out), tmp, ml, es, context_lens, num_heads, np_max,
-        partition_size, prefix_blocks, block_size, slot_split, device_error_ptr());
+    if (wide) {
+      static bool done[64] = {false};
+      int rc = ensure_smem(reduce_kernel<256, 16>, kMaxSmem, done, 64);
+      if (rc != PKV_OK) return rc;
+      reduce_kernel<256, 16><<<grid, 16 * 32, smem, st>>>(
+          static_cast<uint16_t*>(out), tmp, ml, es, context_lens, num_heads, np_max,
+          partition_size, prefix_blocks, block_size, slot_split, device_error_ptr());
+    } else {
+      static bool done[64] = {false};
+      int rc = ensure_smem(reduce_kernel<256, 4>, kMaxSmem, done, 64);
+      if (rc != PKV_OK) return rc;
+      reduce_kernel<256, 4><<<grid, 4 * 32, smem, st>>>(
+          static_cast<uint16_t*>(out), tmp, ml, es, context_lens, num_heads, np_max,
+          partition_size, prefix_blocks, block_size, slot_split, device_error_ptr());
+    }
   }
   return launch_status();
 }

@@ -359,3 +359,28 @@ def step_shared_prefix(pw: PagedWorkload, out: List[torch.Tensor], groups, works
                                           pw.context_lens, pw.w.scale, pw.max_context, gs, pre,
                                           maxpre, P, out=out[layer], workspace=workspace,
                                           stream=stream)
+
+
+# ---- several GPUs: sequences are independent, so every rank runs its own
+# batch (weak scaling, no collective on the data path); only the timing is
+# combined across ranks.
+def rank_workload(w: synth.Workload, rank: int, world: int) -> synth.Workload:
+    """The batch of one rank: the same shapes with the rank's own seed."""
+    import dataclasses
+    if world <= 1:
+        return w
+    return dataclasses.replace(w, seed=w.seed + 100 * rank)
+
+
+def max_over_ranks(value: float, dist=None, device="cpu") -> float:
+    """The largest of the ranks' values (e.g. elapsed milliseconds)."""
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(bytes_per_rank_step: int, world: int, ms_per_step: float) -> float:
+    """Whole-job GB/s: every rank's bytes over the slowest rank's step time."""
+    return bytes_per_rank_step * world / (ms_per_step / 1e3) / 1e9
