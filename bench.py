@@ -36,7 +36,8 @@ L2_BYTES = 129 * 1024 * 1024
 DECODE_SOURCES = ["paged_kv_cache_220_gb300/csrc/decode.cu",
                   "paged_kv_cache_220_gb300/csrc/decode_tc.cu",
                   "paged_kv_cache_220_gb300/csrc/decode_params.h",
-                  "paged_kv_cache_220_gb300/csrc/common.cuh"]
+                  "paged_kv_cache_220_gb300/csrc/common.cuh",
+                  "paged_kv_cache_220_gb300/csrc/tc_common.cuh"]
 
 
 def workload_for(name: str):

@@ -23,7 +23,7 @@ INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CUFLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2",
            "--expt-relaxed-constexpr", "-I" + INCLUDE]
-SOURCES = ["api.cu", "kv_cache_write.cu", "copy_blocks.cu", "swap_blocks.cu", "decode.cu", "decode_tc.cu", "reduce.cu",
+SOURCES = ["api.cu", "kv_cache_write.cu", "copy_blocks.cu", "swap_blocks.cu", "decode.cu", "decode_tc.cu", "decode_prefix.cu", "reduce.cu",
            "decode_noalloc.cu", "allocator.cpp", "scheduler.cpp"]
 
 
