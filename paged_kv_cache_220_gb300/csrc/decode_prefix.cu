@@ -6,6 +6,7 @@
 #include "decode_params.h"
 #include "host_util.h"
 #include "tc_common.cuh"
+#include "tmem.cuh"
 
 namespace pkv {
 
@@ -15,15 +16,12 @@ namespace pkv {
 // physical blocks ("How vLLM gets real throughput on H100s ...", section
 // "PagedAttention borrows from operating systems"; "Dissecting vLLM ...",
 // section "PagedAttention: Virtual Memory for KV Cache"). The decode of such a
-// group can read every shared page once: this kernel takes one (group, KV
-// head, partition of the shared prefix) per CTA and computes the logits and
+// group can read every shared page once: the kernel below takes one (group,
+// KV head, partition of the shared prefix) per CTA and computes the logits and
 // P.V of all the group's query heads (members x g <= 128 rows) against each
-// page, the queries being the M side of mma.m16n8k16 (16 rows per consumer
-// warp, Q tile in shared memory with the 128-byte swizzle), the page tokens
-// the N side; the probabilities in the accumulator fragment are the A
-// operand of P.V directly. It writes per-partition partials in the split-decode
-// workspace format; the rest of each member's context goes through the split
-// decode with a block offset, and the merge combines both.
+// page. It writes per-partition partials in the split-decode workspace
+// format; the rest of each member's context goes through the split decode
+// with a block offset, and the merge combines both.
 
 struct PrefixParams {
   const uint16_t* q;
@@ -44,35 +42,57 @@ struct PrefixParams {
   float qscale;
 };
 
-constexpr int kPrefixRows = 128;    // members x g
-constexpr int kPrefixWarps = kPrefixRows / 16;
+// Products on the 5th-generation tensor cores (tcgen05): the group's
+// query rows (padded to M = 128) are the A operand of both products, staged
+// once in shared memory (K-major, 128-byte swizzle); a page's K rows are the
+// B operand of S = Q.K^T (N = B tokens), V the MN-major B operand of
+// O += P.V (N = D) taken straight from the TMA-swizzled page. S (double
+// buffered) and O live in tensor memory. Warps: 0 loads pages (TMA), 1 owns
+// tensor memory and issues the MMAs (one thread), 2-5 run the softmax: thread
+// t of warp w owns query row 32*(w%4) + t, so row maxima and sums need no
+// shuffles. O is rescaled only when a row maximum grows by more than 2^8 (the
+// final O / l uses the same reference, so the result does not depend on when
+// that happens). P goes to shared memory as bf16 high and low parts, two MMAs
+// per k-step, so P carries ~16 significant bits like the other kernels.
 
 template <int D, int BS, int NST>
-struct PrefixGeom {
+struct TmemPrefixGeom {
   static constexpr int kPage = BS * D * 2;
   static constexpr int kStage = 2 * kPage;
-  static constexpr int kQ = kPrefixRows * D * 2;
-  static constexpr int kSmem = 1024 + 1024 + kQ + NST * kStage;
-  static constexpr int kThreads = (kPrefixWarps + 1) * 32;
+  static constexpr int kQ = 128 * D * 2;
+  static constexpr int kP = 128 * BS * 2;  // one P tile
+  static constexpr int kSmem = 1024 + 1024 + kQ + NST * kStage + 2 * kP;
+  static constexpr int kThreads = 6 * 32;
+  static constexpr uint32_t kCols = (D + 2 * BS) <= 256 ? 256u : 512u;
 };
 
 template <int D, int BS, int NST>
-__global__ void __launch_bounds__(PrefixGeom<D, BS, NST>::kThreads)
-    prefix_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
-                  const PrefixParams p) {
-  using G = PrefixGeom<D, BS, NST>;
+__global__ void __launch_bounds__(TmemPrefixGeom<D, BS, NST>::kThreads)
+    prefix_tmem_kernel(const __grid_constant__ CUtensorMap tmk,
+                       const __grid_constant__ CUtensorMap tmv, const PrefixParams p) {
+  using G = TmemPrefixGeom<D, BS, NST>;
   constexpr int PAGE = G::kPage;
   constexpr int KT = D / 16;
-  constexpr int NT = D / 8;  // n-tiles of the output
+  constexpr uint32_t P_SBO = (BS / 8) * 128;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* sbase = smem_raw + (base - raw);
-  uint64_t* full = reinterpret_cast<uint64_t*>(sbase);
-  uint64_t* empty = full + NST;
-  const uint32_t qtile = base + 1024;            // [D/64][128 rows][128 B]
+  uint64_t* kv_full = reinterpret_cast<uint64_t*>(sbase);
+  uint64_t* kv_empty = kv_full + NST;
+  uint64_t* s_full = kv_empty + NST;   // [2]
+  uint64_t* s_empty = s_full + 2;      // [2]
+  uint64_t* p_full = s_empty + 2;
+  uint64_t* o_done = p_full + 1;
+  uint64_t* drained = o_done + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sbase + 1000);
+  const uint32_t qtile = base + 1024;
   const uint32_t ring = qtile + G::kQ;
+  const uint32_t p_hi = ring + NST * G::kStage;
+  const uint32_t p_lo = p_hi + G::kP;
   uint8_t* qtile_p = sbase + 1024;
+  uint8_t* p_hi_p = sbase + (p_hi - base);
+  uint8_t* p_lo_p = sbase + (p_lo - base);
 
   const int part = blockIdx.x, h = blockIdx.y, gi = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -80,7 +100,7 @@ __global__ void __launch_bounds__(PrefixGeom<D, BS, NST>::kThreads)
   const int s0 = p.group_start[gi];
   const int members = p.group_start[gi + 1] - s0;
   const int R = members * g;
-  if (members <= 0 || R > kPrefixRows) {
+  if (members <= 0 || R > 128) {
     if (threadIdx.x == 0 && members > 0) report_error(p.err, PKV_DEVERR_CONTEXT);
     return;
   }
@@ -89,17 +109,24 @@ __global__ void __launch_bounds__(PrefixGeom<D, BS, NST>::kThreads)
   if (blk_begin >= pre) return;
   const int blk_end = min(pre, blk_begin + p.partition_blocks);
   const int nblk = blk_end - blk_begin;
-  const int nwa = (R + 15) / 16;  // consumer warps with rows
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < NST; ++i) {
-      mbar_init(&full[i], 1);
-      mbar_init(&empty[i], nwa);
+      mbar_init(&kv_full[i], 1);
+      mbar_init(&kv_empty[i], 1);
     }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&s_empty[i], 128);
+    }
+    mbar_init(p_full, 128);
+    mbar_init(o_done, 1);
+    mbar_init(drained, 1);
     fence_mbar_init();
   }
-  // Q tile: row r = member * g + jj, 16-byte units, rows >= R are zero
-  for (int u = threadIdx.x; u < kPrefixRows * (D / 8); u += G::kThreads) {
+  if (warp == 1) tmem_alloc(tmem_slot, G::kCols);
+  // Q tile: row r = member * g + jj, rows >= R are zero
+  for (int u = threadIdx.x; u < 128 * (D / 8); u += G::kThreads) {
     const int r = u / (D / 8);
     const int c = (u % (D / 8)) * 8;
     uint4 v = make_uint4(0u, 0u, 0u, 0u);
@@ -108,172 +135,202 @@ __global__ void __launch_bounds__(PrefixGeom<D, BS, NST>::kThreads)
       const int hq = h * g + r % g;
       v = *reinterpret_cast<const uint4*>(p.q + (static_cast<int64_t>(s) * p.num_heads + hq) * D + c);
     }
-    const uint32_t a = qtile + (c >> 6) * (kPrefixRows * 128) + r * 128 + (c & 63) * 2;
+    const uint32_t a = qtile + (c >> 6) * (128 * 128) + r * 128 + (c & 63) * 2;
     *reinterpret_cast<uint4*>(qtile_p + ((a ^ (((a >> 7) & 7u) << 4)) - qtile)) = v;
   }
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  tc_fence_before();
   __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t t_o = tmem;                 // columns [0, D)
+  const uint32_t t_s = tmem + D;             // columns [D, D + 2B)
 
   int issued = 0;
-  if (warp == kPrefixWarps) {
+  if (warp == 0) {
     if (lane == 0) {
       const int32_t* bt = p.block_tables + static_cast<int64_t>(s0) * p.max_blocks_per_seq;
       for (int it = 0; it < nblk; ++it) {
         const int st = it % NST;
-        if (it >= NST && !mbar_wait(&empty[st], ((it / NST) - 1) & 1, p.err)) break;
+        if (it >= NST && !mbar_wait(&kv_empty[st], ((it / NST) - 1) & 1, p.err)) break;
         const int32_t pb = bt[blk_begin + it];
         issued = it + 1;
         if (pb < 0 || pb >= p.num_blocks) {
           report_error(p.err, PKV_DEVERR_BLOCK_ID);
-          mbar_arrive(&full[st]);
+          mbar_arrive(&kv_full[st]);
           continue;
         }
         const uint32_t kdst = ring + st * G::kStage;
         const int y = (pb * p.num_kv_heads + h) * BS;
-        mbar_arrive_expect_tx(&full[st], 2 * PAGE);
+        mbar_arrive_expect_tx(&kv_full[st], 2 * PAGE);
 #pragma unroll
         for (int c = 0; c < D / 64; ++c) {
-          tma_load_2d(kdst + c * BS * 128, &tmk, c * 64, y, &full[st]);
-          tma_load_2d(kdst + PAGE + c * BS * 128, &tmv, c * 64, y, &full[st]);
+          tma_load_2d(kdst + c * BS * 128, &tmk, c * 64, y, &kv_full[st]);
+          tma_load_2d(kdst + PAGE + c * BS * 128, &tmv, c * 64, y, &kv_full[st]);
         }
       }
     }
-  } else if (warp < nwa) {
-    float o[NT][4];
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc_qk = umma_idesc_bf16(128, BS, false);
+      constexpr uint32_t idesc_pv = umma_idesc_bf16(128, D, true);
+      bool ok = true;
+      for (int it = 0; it <= nblk && ok; ++it) {
+        if (it < nblk) {
+          const int st = it % NST;
+          if (!mbar_wait(&kv_full[st], (it / NST) & 1, p.err)) break;
+          if (it >= 2 && !mbar_wait(&s_empty[it & 1], ((it >> 1) - 1) & 1, p.err)) break;
+          tc_fence_after();
+          const uint32_t kp = ring + st * G::kStage;
 #pragma unroll
-    for (int n = 0; n < NT; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
-    float ma = -INFINITY, mb = -INFINITY, la = 0.f, lb = 0.f;  // rows lane/4 and lane/4+8
-    const float qs = p.qscale;
-    const int qrow = warp * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
-    const int qcol = (lane >> 4) * 16;  // bytes
-    for (int it = 0; it < nblk; ++it) {
-      const int st = it % NST;
-      if (!mbar_wait(&full[st], (it / NST) & 1, p.err)) break;
-      const uint32_t kp = ring + st * G::kStage;
-      const uint32_t vp = kp + PAGE;
-#pragma unroll 1
-      for (int r0 = 0; r0 < BS; r0 += 16) {
-        // S[16 rows x 16 tokens] = Q_rows . K_slice^T; even and odd k-steps
-        // accumulate separately (four chains of KT/2 dependent products)
-        float s0f[4] = {0.f, 0.f, 0.f, 0.f}, s1f[4] = {0.f, 0.f, 0.f, 0.f};
-        float s0g[4] = {0.f, 0.f, 0.f, 0.f}, s1g[4] = {0.f, 0.f, 0.f, 0.f};
-        const int krow = r0 + (lane & 7) + ((lane >> 4) & 1) * 8;
-        const int kcol = ((lane >> 3) & 1) * 16;  // bytes
-#pragma unroll
-        for (int k = 0; k < KT; ++k) {
-          uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
-          const uint32_t qa = qtile + (k >> 2) * (kPrefixRows * 128) + qrow * 128 + ((k & 3) * 32 + qcol);
-          ldsm_x4(qa ^ (((qa >> 7) & 7u) << 4), a0, a1, a2, a3);
-          ldsm_x4(swz_bytes<BS>(kp, krow, k * 32 + kcol), b0, b1, b2, b3);
-          mma_bf16((k & 1) ? s0g : s0f, a0, a1, a2, a3, b0, b1);
-          mma_bf16((k & 1) ? s1g : s1f, a0, a1, a2, a3, b2, b3);
-        }
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          s0f[i] += s0g[i];
-          s1f[i] += s1g[i];
-        }
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          s0f[i] *= qs;
-          s1f[i] *= qs;
-        }
-        float mxa = fmaxf(fmaxf(s0f[0], s0f[1]), fmaxf(s1f[0], s1f[1]));
-        float mxb = fmaxf(fmaxf(s0f[2], s0f[3]), fmaxf(s1f[2], s1f[3]));
-        mxa = fmaxf(mxa, __shfl_xor_sync(0xffffffffu, mxa, 1));
-        mxa = fmaxf(mxa, __shfl_xor_sync(0xffffffffu, mxa, 2));
-        mxb = fmaxf(mxb, __shfl_xor_sync(0xffffffffu, mxb, 1));
-        mxb = fmaxf(mxb, __shfl_xor_sync(0xffffffffu, mxb, 2));
-        const float na = fmaxf(ma, mxa), nb = fmaxf(mb, mxb);
-        if (__any_sync(0xffffffffu, (na > ma) || (nb > mb))) {
-          const float ca = fast_exp2(ma - na), cb = fast_exp2(mb - nb);
-          la *= ca;
-          lb *= cb;
-#pragma unroll
-          for (int n = 0; n < NT; ++n) {
-            o[n][0] *= ca;
-            o[n][1] *= ca;
-            o[n][2] *= cb;
-            o[n][3] *= cb;
+          for (int k = 0; k < KT; ++k) {
+            const uint64_t a = umma_sdesc(qtile + (k >> 2) * (128 * 128) + (k & 3) * 32, 16, 1024, 2);
+            const uint64_t b = umma_sdesc(kp + (k >> 2) * (BS * 128) + (k & 3) * 32, 16, 1024, 2);
+            umma_bf16(t_s + (it & 1) * BS, a, b, idesc_qk, k > 0 ? 1u : 0u);
           }
-          ma = na;
-          mb = nb;
+          umma_commit(&s_full[it & 1]);
         }
-        float pv[8];
-        pv[0] = fast_exp2(s0f[0] - ma);
-        pv[1] = fast_exp2(s0f[1] - ma);
-        pv[2] = fast_exp2(s0f[2] - mb);
-        pv[3] = fast_exp2(s0f[3] - mb);
-        pv[4] = fast_exp2(s1f[0] - ma);
-        pv[5] = fast_exp2(s1f[1] - ma);
-        pv[6] = fast_exp2(s1f[2] - mb);
-        pv[7] = fast_exp2(s1f[3] - mb);
-        la += pv[0] + pv[1] + pv[4] + pv[5];
-        lb += pv[2] + pv[3] + pv[6] + pv[7];
-        // P as the A operand (rows = queries, k = tokens), bf16 high + low parts
-        uint32_t ah[4], al[4];
+        if (it >= 1) {
+          const int j = it - 1;
+          if (!mbar_wait(p_full, j & 1, p.err)) break;
+          tc_fence_after();
+          const uint32_t vp = ring + (j % NST) * G::kStage + PAGE;
+#pragma unroll
+          for (int kk = 0; kk < BS / 16; ++kk) {
+            const uint64_t bv = umma_sdesc(vp + kk * 2048, BS * 128, 1024, 2);
+            umma_bf16(t_o, umma_sdesc(p_hi + kk * 256, 128, P_SBO, 0), bv, idesc_pv,
+                      (j > 0 || kk > 0) ? 1u : 0u);
+            umma_bf16(t_o, umma_sdesc(p_lo + kk * 256, 128, P_SBO, 0), bv, idesc_pv, 1u);
+          }
+          umma_commit(o_done);
+          umma_commit(&kv_empty[j % NST]);
+        }
+      }
+      // every tensor-core operation issued here has finished before tensor
+      // memory is released
+      umma_commit(drained);
+      (void)mbar_wait(drained, 0, p.err);
+      (void)ok;
+    }
+  } else {
+    // softmax: one query row per thread
+    const int row = 32 * (warp & 3) + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+    const float qs = p.qscale;
+    float m_used = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int it = 0; it < nblk; ++it) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&s_full[it & 1], (it >> 1) & 1, p.err))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      float sv[BS];
+#pragma unroll
+      for (int c = 0; c < BS; c += 16) tmem_ld16(t_s + lane_off + (it & 1) * BS + c, sv + c);
+      tc_fence_before();
+      mbar_arrive(&s_empty[it & 1]);
+      float mx = -INFINITY;
+#pragma unroll
+      for (int t = 0; t < BS; ++t) {
+        sv[t] *= qs;
+        mx = fmaxf(mx, sv[t]);
+      }
+      if (it >= 1) {
+        if (!__all_sync(0xffffffffu, mbar_wait(o_done, (it - 1) & 1, p.err))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+      }
+      // tensor-memory loads and stores are warp-collective: the rescale runs
+      // on every lane of the warp if any lane needs it (alpha = 1 elsewhere)
+      const bool want = mx > m_used + 8.f;
+      const float alpha = want ? fast_exp2(m_used - mx) : 1.f;  // 0 while m_used is -inf
+      if (it >= 1 && __any_sync(0xffffffffu, want)) {
+#pragma unroll 1
+        for (int c = 0; c < D; c += 16) {
+          float ov[16];
+          tmem_ld16(t_o + lane_off + c, ov);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) ov[i] *= alpha;
+          tmem_st16(t_o + lane_off + c, ov);
+        }
+      }
+      if (want) {
+        l *= alpha;
+        m_used = mx;
+      }
+      float pv[BS];
+#pragma unroll
+      for (int t = 0; t < BS; ++t) {
+        pv[t] = fast_exp2(sv[t] - m_used);
+        l += pv[t];
+      }
+      // row `row` of the P tiles: [m-group][k-chunk][8 rows][8 tokens]
+#pragma unroll
+      for (int t = 0; t < BS; t += 8) {
+        uint32_t hw[4], lw[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          ah[i] = pack_bf16(pv[2 * i], pv[2 * i + 1]);
-          const __nv_bfloat162 hv = *reinterpret_cast<const __nv_bfloat162*>(&ah[i]);
-          al[i] = pack_bf16(pv[2 * i] - __low2float(hv), pv[2 * i + 1] - __high2float(hv));
+          hw[i] = pack_bf16(pv[t + 2 * i], pv[t + 2 * i + 1]);
+          const __nv_bfloat162 hv = *reinterpret_cast<const __nv_bfloat162*>(&hw[i]);
+          lw[i] = pack_bf16(pv[t + 2 * i] - __low2float(hv), pv[t + 2 * i + 1] - __high2float(hv));
         }
-        // fragment order a0 (row a, tokens 0-7), a1 (row b, 0-7), a2 (row a, 8-15), a3 (row b, 8-15)
-        const int vrow = r0 + (lane & 7) + ((lane >> 3) & 1) * 8;
-        const int vcol = ((lane >> 4) & 1) * 16;  // bytes
-#pragma unroll
-        for (int j = 0; j < KT; ++j) {
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4_t(swz_bytes<BS>(vp, vrow, j * 32 + vcol), b0, b1, b2, b3);
-          mma_bf16(o[2 * j], ah[0], ah[1], ah[2], ah[3], b0, b1);
-          mma_bf16(o[2 * j], al[0], al[1], al[2], al[3], b0, b1);
-          mma_bf16(o[2 * j + 1], ah[0], ah[1], ah[2], ah[3], b2, b3);
-          mma_bf16(o[2 * j + 1], al[0], al[1], al[2], al[3], b2, b3);
-        }
+        const uint32_t off = (row >> 3) * P_SBO + (t >> 3) * 128 + (row & 7) * 16;
+        *reinterpret_cast<uint4*>(p_hi_p + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+        *reinterpret_cast<uint4*>(p_lo_p + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[st]);
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      tc_fence_before();
+      mbar_arrive(p_full);
     }
-    la += __shfl_xor_sync(0xffffffffu, la, 1);
-    la += __shfl_xor_sync(0xffffffffu, la, 2);
-    lb += __shfl_xor_sync(0xffffffffu, lb, 1);
-    lb += __shfl_xor_sync(0xffffffffu, lb, 2);
-    // partials of rows a and b
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      const int r = warp * 16 + (lane >> 2) + half * 8;
-      if (r >= R) continue;
-      const float m = half ? mb : ma;
-      const float l = half ? lb : la;
-      const float inv = l > 0.f ? 1.f / l : 0.f;
-      const int s = s0 + r / g;
-      const int64_t hq = static_cast<int64_t>(s) * p.num_heads + h * g + r % g;
+    ok = __all_sync(0xffffffffu, ok);
+    if (ok && nblk > 0 && mbar_wait(o_done, (nblk - 1) & 1, p.err)) {
+      tc_fence_after();
+      // every lane runs the same (warp-collective) loads; rows past the
+      // group's query rows store nothing
+      const bool live = row < R;
+      const int s = s0 + (live ? row / g : 0);
+      const int64_t hq = static_cast<int64_t>(s) * p.num_heads + h * g + (live ? row % g : 0);
       float* dst = p.tmp_out + (hq * p.np_max + part) * D;
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll 1
+      for (int c = 0; c < D; c += 16) {
+        float ov[16];
+        tmem_ld16(t_o + lane_off + c, ov);
+        if (live) {
 #pragma unroll
-      for (int n = 0; n < NT; ++n) {
-        const float2 v = half ? make_float2(o[n][2] * inv, o[n][3] * inv)
-                              : make_float2(o[n][0] * inv, o[n][1] * inv);
-        *reinterpret_cast<float2*>(dst + n * 8 + (lane & 3) * 2) = v;
+          for (int i = 0; i < 16; i += 4)
+            *reinterpret_cast<float4*>(dst + c + i) =
+                make_float4(ov[i] * inv, ov[i + 1] * inv, ov[i + 2] * inv, ov[i + 3] * inv);
+        }
       }
-      if ((lane & 3) == 0) {
-        p.max_logits[hq * p.np_max + part] = m * kLn2Tc;
+      if (live) {
+        p.max_logits[hq * p.np_max + part] = m_used * kLn2Tc;
         p.exp_sums[hq * p.np_max + part] = l;
       }
     }
   }
+  tc_fence_before();
   __syncthreads();
-  if (warp == kPrefixWarps && lane == 0) {
+  if (warp == 0 && lane == 0) {
     const int first = issued > NST ? issued - NST : 0;
     for (int it = first; it < issued; ++it)
-      if (!mbar_wait(&full[it % NST], (it / NST) & 1, p.err)) break;
+      if (!mbar_wait(&kv_full[it % NST], (it / NST) & 1, p.err)) break;
+  }
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, G::kCols);
   }
 }
 
 template <int D, int BS, int NST>
-static int launch_prefix_t(const PrefixParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
-                           dim3 grid, cudaStream_t st) {
-  using G = PrefixGeom<D, BS, NST>;
+static int launch_prefix_tmem_t(const PrefixParams& p, const CUtensorMap& tk,
+                                const CUtensorMap& tv, dim3 grid, cudaStream_t st) {
+  using G = TmemPrefixGeom<D, BS, NST>;
   static bool done[64] = {false};
-  auto kern = prefix_kernel<D, BS, NST>;
+  auto kern = prefix_tmem_kernel<D, BS, NST>;
   int rc = ensure_smem(kern, G::kSmem, done, 64);
   if (rc != PKV_OK) return rc;
   kern<<<grid, G::kThreads, G::kSmem, st>>>(tk, tv, p);
@@ -288,10 +345,10 @@ int launch_prefix(const PrefixParams& p, const void* k_cache, const void* v_cach
   if (rc != PKV_OK) return rc;
   rc = pool_tensor_map(&tv, v_cache, rows, head_dim, block_size, false);
   if (rc != PKV_OK) return rc;
-  if (head_dim == 256 && block_size == 16) return launch_prefix_t<256, 16, 4>(p, tk, tv, grid, st);
-  if (head_dim == 256 && block_size == 32) return launch_prefix_t<256, 32, 2>(p, tk, tv, grid, st);
-  if (head_dim == 128 && block_size == 16) return launch_prefix_t<128, 16, 8>(p, tk, tv, grid, st);
-  return launch_prefix_t<128, 32, 4>(p, tk, tv, grid, st);
+  if (head_dim == 256 && block_size == 16) return launch_prefix_tmem_t<256, 16, 4>(p, tk, tv, grid, st);
+  if (head_dim == 256 && block_size == 32) return launch_prefix_tmem_t<256, 32, 2>(p, tk, tv, grid, st);
+  if (head_dim == 128 && block_size == 16) return launch_prefix_tmem_t<128, 16, 8>(p, tk, tv, grid, st);
+  return launch_prefix_tmem_t<128, 32, 4>(p, tk, tv, grid, st);
 }
 
 }  // namespace pkv

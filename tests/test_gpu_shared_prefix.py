@@ -22,13 +22,14 @@ def _lib():
     pkv.set_device_check(None)
 
 
-@pytest.mark.parametrize("prompt,B,P,rollouts", [(40, 16, 32, 4), (48, 16, 16, 16),
-                                                  (2040, 16, 512, 16), (200, 32, 64, 3),
-                                                  (100, 16, 512, 21)])
-def test_shared_prefix_matches_oracle(prompt, B, P, rollouts, _lib):
+@pytest.mark.parametrize("prompt,B,P,rollouts,d", [(40, 16, 32, 4, 256), (48, 16, 16, 16, 256),
+                                                    (2040, 16, 512, 16, 256), (200, 32, 64, 3, 256),
+                                                    (100, 16, 512, 21, 256), (300, 16, 64, 16, 128),
+                                                    (330, 32, 128, 5, 128)])
+def test_shared_prefix_matches_oracle(prompt, B, P, rollouts, d, _lib):
     w = synth.cow(prompt_len=prompt, prompts=2, rollouts=rollouts)
     comp = w.extra["completion"][:2 * rollouts]
-    w = dataclasses.replace(w, block_size=B, ctx=[prompt + (c % 300) + 1 for c in comp],
+    w = dataclasses.replace(w, block_size=B, head_dim=d, ctx=[prompt + (c % 300) + 1 for c in comp],
                             slack_blocks=64)
     if rollouts * w.num_heads // w.num_kv_heads > 128:
         pytest.skip("group larger than one prefix CTA")
