@@ -38,11 +38,11 @@ int launch_decode_tc(const DecodeParams& p, const void* k_cache, const void* v_c
 
 // Merge of split partials (reduce.cu). With prefix_blocks == NULL the slots of
 // sequence s are [0, ceil(ctx/P)); otherwise [0, npre) and [slot_split,
-// slot_split + nsuf) with npre = ceil(prefix_blocks[s]*B/P) and nsuf =
-// ceil((ctx - prefix_blocks[s]*B)/P).
+// slot_split + nsuf) with npre = ceil(prefix_blocks[s]*B/Pp) (Pp = the prefix
+// partition size) and nsuf = ceil((ctx - prefix_blocks[s]*B)/P).
 int launch_reduce(void* out, const float* tmp, const float* ml, const float* es,
                   const int32_t* context_lens, int num_seqs, int num_heads, int head_dim,
                   int np_max, int partition_size, const int32_t* prefix_blocks, int block_size,
-                  int slot_split, cudaStream_t st);
+                  int slot_split, int prefix_partition, cudaStream_t st);
 
 }  // namespace pkv

@@ -23,7 +23,8 @@ __global__ void __launch_bounds__(kReduceWarps * 32) reduce_kernel(
     uint16_t* __restrict__ out, const float* __restrict__ tmp_out,
     const float* __restrict__ max_logits, const float* __restrict__ exp_sums,
     const int32_t* __restrict__ context_lens, int num_heads, int np_max, int partition_size,
-    const int32_t* __restrict__ prefix_blocks, int block_size, int slot_split, int* err) {
+    const int32_t* __restrict__ prefix_blocks, int block_size, int slot_split,
+    int prefix_partition, int* err) {
   constexpr int kReduceThreads = kReduceWarps * 32;
   constexpr int V4 = D / 128;  // float4 per lane per partition row
   extern __shared__ float wsh[];  // [np_max] normalised weights
@@ -38,7 +39,7 @@ __global__ void __launch_bounds__(kReduceWarps * 32) reduce_kernel(
   int npre = 0, nsuf = ctx > 0 ? (ctx + partition_size - 1) / partition_size : 0;
   if (prefix_blocks != nullptr) {
     const int ptok = prefix_blocks[s] * block_size;
-    npre = (ptok + partition_size - 1) / partition_size;
+    npre = (ptok + prefix_partition - 1) / prefix_partition;
     nsuf = ctx > ptok ? (ctx - ptok + partition_size - 1) / partition_size : 0;
   }
   if (slot_split + nsuf > np_max || npre > slot_split) {
@@ -150,7 +151,7 @@ namespace pkv {
 int launch_reduce(void* out, const float* tmp, const float* ml, const float* es,
                   const int32_t* context_lens, int num_seqs, int num_heads, int head_dim,
                   int np_max, int partition_size, const int32_t* prefix_blocks, int block_size,
-                  int slot_split, cudaStream_t st) {
+                  int slot_split, int prefix_partition, cudaStream_t st) {
   const size_t smem = static_cast<size_t>(np_max > 0 ? np_max : 1) * sizeof(float);
   constexpr size_t kMaxSmem = 160 * 1024;  // plus the static accumulators
   if (smem > kMaxSmem) return PKV_ERR_UNSUPPORTED;
@@ -163,14 +164,16 @@ int launch_reduce(void* out, const float* tmp, const float* ml, const float* es,
       if (rc != PKV_OK) return rc;
       reduce_kernel<128, 16><<<grid, 16 * 32, smem, st>>>(
           static_cast<uint16_t*>(out), tmp, ml, es, context_lens, num_heads, np_max,
-          partition_size, prefix_blocks, block_size, slot_split, device_error_ptr());
+          partition_size, prefix_blocks, block_size, slot_split,
+          prefix_partition > 0 ? prefix_partition : partition_size, device_error_ptr());
     } else {
       static bool done[64] = {false};
       int rc = ensure_smem(reduce_kernel<128, 4>, kMaxSmem, done, 64);
       if (rc != PKV_OK) return rc;
       reduce_kernel<128, 4><<<grid, 4 * 32, smem, st>>>(
           static_cast<uint16_t*>(out), tmp, ml, es, context_lens, num_heads, np_max,
-          partition_size, prefix_blocks, block_size, slot_split, device_error_ptr());
+          partition_size, prefix_blocks, block_size, slot_split,
+          prefix_partition > 0 ? prefix_partition : partition_size, device_error_ptr());
     }
   } else {
     if (wide) {
@@ -179,14 +182,16 @@ int launch_reduce(void* out, const float* tmp, const float* ml, const float* es,
       if (rc != PKV_OK) return rc;
       reduce_kernel<256, 16><<<grid, 16 * 32, smem, st>>>(
           static_cast<uint16_t*>(out), tmp, ml, es, context_lens, num_heads, np_max,
-          partition_size, prefix_blocks, block_size, slot_split, device_error_ptr());
+          partition_size, prefix_blocks, block_size, slot_split,
+          prefix_partition > 0 ? prefix_partition : partition_size, device_error_ptr());
     } else {
       static bool done[64] = {false};
       int rc = ensure_smem(reduce_kernel<256, 4>, kMaxSmem, done, 64);
       if (rc != PKV_OK) return rc;
       reduce_kernel<256, 4><<<grid, 4 * 32, smem, st>>>(
           static_cast<uint16_t*>(out), tmp, ml, es, context_lens, num_heads, np_max,
-          partition_size, prefix_blocks, block_size, slot_split, device_error_ptr());
+          partition_size, prefix_blocks, block_size, slot_split,
+          prefix_partition > 0 ? prefix_partition : partition_size, device_error_ptr());
     }
   }
   return launch_status();
@@ -220,5 +225,6 @@ extern "C" int pkv_paged_attention_reduce(void* out, const void* workspace,
   const float* ml = ws ? ws + rows * head_dim : nullptr;
   const float* es = ws ? ml + rows : nullptr;
   return launch_reduce(out, tmp, ml, es, context_lens, num_seqs, num_heads, head_dim, np_arg,
-                       partition_size, nullptr, 1, 0, static_cast<cudaStream_t>(stream));
+                       partition_size, nullptr, 1, 0, partition_size,
+                       static_cast<cudaStream_t>(stream));
 }
