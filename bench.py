@@ -365,10 +365,7 @@ def main():
     # dispatch per step), or eager launches with --graph 0
     graph = None
     if args.graph:
-        if cascade is not None:
-            graph = capture(one_step)
-        else:
-            graph = workload.capture_step(pw, out, ws, P)
+        graph = workload.capture_step(pw, out, ws, P, groups=cascade)
         for _ in range(args.warmup):
             graph.replay()
     if dist is not None:
@@ -455,21 +452,6 @@ def main():
     if dist is not None:
         dist.destroy_process_group()
     return 0
-
-
-def capture(fn):
-    """CUDA graph of fn() (run once eagerly on the capture stream first)."""
-    import torch
-    s = torch.cuda.Stream()
-    s.wait_stream(torch.cuda.current_stream())
-    with torch.cuda.stream(s):
-        fn()
-    torch.cuda.current_stream().wait_stream(s)
-    torch.cuda.synchronize()
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g, stream=s):
-        fn()
-    return g
 
 
 def time_copy_blocks(pw, args):

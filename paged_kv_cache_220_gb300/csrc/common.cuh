@@ -30,6 +30,29 @@ __device__ __forceinline__ unsigned long long global_ns() {
   return t;
 }
 
+// Programmatic dependent launch (sm_90+): a kernel that calls
+// allow_dependents() lets the next launch on its stream that was made with the
+// programmatic-serialization attribute start before it finishes;
+// wait_prerequisite() in that next launch blocks until the earlier grid has
+// completed and its memory writes are visible. Both are no-ops for launches
+// made without the attribute.
+__device__ __forceinline__ void allow_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void wait_prerequisite() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Waits for the prerequisite grid when it goes out of scope (on every return
+// path of the kernel that declares it) if `on`.
+struct PrerequisiteTail {
+  bool on;
+  __device__ __forceinline__ ~PrerequisiteTail() {
+    if (on) wait_prerequisite();
+  }
+};
+
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

@@ -29,6 +29,12 @@ struct DecodeParams {
   int cluster;           // one pass: CTAs (a thread-block cluster) per (seq, KV head)
   const int32_t* block_offset;  // split form: first logical block per sequence (NULL = 0)
   int slot_offset;              // split form: partial p is stored at slot slot_offset + p
+  // 1: launched as a programmatic dependent of the kernel before it on the
+  // stream (it may start while that kernel runs; it must not read what that
+  // kernel writes). One thread waits for that kernel before its CTA exits, so
+  // this launch completes only after the earlier one: work queued behind it
+  // sees both results.
+  int overlap_prev;
   float qscale;          // scale * log2(e)
 };
 

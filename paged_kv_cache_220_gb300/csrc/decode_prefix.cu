@@ -97,6 +97,10 @@ __global__ void __launch_bounds__(TmemPrefixGeom<D, BS, NST>::kThreads)
   uint8_t* qtile_p = sbase + 1024;
   uint8_t* p_hi_p = sbase + (p_hi - base);
   uint8_t* p_lo_p = sbase + (p_lo - base);
+  // the members' own-block decode launched next may start on the room this
+  // grid leaves free (it writes other workspace slots and reads no output of
+  // this kernel)
+  allow_dependents();
 
   const int part = blockIdx.x, h = blockIdx.y, gi = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -493,6 +497,7 @@ extern "C" int pkv_paged_attention_decode_shared_prefix(
   p.exp_sums = es;
   p.block_offset = prefix_blocks;
   p.slot_offset = npp;
+  p.overlap_prev = (num_groups > 0 && npp > 0) ? 1 : 0;
   rc = launch_decode_tc(p, k_cache, v_cache, cache.head_dim, cache.block_size, false,
                         dim3(nps, cache.num_kv_heads, num_seqs), st);
   if (rc != PKV_OK) return rc;

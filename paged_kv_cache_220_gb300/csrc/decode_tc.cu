@@ -78,6 +78,9 @@ __global__ void __launch_bounds__(TcGeom<D, BS, FP8, NW, NST>::kThreads)
   const int part = blockIdx.x;
   const int h = blockIdx.y;
   const int s = blockIdx.z;
+  // overlapped with the kernel before it: thread 0 of CTA (0, 0, 0), which
+  // every launch has, keeps the grid alive until that kernel has completed
+  PrerequisiteTail tail{p.overlap_prev != 0 && threadIdx.x == 0 && part == 0 && h == 0 && s == 0};
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int g = p.group;
@@ -490,9 +493,24 @@ static int launch_tc(const DecodeParams& p_in, const CUtensorMap& tk, const CUte
   DecodeParams p = p_in;
   if (p.partition_blocks > 0 || p.cluster <= 1) {
     p.cluster = 1;
+    if (p.overlap_prev) {
+      cudaLaunchConfig_t cfg = {};
+      cudaLaunchAttribute attr[1];
+      cfg.gridDim = grid;
+      cfg.blockDim = dim3(G::kThreads);
+      cfg.dynamicSmemBytes = G::kSmem;
+      cfg.stream = st;
+      attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+      attr[0].val.programmaticStreamSerializationAllowed = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      if (cudaLaunchKernelEx(&cfg, kern, tk, tv, p) != cudaSuccess) return PKV_ERR_CUDA;
+      return launch_status();
+    }
     kern<<<grid, G::kThreads, G::kSmem, st>>>(tk, tv, p);
     return launch_status();
   }
+  p.overlap_prev = 0;
   // One pass: a cluster of C CTAs per (KV head, sequence), C a power of two
   // <= 16; shrink C if the device cannot co-schedule clusters that large.
   static bool nonportable[64] = {false};

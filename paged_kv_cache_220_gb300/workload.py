@@ -204,7 +204,7 @@ def step(pw: PagedWorkload, out: List[torch.Tensor], workspace: Optional[torch.T
 
 
 def capture_step(pw: PagedWorkload, out: List[torch.Tensor], workspace: Optional[torch.Tensor],
-                 partition_size: Optional[int] = None, copy_pairs: bool = False):
+                 partition_size: Optional[int] = None, copy_pairs: bool = False, groups=None):
     """Record one decode step (every layer's cache write, decode and merge;
     with copy_pairs also the copy-on-write block copies) as a CUDA graph, so a
     step is replayed with one launch from the host instead of 3-4 per layer
@@ -217,24 +217,29 @@ def capture_step(pw: PagedWorkload, out: List[torch.Tensor], workspace: Optional
     slots, block tables and context lengths in place, then replay().
     copy_pairs records the copy-on-write copies too; that is only right for
     the divergence iteration itself, since a clone later also holds tokens
-    written after the copy.
+    written after the copy. With groups (from prefix_groups) the step uses the
+    shared-prefix decode.
     Every kernel is run once eagerly first (on the capture stream), so the
     library's one-time per-device set-up happens outside the capture."""
-    s = torch.cuda.Stream()
-    s.wait_stream(torch.cuda.current_stream())
-    with torch.cuda.stream(s):
+
+    def one():
         if copy_pairs and pw.cow_pairs is not None:
             for st in pw.layers:
                 pkv.copy_blocks(st.k_cache, st.v_cache, pw.cow_pairs)
-        step(pw, out, workspace, partition_size)
+        if groups is not None:
+            step_shared_prefix(pw, out, groups, workspace, partition_size)
+        else:
+            step(pw, out, workspace, partition_size)
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        one()
     torch.cuda.current_stream().wait_stream(s)
     torch.cuda.synchronize()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=s):
-        if copy_pairs and pw.cow_pairs is not None:
-            for st in pw.layers:
-                pkv.copy_blocks(st.k_cache, st.v_cache, pw.cow_pairs)
-        step(pw, out, workspace, partition_size)
+        one()
     return g
 
 
