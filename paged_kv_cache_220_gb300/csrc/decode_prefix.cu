@@ -42,61 +42,71 @@ struct PrefixParams {
   float qscale;
 };
 
-// Products on the 5th-generation tensor cores (tcgen05): the group's
-// query rows (padded to M = 128) are the A operand of both products, staged
-// once in shared memory (K-major, 128-byte swizzle); a page's K rows are the
-// B operand of S = Q.K^T (N = B tokens), V the MN-major B operand of
-// O += P.V (N = D) taken straight from the TMA-swizzled page. S (double
-// buffered) and O live in tensor memory. Warps: 0 loads pages (TMA), 1 owns
-// tensor memory and issues the MMAs (one thread), 2-5 run the softmax: thread
-// t of warp w owns query row 32*(w%4) + t, so row maxima and sums need no
-// shuffles. O is rescaled only when a row maximum grows by more than 2^8 (the
-// final O / l uses the same reference, so the result does not depend on when
-// that happens). P goes to shared memory as bf16 high and low parts, two MMAs
-// per k-step, so P carries ~16 significant bits like the other kernels. P is
-// double buffered by page parity (with a ready and a consumed barrier per
-// buffer), so the softmax of page i overlaps the P.V of page i - 1.
+// Products on the 5th-generation tensor cores (tcgen05). The group's query
+// rows (padded to M = 128) are the A operand of S = Q.K^T, P the A operand of
+// O += P.V; both sit in tensor memory (row i in lane i). A step covers 64
+// tokens (4 pages of 16 or 2 of 32): the step's K rows are the B operand of S
+// (N = 64), its V rows, 16 tokens per k-step, the MN-major B operand of P.V
+// (N = D); both come straight from the TMA-swizzled pages. Few wide MMAs
+// matter here: a 128 x 16 x 16 product costs the tensor core about as long
+// as a 128 x 64 x 16 one, so a page-sized S (N = 16) left the kernel bound by
+// the MMA issue rate.
+//
+// Tensor memory: O [D] fp32, S [2 steps][64] fp32, Q [D/2] bf16 pairs. P of a
+// step is written over that step's S columns (bf16 high parts in the first
+// 32 columns, the low parts, i.e. the rounding remainders, in the next 32),
+// so S of step t + 2 is issued only after P.V of step t has completed.
+// Shared memory: two K stages and two V stages of one step each (K is
+// released when S is done, V when P.V is done).
+//
+// Warps: 0 loads pages (TMA), 1 owns tensor memory and issues the MMAs (one
+// thread), 2-5 run the softmax: thread t of warp w owns query row
+// 32*(w%4) + t, so row maxima and sums need no shuffles. O is rescaled only
+// when a row maximum grows by more than 2^8 (the final O / l uses the same
+// reference, so the result does not depend on when that happens). P carries
+// ~16 significant bits (high + low bf16 parts, two MMAs per k-step) like the
+// other kernels.
 
-template <int D, int BS, int NST>
+template <int D, int BS>
 struct TmemPrefixGeom {
-  static constexpr int kPage = BS * D * 2;
-  static constexpr int kStage = 2 * kPage;
-  static constexpr int kQ = 128 * D * 2;
-  static constexpr int kP = 128 * BS * 2;  // one P tile
-  // P double buffered (page parity), each as bf16 high and low tiles
-  static constexpr int kSmem = 1024 + 1024 + kQ + NST * kStage + 4 * kP;
+  static constexpr int kTok = 64;             // tokens per step (one 64-column load of S)
+  static constexpr int kPages = kTok / BS;    // pages per step
+  static constexpr int kPage = BS * D * 2;    // bytes of one page of K (or V)
+  static constexpr int kGroup = kTok * D * 2; // bytes of one step of K (or V)
+  static constexpr int kChunk = kTok * 128;   // one 64-column chunk of a step
+  static constexpr int kSmem = 1024 + 1024 + 4 * kGroup;
   static constexpr int kThreads = 6 * 32;
-  static constexpr uint32_t kCols = (D + 2 * BS) <= 256 ? 256u : 512u;
+  static constexpr uint32_t kColS = D;              // S of step t at kColS + 64 * (t & 1)
+  static constexpr uint32_t kColQ = D + 2 * kTok;   // Q: k-step k at kColQ + 8 k
+  static constexpr uint32_t kUsed = kColQ + D / 2;
+  static constexpr uint32_t kCols = kUsed <= 256 ? 256u : 512u;
+  static_assert(kUsed <= 512, "tensor memory holds 512 columns");
+  static_assert(BS == 16 || BS == 32, "page size");
 };
 
-template <int D, int BS, int NST>
-__global__ void __launch_bounds__(TmemPrefixGeom<D, BS, NST>::kThreads)
+template <int D, int BS>
+__global__ void __launch_bounds__(TmemPrefixGeom<D, BS>::kThreads)
     prefix_tmem_kernel(const __grid_constant__ CUtensorMap tmk,
                        const __grid_constant__ CUtensorMap tmv, const PrefixParams p) {
-  using G = TmemPrefixGeom<D, BS, NST>;
-  constexpr int PAGE = G::kPage;
+  using G = TmemPrefixGeom<D, BS>;
   constexpr int KT = D / 16;
-  constexpr uint32_t P_SBO = (BS / 8) * 128;
+  constexpr int NP = G::kPages;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* sbase = smem_raw + (base - raw);
-  uint64_t* kv_full = reinterpret_cast<uint64_t*>(sbase);
-  uint64_t* kv_empty = kv_full + NST;
-  uint64_t* s_full = kv_empty + NST;   // [2]
-  uint64_t* s_empty = s_full + 2;      // [2]
-  uint64_t* p_full = s_empty + 2;      // [2]
-  uint64_t* o_done = p_full + 2;       // [2]
+  uint64_t* k_full = reinterpret_cast<uint64_t*>(sbase);  // [2]
+  uint64_t* k_empty = k_full + 2;                          // [2]
+  uint64_t* v_full = k_empty + 2;                          // [2]
+  uint64_t* v_empty = v_full + 2;                          // [2]
+  uint64_t* s_full = v_empty + 2;                          // [2]
+  uint64_t* p_full = s_full + 2;                           // [2]
+  uint64_t* o_done = p_full + 2;                           // [2]
   uint64_t* drained = o_done + 2;
+  uint64_t* q_ready = drained + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sbase + 1000);
-  const uint32_t qtile = base + 1024;
-  const uint32_t ring = qtile + G::kQ;
-  // P tiles of page j: hi at p_hi + (j & 1) * 2 * kP, lo kP further
-  const uint32_t p_hi = ring + NST * G::kStage;
-  const uint32_t p_lo = p_hi + G::kP;
-  uint8_t* qtile_p = sbase + 1024;
-  uint8_t* p_hi_p = sbase + (p_hi - base);
-  uint8_t* p_lo_p = sbase + (p_lo - base);
+  const uint32_t kring = base + 1024;           // K stage b at kring + b * kGroup
+  const uint32_t vring = kring + 2 * G::kGroup; // V stage b at vring + b * kGroup
   // the members' own-block decode launched next may start on the room this
   // grid leaves free (it writes other workspace slots and reads no output of
   // this kernel)
@@ -117,111 +127,119 @@ __global__ void __launch_bounds__(TmemPrefixGeom<D, BS, NST>::kThreads)
   if (blk_begin >= pre) return;
   const int blk_end = min(pre, blk_begin + p.partition_blocks);
   const int nblk = blk_end - blk_begin;
+  const int nsteps = (nblk + NP - 1) / NP;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < NST; ++i) {
-      mbar_init(&kv_full[i], 1);
-      mbar_init(&kv_empty[i], 1);
-    }
     for (int i = 0; i < 2; ++i) {
+      mbar_init(&k_full[i], 1);
+      mbar_init(&k_empty[i], 1);
+      mbar_init(&v_full[i], 1);
+      mbar_init(&v_empty[i], 1);
       mbar_init(&s_full[i], 1);
-      mbar_init(&s_empty[i], 128);
-    }
-    for (int i = 0; i < 2; ++i) {
       mbar_init(&p_full[i], 128);
       mbar_init(&o_done[i], 1);
     }
     mbar_init(drained, 1);
+    mbar_init(q_ready, 128);
     fence_mbar_init();
   }
   if (warp == 1) tmem_alloc(tmem_slot, G::kCols);
-  // Q tile: row r = member * g + jj, rows >= R are zero
-  for (int u = threadIdx.x; u < 128 * (D / 8); u += G::kThreads) {
-    const int r = u / (D / 8);
-    const int c = (u % (D / 8)) * 8;
-    uint4 v = make_uint4(0u, 0u, 0u, 0u);
-    if (r < R) {
-      const int s = s0 + r / g;
-      const int hq = h * g + r % g;
-      v = *reinterpret_cast<const uint4*>(p.q + (static_cast<int64_t>(s) * p.num_heads + hq) * D + c);
-    }
-    const uint32_t a = qtile + (c >> 6) * (128 * 128) + r * 128 + (c & 63) * 2;
-    *reinterpret_cast<uint4*>(qtile_p + ((a ^ (((a >> 7) & 7u) << 4)) - qtile)) = v;
-  }
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t t_o = tmem;                 // columns [0, D)
-  const uint32_t t_s = tmem + D;             // columns [D, D + 2B)
+  const uint32_t t_o = tmem;
+  const uint32_t t_s = tmem + G::kColS;
+  const uint32_t t_q = tmem + G::kColQ;
 
-  int issued = 0;
+  int k_issued = 0, v_issued = 0;  // producer lane 0 only
   if (warp == 0) {
     if (lane == 0) {
       const int32_t* bt = p.block_tables + static_cast<int64_t>(s0) * p.max_blocks_per_seq;
-      for (int it = 0; it < nblk; ++it) {
-        const int st = it % NST;
-        if (it >= NST && !mbar_wait(&kv_empty[st], ((it / NST) - 1) & 1, p.err)) break;
-        const int32_t pb = bt[blk_begin + it];
-        issued = it + 1;
-        if (pb < 0 || pb >= p.num_blocks) {
-          report_error(p.err, PKV_DEVERR_BLOCK_ID);
-          mbar_arrive(&kv_full[st]);
-          continue;
-        }
-        const uint32_t kdst = ring + st * G::kStage;
-        const int y = (pb * p.num_kv_heads + h) * BS;
-        mbar_arrive_expect_tx(&kv_full[st], 2 * PAGE);
+      for (int st = 0; st < nsteps; ++st) {
+        const int b = st & 1;
+        const int np = min(NP, nblk - st * NP);
+        int32_t pb[NP];
+        int good = 0;
 #pragma unroll
-        for (int c = 0; c < D / 64; ++c) {
-          tma_load_2d(kdst + c * BS * 128, &tmk, c * 64, y, &kv_full[st]);
-          tma_load_2d(kdst + PAGE + c * BS * 128, &tmv, c * 64, y, &kv_full[st]);
+        for (int q = 0; q < NP; ++q) {
+          pb[q] = q < np ? bt[blk_begin + st * NP + q] : -1;
+          if (q < np && (pb[q] < 0 || pb[q] >= p.num_blocks)) {
+            report_error(p.err, PKV_DEVERR_BLOCK_ID);
+            pb[q] = -1;
+          }
+          good += pb[q] >= 0 ? 1 : 0;
+        }
+        // K of this step: its stage was last read by S of step st - 2
+        if (st >= 2 && !mbar_wait(&k_empty[b], ((st >> 1) - 1) & 1, p.err)) break;
+        k_issued = st + 1;
+        mbar_arrive_expect_tx(&k_full[b], good * G::kPage);
+#pragma unroll
+        for (int q = 0; q < NP; ++q) {
+          if (pb[q] < 0) continue;
+          const int y = (pb[q] * p.num_kv_heads + h) * BS;
+#pragma unroll
+          for (int c = 0; c < D / 64; ++c)
+            tma_load_2d(kring + b * G::kGroup + c * G::kChunk + q * BS * 128, &tmk, c * 64, y,
+                        &k_full[b]);
+        }
+        // V of this step: its stage was last read by P.V of step st - 2
+        if (st >= 2 && !mbar_wait(&v_empty[b], ((st >> 1) - 1) & 1, p.err)) break;
+        v_issued = st + 1;
+        mbar_arrive_expect_tx(&v_full[b], good * G::kPage);
+#pragma unroll
+        for (int q = 0; q < NP; ++q) {
+          if (pb[q] < 0) continue;
+          const int y = (pb[q] * p.num_kv_heads + h) * BS;
+#pragma unroll
+          for (int c = 0; c < D / 64; ++c)
+            tma_load_2d(vring + b * G::kGroup + c * G::kChunk + q * BS * 128, &tmv, c * 64, y,
+                        &v_full[b]);
         }
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      constexpr uint32_t idesc_qk = umma_idesc_bf16(128, BS, false);
+      constexpr uint32_t idesc_qk = umma_idesc_bf16(128, G::kTok, false);
       constexpr uint32_t idesc_pv = umma_idesc_bf16(128, D, true);
-      bool ok = true;
-      for (int it = 0; it <= nblk && ok; ++it) {
-        if (it < nblk) {
-          const int st = it % NST;
-          if (!mbar_wait(&kv_full[st], (it / NST) & 1, p.err)) break;
-          if (it >= 2 && !mbar_wait(&s_empty[it & 1], ((it >> 1) - 1) & 1, p.err)) break;
+      const bool ok = mbar_wait(q_ready, 0, p.err);
+      for (int st = 0; st <= nsteps && ok; ++st) {
+        if (st < nsteps) {
+          const int b = st & 1;
+          if (!mbar_wait(&k_full[b], (st >> 1) & 1, p.err)) break;
+          // S of step st overwrites P of step st - 2
+          if (st >= 2 && !mbar_wait(&o_done[b], ((st - 2) >> 1) & 1, p.err)) break;
           tc_fence_after();
-          const uint32_t kp = ring + st * G::kStage;
+          const uint32_t kp = kring + b * G::kGroup;
 #pragma unroll
           for (int k = 0; k < KT; ++k) {
-            const uint64_t a = umma_sdesc(qtile + (k >> 2) * (128 * 128) + (k & 3) * 32, 16, 1024, 2);
-            const uint64_t b = umma_sdesc(kp + (k >> 2) * (BS * 128) + (k & 3) * 32, 16, 1024, 2);
-            umma_bf16(t_s + (it & 1) * BS, a, b, idesc_qk, k > 0 ? 1u : 0u);
+            const uint64_t bk = umma_sdesc(kp + (k >> 2) * G::kChunk + (k & 3) * 32, 16, 1024, 2);
+            umma_bf16_ta(t_s + b * G::kTok, t_q + 8 * k, bk, idesc_qk, k > 0 ? 1u : 0u);
           }
-          umma_commit(&s_full[it & 1]);
+          umma_commit(&s_full[b]);
+          umma_commit(&k_empty[b]);
         }
-        if (it >= 1) {
-          const int j = it - 1;
-          if (!mbar_wait(&p_full[j & 1], (j >> 1) & 1, p.err)) break;
+        if (st >= 1) {
+          const int j = st - 1, b = j & 1;
+          if (!mbar_wait(&p_full[b], (j >> 1) & 1, p.err)) break;
+          if (!mbar_wait(&v_full[b], (j >> 1) & 1, p.err)) break;
           tc_fence_after();
-          const uint32_t vp = ring + (j % NST) * G::kStage + PAGE;
-          const uint32_t pb = (j & 1) * 2 * G::kP;
-#pragma unroll
-          for (int kk = 0; kk < BS / 16; ++kk) {
-            const uint64_t bv = umma_sdesc(vp + kk * 2048, BS * 128, 1024, 2);
-            umma_bf16(t_o, umma_sdesc(p_hi + pb + kk * 256, 128, P_SBO, 0), bv, idesc_pv,
-                      (j > 0 || kk > 0) ? 1u : 0u);
-            umma_bf16(t_o, umma_sdesc(p_lo + pb + kk * 256, 128, P_SBO, 0), bv, idesc_pv, 1u);
+          const uint32_t vp = vring + b * G::kGroup;
+          const uint32_t ph = t_s + b * G::kTok;
+          const int ksteps = min(NP, nblk - j * NP) * (BS / 16);
+          for (int kk = 0; kk < ksteps; ++kk) {
+            const uint64_t bv = umma_sdesc(vp + kk * 2048, G::kChunk, 1024, 2);
+            umma_bf16_ta(t_o, ph + 8 * kk, bv, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+            umma_bf16_ta(t_o, ph + 32 + 8 * kk, bv, idesc_pv, 1u);
           }
-          umma_commit(&o_done[j & 1]);
-          umma_commit(&kv_empty[j % NST]);
+          umma_commit(&o_done[b]);
+          umma_commit(&v_empty[b]);
         }
       }
       // every tensor-core operation issued here has finished before tensor
       // memory is released
       umma_commit(drained);
       (void)mbar_wait(drained, 0, p.err);
-      (void)ok;
     }
   } else {
     // softmax: one query row per thread
@@ -229,48 +247,63 @@ __global__ void __launch_bounds__(TmemPrefixGeom<D, BS, NST>::kThreads)
     const uint32_t lane_off = static_cast<uint32_t>(32 * (warp & 3)) << 16;
     const float qs = p.qscale;
     float m_used = -INFINITY, l = 0.f;
+    // Q row `row` (member row / g, head h*g + row % g) into tensor memory;
+    // rows past the group's query rows are zero
+    {
+      const bool live = row < R;
+      const uint16_t* qrow =
+          p.q + (static_cast<int64_t>(s0 + (live ? row / g : 0)) * p.num_heads + h * g +
+                 (live ? row % g : 0)) * D;
+#pragma unroll 1
+      for (int c = 0; c < D; c += 32) {
+        uint32_t w[16];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const uint4 v = live ? *reinterpret_cast<const uint4*>(qrow + c + 8 * i)
+                               : make_uint4(0u, 0u, 0u, 0u);
+          w[4 * i] = v.x;
+          w[4 * i + 1] = v.y;
+          w[4 * i + 2] = v.z;
+          w[4 * i + 3] = v.w;
+        }
+        tmem_st16_nowait(t_q + lane_off + c / 2, w);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(q_ready);
+    }
     bool ok = true;
-    for (int it = 0; it < nblk; ++it) {
-      if (!__all_sync(0xffffffffu, mbar_wait(&s_full[it & 1], (it >> 1) & 1, p.err))) {
+    for (int st = 0; st < nsteps; ++st) {
+      const int b = st & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(&s_full[b], (st >> 1) & 1, p.err))) {
         ok = false;
         break;
       }
       tc_fence_after();
-      float sv[BS];
-#pragma unroll
-      for (int c = 0; c < BS; c += 16) tmem_ld16(t_s + lane_off + (it & 1) * BS + c, sv + c);
-      tc_fence_before();
-      mbar_arrive(&s_empty[it & 1]);
+      const uint32_t ts = t_s + lane_off + b * G::kTok;
+      float sv[G::kTok];
+      tmem_ld64(ts, sv);
+      // tokens past the partition's last page hold stale rows
+      const int valid = min(G::kTok, (nblk - st * NP) * BS);
       float mx = -INFINITY;
 #pragma unroll
-      for (int t = 0; t < BS; ++t) {
-        sv[t] *= qs;
+      for (int t = 0; t < G::kTok; ++t) {
+        sv[t] = t < valid ? sv[t] * qs : -INFINITY;
         mx = fmaxf(mx, sv[t]);
-      }
-      // this page's P tiles were last read by P.V of page it - 2
-      if (it >= 2) {
-        if (!__all_sync(0xffffffffu,
-                        mbar_wait(&o_done[it & 1], ((it - 2) >> 1) & 1, p.err))) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
       }
       // tensor-memory loads and stores are warp-collective: the rescale runs
       // on every lane of the warp if any lane needs it (alpha = 1 elsewhere);
-      // it needs O complete up to page it - 1 (a commit covers all earlier MMAs)
+      // it needs O complete up to step st - 1 (a commit covers all earlier MMAs)
       const bool want = mx > m_used + 8.f;
       const float alpha = want ? fast_exp2(m_used - mx) : 1.f;  // 0 while m_used is -inf
-      const bool rescale = it >= 1 && __any_sync(0xffffffffu, want);
+      const bool rescale = st >= 1 && __any_sync(0xffffffffu, want);
       if (rescale) {
         if (!__all_sync(0xffffffffu,
-                        mbar_wait(&o_done[(it - 1) & 1], ((it - 1) >> 1) & 1, p.err))) {
+                        mbar_wait(&o_done[(st - 1) & 1], ((st - 1) >> 1) & 1, p.err))) {
           ok = false;
           break;
         }
         tc_fence_after();
-      }
-      if (rescale) {
 #pragma unroll 1
         for (int c = 0; c < D; c += 16) {
           float ov[16];
@@ -284,34 +317,29 @@ __global__ void __launch_bounds__(TmemPrefixGeom<D, BS, NST>::kThreads)
         l *= alpha;
         m_used = mx;
       }
-      float pv[BS];
+      // P over S's columns: bf16 high parts, then the low parts
+      uint32_t hw[G::kTok / 2], lw[G::kTok / 2];
 #pragma unroll
-      for (int t = 0; t < BS; ++t) {
-        pv[t] = fast_exp2(sv[t] - m_used);
-        l += pv[t];
+      for (int i = 0; i < G::kTok / 2; ++i) {
+        const float p0 = fast_exp2(sv[2 * i] - m_used);
+        const float p1 = fast_exp2(sv[2 * i + 1] - m_used);
+        l += p0;
+        l += p1;
+        hw[i] = pack_bf16(p0, p1);
+        const __nv_bfloat162 hv = *reinterpret_cast<const __nv_bfloat162*>(&hw[i]);
+        lw[i] = pack_bf16(p0 - __low2float(hv), p1 - __high2float(hv));
       }
-      // row `row` of the P tiles: [m-group][k-chunk][8 rows][8 tokens]
-#pragma unroll
-      for (int t = 0; t < BS; t += 8) {
-        uint32_t hw[4], lw[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          hw[i] = pack_bf16(pv[t + 2 * i], pv[t + 2 * i + 1]);
-          const __nv_bfloat162 hv = *reinterpret_cast<const __nv_bfloat162*>(&hw[i]);
-          lw[i] = pack_bf16(pv[t + 2 * i] - __low2float(hv), pv[t + 2 * i + 1] - __high2float(hv));
-        }
-        const uint32_t off = (it & 1) * 2 * G::kP + (row >> 3) * P_SBO + (t >> 3) * 128 +
-                             (row & 7) * 16;
-        *reinterpret_cast<uint4*>(p_hi_p + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-        *reinterpret_cast<uint4*>(p_lo_p + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-      }
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      tmem_st16_nowait(ts, hw);
+      tmem_st16_nowait(ts + 16, hw + 16);
+      tmem_st16_nowait(ts + 32, lw);
+      tmem_st16_nowait(ts + 48, lw + 16);
+      tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(&p_full[it & 1]);
+      mbar_arrive(&p_full[b]);
     }
     ok = __all_sync(0xffffffffu, ok);
-    if (ok && nblk > 0 &&
-        mbar_wait(&o_done[(nblk - 1) & 1], ((nblk - 1) >> 1) & 1, p.err)) {
+    if (ok && nsteps > 0 &&
+        mbar_wait(&o_done[(nsteps - 1) & 1], ((nsteps - 1) >> 1) & 1, p.err)) {
       tc_fence_after();
       // every lane runs the same (warp-collective) loads; rows past the
       // group's query rows store nothing
@@ -340,9 +368,11 @@ __global__ void __launch_bounds__(TmemPrefixGeom<D, BS, NST>::kThreads)
   tc_fence_before();
   __syncthreads();
   if (warp == 0 && lane == 0) {
-    const int first = issued > NST ? issued - NST : 0;
-    for (int it = first; it < issued; ++it)
-      if (!mbar_wait(&kv_full[it % NST], (it / NST) & 1, p.err)) break;
+    // no copy may still be writing this CTA's shared memory when it exits
+    for (int st = max(0, k_issued - 2); st < k_issued; ++st)
+      if (!mbar_wait(&k_full[st & 1], (st >> 1) & 1, p.err)) break;
+    for (int st = max(0, v_issued - 2); st < v_issued; ++st)
+      if (!mbar_wait(&v_full[st & 1], (st >> 1) & 1, p.err)) break;
   }
   if (warp == 1) {
     tc_fence_after();
@@ -350,12 +380,12 @@ __global__ void __launch_bounds__(TmemPrefixGeom<D, BS, NST>::kThreads)
   }
 }
 
-template <int D, int BS, int NST>
+template <int D, int BS>
 static int launch_prefix_tmem_t(const PrefixParams& p, const CUtensorMap& tk,
                                 const CUtensorMap& tv, dim3 grid, cudaStream_t st) {
-  using G = TmemPrefixGeom<D, BS, NST>;
+  using G = TmemPrefixGeom<D, BS>;
   static bool done[64] = {false};
-  auto kern = prefix_tmem_kernel<D, BS, NST>;
+  auto kern = prefix_tmem_kernel<D, BS>;
   int rc = ensure_smem(kern, G::kSmem, done, 64);
   if (rc != PKV_OK) return rc;
   kern<<<grid, G::kThreads, G::kSmem, st>>>(tk, tv, p);
@@ -370,10 +400,10 @@ int launch_prefix(const PrefixParams& p, const void* k_cache, const void* v_cach
   if (rc != PKV_OK) return rc;
   rc = pool_tensor_map(&tv, v_cache, rows, head_dim, block_size, false);
   if (rc != PKV_OK) return rc;
-  if (head_dim == 256 && block_size == 16) return launch_prefix_tmem_t<256, 16, 4>(p, tk, tv, grid, st);
-  if (head_dim == 256 && block_size == 32) return launch_prefix_tmem_t<256, 32, 2>(p, tk, tv, grid, st);
-  if (head_dim == 128 && block_size == 16) return launch_prefix_tmem_t<128, 16, 8>(p, tk, tv, grid, st);
-  return launch_prefix_tmem_t<128, 32, 4>(p, tk, tv, grid, st);
+  if (head_dim == 256 && block_size == 16) return launch_prefix_tmem_t<256, 16>(p, tk, tv, grid, st);
+  if (head_dim == 256 && block_size == 32) return launch_prefix_tmem_t<256, 32>(p, tk, tv, grid, st);
+  if (head_dim == 128 && block_size == 16) return launch_prefix_tmem_t<128, 16>(p, tk, tv, grid, st);
+  return launch_prefix_tmem_t<128, 32>(p, tk, tv, grid, st);
 }
 
 }  // namespace pkv
