@@ -196,8 +196,9 @@ int pkv_paged_attention_reduce(void* out, const void* workspace,
  *                   0 for a sequence outside every group
  *   max_prefix_blocks : host upper bound of prefix_blocks
  *   partition_size: split size of each member's own part (multiple of
- *                   block_size); the shared part uses a power-of-two multiple
- *                   of it chosen by the library (enough CTAs to cover the SMs)
+ *                   block_size, at most 2048 blocks); the shared part uses a
+ *                   power-of-two multiple of it chosen by the library (enough
+ *                   CTAs to cover the SMs, at most 2048 blocks)
  *   workspace     : at least pkv_shared_prefix_workspace_bytes(...) bytes
  * Per group and KV head, a kernel computes partials of every member's query
  * heads over the shared pages (the members' queries form the rows of one

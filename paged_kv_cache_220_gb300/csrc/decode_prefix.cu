@@ -57,7 +57,10 @@ struct PrefixParams {
 // 32 columns, the low parts, i.e. the rounding remainders, in the next 32),
 // so S of step t + 2 is issued only after P.V of step t has completed.
 // Shared memory: two K stages and two V stages of one step each (K is
-// released when S is done, V when P.V is done).
+// released when S is done, V when P.V is done), and the partition's block
+// ids, read once at the start so the loads are issued without a global read
+// on the way. The producer issues K of step t + 1 before V of step t: K(t+1)
+// waits for S(t-1), V(t) for P.V(t-2), which completes later.
 //
 // Warps: 0 loads pages (TMA), 1 owns tensor memory and issues the MMAs (one
 // thread), 2-5 run the softmax: thread t of warp w owns query row
@@ -74,7 +77,8 @@ struct TmemPrefixGeom {
   static constexpr int kPage = BS * D * 2;    // bytes of one page of K (or V)
   static constexpr int kGroup = kTok * D * 2; // bytes of one step of K (or V)
   static constexpr int kChunk = kTok * 128;   // one 64-column chunk of a step
-  static constexpr int kSmem = 1024 + 1024 + 4 * kGroup;
+  static constexpr int kSmem = 1024 + 1024 + 4 * kGroup;  // + the block ids
+  static constexpr int kMaxIds = 2048;                     // partition_blocks limit
   static constexpr int kThreads = 6 * 32;
   static constexpr uint32_t kColS = D;              // S of step t at kColS + 64 * (t & 1)
   static constexpr uint32_t kColQ = D + 2 * kTok;   // Q: k-step k at kColQ + 8 k
@@ -107,6 +111,7 @@ __global__ void __launch_bounds__(TmemPrefixGeom<D, BS>::kThreads)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sbase + 1000);
   const uint32_t kring = base + 1024;           // K stage b at kring + b * kGroup
   const uint32_t vring = kring + 2 * G::kGroup; // V stage b at vring + b * kGroup
+  int32_t* ids = reinterpret_cast<int32_t*>(sbase + 1024 + 4 * G::kGroup);
   // the members' own-block decode launched next may start on the room this
   // grid leaves free (it writes other workspace slots and reads no output of
   // this kernel)
@@ -144,6 +149,18 @@ __global__ void __launch_bounds__(TmemPrefixGeom<D, BS>::kThreads)
     fence_mbar_init();
   }
   if (warp == 1) tmem_alloc(tmem_slot, G::kCols);
+  if (warp == 0) {
+    // the partition's block ids; out-of-range ids become -1 (skipped)
+    const int32_t* bt = p.block_tables + static_cast<int64_t>(s0) * p.max_blocks_per_seq + blk_begin;
+    for (int i = lane; i < nblk; i += 32) {
+      int32_t pb = bt[i];
+      if (pb < 0 || pb >= p.num_blocks) {
+        report_error(p.err, PKV_DEVERR_BLOCK_ID);
+        pb = -1;
+      }
+      ids[i] = pb;
+    }
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -155,47 +172,38 @@ __global__ void __launch_bounds__(TmemPrefixGeom<D, BS>::kThreads)
   int k_issued = 0, v_issued = 0;  // producer lane 0 only
   if (warp == 0) {
     if (lane == 0) {
-      const int32_t* bt = p.block_tables + static_cast<int64_t>(s0) * p.max_blocks_per_seq;
-      for (int st = 0; st < nsteps; ++st) {
+      // K (kind 0) or V (kind 1) of step st into stage st & 1; the stage was
+      // last read by S (K) or P.V (V) of step st - 2
+      auto issue = [&](int kind, int st) -> bool {
         const int b = st & 1;
+        uint64_t* full = kind == 0 ? &k_full[b] : &v_full[b];
+        uint64_t* empty = kind == 0 ? &k_empty[b] : &v_empty[b];
+        if (st >= 2 && !mbar_wait(empty, ((st >> 1) - 1) & 1, p.err)) return false;
         const int np = min(NP, nblk - st * NP);
-        int32_t pb[NP];
         int good = 0;
-#pragma unroll
-        for (int q = 0; q < NP; ++q) {
-          pb[q] = q < np ? bt[blk_begin + st * NP + q] : -1;
-          if (q < np && (pb[q] < 0 || pb[q] >= p.num_blocks)) {
-            report_error(p.err, PKV_DEVERR_BLOCK_ID);
-            pb[q] = -1;
-          }
-          good += pb[q] >= 0 ? 1 : 0;
-        }
-        // K of this step: its stage was last read by S of step st - 2
-        if (st >= 2 && !mbar_wait(&k_empty[b], ((st >> 1) - 1) & 1, p.err)) break;
-        k_issued = st + 1;
-        mbar_arrive_expect_tx(&k_full[b], good * G::kPage);
-#pragma unroll
-        for (int q = 0; q < NP; ++q) {
-          if (pb[q] < 0) continue;
-          const int y = (pb[q] * p.num_kv_heads + h) * BS;
+        for (int q = 0; q < np; ++q) good += ids[st * NP + q] >= 0 ? 1 : 0;
+        mbar_arrive_expect_tx(full, good * G::kPage);
+        const uint32_t dst = (kind == 0 ? kring : vring) + b * G::kGroup;
+        const CUtensorMap* map = kind == 0 ? &tmk : &tmv;
+        for (int q = 0; q < np; ++q) {
+          const int32_t pb = ids[st * NP + q];
+          if (pb < 0) continue;
+          const int y = (pb * p.num_kv_heads + h) * BS;
 #pragma unroll
           for (int c = 0; c < D / 64; ++c)
-            tma_load_2d(kring + b * G::kGroup + c * G::kChunk + q * BS * 128, &tmk, c * 64, y,
-                        &k_full[b]);
+            tma_load_2d(dst + c * G::kChunk + q * BS * 128, map, c * 64, y, full);
         }
-        // V of this step: its stage was last read by P.V of step st - 2
-        if (st >= 2 && !mbar_wait(&v_empty[b], ((st >> 1) - 1) & 1, p.err)) break;
+        return true;
+      };
+      bool ok = nsteps > 0 && issue(0, 0);
+      k_issued = ok ? 1 : 0;
+      for (int st = 0; st < nsteps && ok; ++st) {
+        if (st + 1 < nsteps) {
+          if (!(ok = issue(0, st + 1))) break;
+          k_issued = st + 2;
+        }
+        if (!(ok = issue(1, st))) break;
         v_issued = st + 1;
-        mbar_arrive_expect_tx(&v_full[b], good * G::kPage);
-#pragma unroll
-        for (int q = 0; q < NP; ++q) {
-          if (pb[q] < 0) continue;
-          const int y = (pb[q] * p.num_kv_heads + h) * BS;
-#pragma unroll
-          for (int c = 0; c < D / 64; ++c)
-            tma_load_2d(vring + b * G::kGroup + c * G::kChunk + q * BS * 128, &tmv, c * 64, y,
-                        &v_full[b]);
-        }
       }
     }
   } else if (warp == 1) {
@@ -386,9 +394,11 @@ static int launch_prefix_tmem_t(const PrefixParams& p, const CUtensorMap& tk,
   using G = TmemPrefixGeom<D, BS>;
   static bool done[64] = {false};
   auto kern = prefix_tmem_kernel<D, BS>;
-  int rc = ensure_smem(kern, G::kSmem, done, 64);
+  if (p.partition_blocks <= 0 || p.partition_blocks > G::kMaxIds) return PKV_ERR_UNSUPPORTED;
+  int rc = ensure_smem(kern, G::kSmem + 4 * G::kMaxIds, done, 64);
   if (rc != PKV_OK) return rc;
-  kern<<<grid, G::kThreads, G::kSmem, st>>>(tk, tv, p);
+  const int smem = G::kSmem + ((4 * p.partition_blocks + 15) & ~15);
+  kern<<<grid, G::kThreads, smem, st>>>(tk, tv, p);
   return launch_status();
 }
 
@@ -467,8 +477,10 @@ extern "C" int pkv_paged_attention_decode_shared_prefix(
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
       return PKV_ERR_CUDA;
   }
+  constexpr int kMaxPrefixPartitionBlocks = 2048;  // block ids a prefix CTA holds
+  if (partition_size / cache.block_size > kMaxPrefixPartitionBlocks) return PKV_ERR_UNSUPPORTED;
   int pre_p = partition_size;
-  while (pre_p < pre_tokens &&
+  while (pre_p < pre_tokens && 2 * pre_p / cache.block_size <= kMaxPrefixPartitionBlocks &&
          static_cast<int64_t>((pre_tokens + pre_p - 1) / pre_p) * cache.num_kv_heads * num_groups >
              sms)
     pre_p *= 2;
