@@ -59,11 +59,16 @@ struct PrefixParams {
 // Shared memory: two K stages and two V stages of one step each (K is
 // released when S is done, V when P.V is done), and the partition's block
 // ids, read once at the start so the loads are issued without a global read
-// on the way. The producer issues K of step t + 1 before V of step t: K(t+1)
-// waits for S(t-1), V(t) for P.V(t-2), which completes later.
+// on the way. K of a step is laid out [128-byte chunk][64 rows][128 B] (the
+// N = 64 operand needs the rows of all its pages at one stride), which takes
+// one TMA box per page and chunk; V is laid out page by page and takes one
+// 3-D box per page. A TMA instruction costs its issuing thread ~100 cycles,
+// so two producer warps share the pages of each step. Each issues K of step
+// t + 1 before V of step t: K(t+1) waits for S(t-1), V(t) for P.V(t-2), which
+// completes later.
 //
-// Warps: 0 loads pages (TMA), 1 owns tensor memory and issues the MMAs (one
-// thread), 2-5 run the softmax: thread t of warp w owns query row
+// Warps: 0 and 6 load pages (TMA), 1 owns tensor memory and issues the MMAs
+// (one thread), 2-5 run the softmax: thread t of warp w owns query row
 // 32*(w%4) + t, so row maxima and sums need no shuffles. O is rescaled only
 // when a row maximum grows by more than 2^8 (the final O / l uses the same
 // reference, so the result does not depend on when that happens). P carries
@@ -79,7 +84,7 @@ struct TmemPrefixGeom {
   static constexpr int kChunk = kTok * 128;   // one 64-column chunk of a step
   static constexpr int kSmem = 1024 + 1024 + 4 * kGroup;  // + the block ids
   static constexpr int kMaxIds = 2048;                     // partition_blocks limit
-  static constexpr int kThreads = 6 * 32;
+  static constexpr int kThreads = 7 * 32;
   static constexpr uint32_t kColS = D;              // S of step t at kColS + 64 * (t & 1)
   static constexpr uint32_t kColQ = D + 2 * kTok;   // Q: k-step k at kColQ + 8 k
   static constexpr uint32_t kUsed = kColQ + D / 2;
@@ -136,9 +141,9 @@ __global__ void __launch_bounds__(TmemPrefixGeom<D, BS>::kThreads)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&k_full[i], 1);
+      mbar_init(&k_full[i], 2);  // one arrival per producer warp
       mbar_init(&k_empty[i], 1);
-      mbar_init(&v_full[i], 1);
+      mbar_init(&v_full[i], 2);
       mbar_init(&v_empty[i], 1);
       mbar_init(&s_full[i], 1);
       mbar_init(&p_full[i], 128);
@@ -169,9 +174,10 @@ __global__ void __launch_bounds__(TmemPrefixGeom<D, BS>::kThreads)
   const uint32_t t_s = tmem + G::kColS;
   const uint32_t t_q = tmem + G::kColQ;
 
-  int k_issued = 0, v_issued = 0;  // producer lane 0 only
-  if (warp == 0) {
+  int k_issued = 0, v_issued = 0;  // producer lanes 0 only
+  if (warp == 0 || warp == 6) {
     if (lane == 0) {
+      const int half = warp == 0 ? 0 : 1;  // this producer's pages: q % 2 == half
       // K (kind 0) or V (kind 1) of step st into stage st & 1; the stage was
       // last read by S (K) or P.V (V) of step st - 2
       auto issue = [&](int kind, int st) -> bool {
@@ -181,17 +187,20 @@ __global__ void __launch_bounds__(TmemPrefixGeom<D, BS>::kThreads)
         if (st >= 2 && !mbar_wait(empty, ((st >> 1) - 1) & 1, p.err)) return false;
         const int np = min(NP, nblk - st * NP);
         int good = 0;
-        for (int q = 0; q < np; ++q) good += ids[st * NP + q] >= 0 ? 1 : 0;
+        for (int q = half; q < np; q += 2) good += ids[st * NP + q] >= 0 ? 1 : 0;
         mbar_arrive_expect_tx(full, good * G::kPage);
-        const uint32_t dst = (kind == 0 ? kring : vring) + b * G::kGroup;
-        const CUtensorMap* map = kind == 0 ? &tmk : &tmv;
-        for (int q = 0; q < np; ++q) {
+        for (int q = half; q < np; q += 2) {
           const int32_t pb = ids[st * NP + q];
           if (pb < 0) continue;
           const int y = (pb * p.num_kv_heads + h) * BS;
+          if (kind == 0) {
 #pragma unroll
-          for (int c = 0; c < D / 64; ++c)
-            tma_load_2d(dst + c * G::kChunk + q * BS * 128, map, c * 64, y, full);
+            for (int c = 0; c < D / 64; ++c)
+              tma_load_2d(kring + b * G::kGroup + c * G::kChunk + q * BS * 128, &tmk, c * 64, y,
+                          full);
+          } else {
+            tma_load_page(vring + b * G::kGroup + q * G::kPage, &tmv, y, full);
+          }
         }
         return true;
       };
@@ -236,7 +245,10 @@ __global__ void __launch_bounds__(TmemPrefixGeom<D, BS>::kThreads)
           const uint32_t ph = t_s + b * G::kTok;
           const int ksteps = min(NP, nblk - j * NP) * (BS / 16);
           for (int kk = 0; kk < ksteps; ++kk) {
-            const uint64_t bv = umma_sdesc(vp + kk * 2048, G::kChunk, 1024, 2);
+            // V rows 16 kk .. 16 kk + 15 of the step: page kk / (B/16), page
+            // layout [chunk][B rows][128 B]
+            const uint32_t va = vp + (kk / (BS / 16)) * G::kPage + (kk % (BS / 16)) * 2048;
+            const uint64_t bv = umma_sdesc(va, BS * 128, 1024, 2);
             umma_bf16_ta(t_o, ph + 8 * kk, bv, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
             umma_bf16_ta(t_o, ph + 32 + 8 * kk, bv, idesc_pv, 1u);
           }
@@ -375,7 +387,7 @@ __global__ void __launch_bounds__(TmemPrefixGeom<D, BS>::kThreads)
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 0 && lane == 0) {
+  if ((warp == 0 || warp == 6) && lane == 0) {
     // no copy may still be writing this CTA's shared memory when it exits
     for (int st = max(0, k_issued - 2); st < k_issued; ++st)
       if (!mbar_wait(&k_full[st & 1], (st >> 1) & 1, p.err)) break;
@@ -408,7 +420,7 @@ int launch_prefix(const PrefixParams& p, const void* k_cache, const void* v_cach
   CUtensorMap tk, tv;
   int rc = pool_tensor_map(&tk, k_cache, rows, head_dim, block_size, false);
   if (rc != PKV_OK) return rc;
-  rc = pool_tensor_map(&tv, v_cache, rows, head_dim, block_size, false);
+  rc = pool_tensor_map(&tv, v_cache, rows, head_dim, block_size, false, true);
   if (rc != PKV_OK) return rc;
   if (head_dim == 256 && block_size == 16) return launch_prefix_tmem_t<256, 16>(p, tk, tv, grid, st);
   if (head_dim == 256 && block_size == 32) return launch_prefix_tmem_t<256, 32>(p, tk, tv, grid, st);

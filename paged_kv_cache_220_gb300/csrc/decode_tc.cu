@@ -436,16 +436,16 @@ static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-// Tensor map of one pool viewed as a 2-D array [rows = NB*Hk*B][D] of bf16
-// or bytes (E4M3), box = 128 bytes x B rows, 128-byte swizzle. Encodings are
-// cached per (pointer, shape).
+// Tensor map of one pool: 2-D with one box per 128-byte chunk of a page, or
+// 3-D with one box per whole page (declared in tc_common.cuh). Encodings are
+// cached per (pointer, shape, kind).
 int pool_tensor_map(CUtensorMap* out, const void* base, int64_t rows, int D, int BS,
-                    bool fp8) {
+                    bool fp8, bool whole_page) {
   struct Entry {
     const void* base;
     int64_t rows;
     int d, bs;
-    bool fp8;
+    bool fp8, whole_page;
     CUtensorMap map;
   };
   static std::mutex mu;
@@ -455,7 +455,7 @@ int pool_tensor_map(CUtensorMap* out, const void* base, int64_t rows, int D, int
     std::lock_guard<std::mutex> lock(mu);
     for (int i = 0; i < used; ++i)
       if (cache[i].base == base && cache[i].rows == rows && cache[i].d == D &&
-          cache[i].bs == BS && cache[i].fp8 == fp8) {
+          cache[i].bs == BS && cache[i].fp8 == fp8 && cache[i].whole_page == whole_page) {
         *out = cache[i].map;
         return PKV_OK;
       }
@@ -463,19 +463,32 @@ int pool_tensor_map(CUtensorMap* out, const void* base, int64_t rows, int D, int
   auto enc = tensor_map_encoder();
   if (!enc) return PKV_ERR_CUDA;
   const int esz = fp8 ? 1 : 2;
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(rows)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(D) * esz};
-  cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / esz), static_cast<cuuint32_t>(BS)};
-  cuuint32_t estr[2] = {1u, 1u};
+  const cuuint32_t chunk = static_cast<cuuint32_t>(128 / esz);  // elements per 128 bytes
   CUtensorMap m;
-  CUresult r = enc(&m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
-                   const_cast<void*>(base), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  CUresult r;
+  const auto dtype = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  if (!whole_page) {
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(D) * esz};
+    cuuint32_t box[2] = {chunk, static_cast<cuuint32_t>(BS)};
+    cuuint32_t estr[2] = {1u, 1u};
+    r = enc(&m, dtype, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  } else {
+    const cuuint64_t nchunks = static_cast<cuuint64_t>(D) * esz / 128;
+    cuuint64_t dims[3] = {chunk, static_cast<cuuint64_t>(rows), nchunks};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * esz, 128u};
+    cuuint32_t box[3] = {chunk, static_cast<cuuint32_t>(BS), static_cast<cuuint32_t>(nchunks)};
+    cuuint32_t estr[3] = {1u, 1u, 1u};
+    r = enc(&m, dtype, 3, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  }
   if (r != CUDA_SUCCESS) return PKV_ERR_CUDA;
   std::lock_guard<std::mutex> lock(mu);
   Entry& e = cache[next];
-  e = Entry{base, rows, D, BS, fp8, m};
+  e = Entry{base, rows, D, BS, fp8, whole_page, m};
   next = (next + 1) % 32;
   if (used < 32) ++used;
   *out = m;

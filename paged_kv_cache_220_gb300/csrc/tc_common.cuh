@@ -22,6 +22,16 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// One whole page of a 3-D pool map (x = 0, y = first row, chunk 0).
+__device__ __forceinline__ void tma_load_page(uint32_t dst, const CUtensorMap* map, int y,
+                                              uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(y), "r"(0), "r"(smem_addr(bar))
+      : "memory");
+}
+
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
                                         uint32_t& r3) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
@@ -114,7 +124,12 @@ __device__ __forceinline__ uint32_t swz_bytes(uint32_t page, int row, int byte_c
 
 // Tensor map of one pool viewed as a 2-D array [rows = NB*Hk*B][D] of bf16
 // or bytes (E4M3), box = 128 bytes x B rows, 128-byte swizzle; cached per
-// (pointer, shape). Returns a pkv_status. (decode_tc.cu)
-int pool_tensor_map(CUtensorMap* out, const void* base, int64_t rows, int D, int BS, bool fp8);
+// (pointer, shape). With whole_page the map is 3-D, [chunk][row][128 bytes]
+// (chunk stride 128 bytes, row stride D*esz), and one box is a whole page,
+// landing in the same [chunk][B][128 B] layout as D*esz/128 boxes of the 2-D
+// map: one TMA instruction per page instead of one per 128-byte chunk.
+// Returns a pkv_status. (decode_tc.cu)
+int pool_tensor_map(CUtensorMap* out, const void* base, int64_t rows, int D, int BS, bool fp8,
+                    bool whole_page = false);
 
 }  // namespace pkv
