@@ -4,13 +4,17 @@
 // M = max_p m_p and w_p = l_p * exp(m_p - M), the full softmax output is
 // sum_p (w_p / sum_q w_q) o_p.
 //
-// One CTA per (query head, sequence), RW warps (16 when rows hold many
-// partitions, 4 otherwise). The weights are computed once into shared memory
-// (block-wide max and sum in a fixed tree order), then warp w accumulates the
-// partitions p = w, w + RW, ... with 16-byte loads, four partitions in flight
-// per lane, and the RW warp sums are added in warp order. Normalising the weights before the products makes a single partition
-// reproduce its output exactly. The work is HBM-bound: (d + 2) * 4 bytes per
-// partition read, d * 2 bytes written.
+// Rows with at most 32 partitions (the common case) take one warp per (query
+// head, sequence): lane i holds partition i's max and sum, the maximum and
+// the weight sum are xor-shuffle trees, and every lane accumulates its 16-byte
+// column slices over the partitions in order, with the loads of four
+// partitions in flight. Rows with more partitions (long contexts) take one
+// 16-warp CTA each: the weights go once into shared memory (block-wide max
+// and sum in a fixed tree order), warp w accumulates the partitions
+// p = w, w + 16, ... and the warp sums are added in warp order. Normalising
+// the weights before the products makes a single partition reproduce its
+// output exactly. The work is HBM-bound: (d + 2) * 4 bytes per partition
+// read, d * 2 bytes written.
 #include "common.cuh"
 #include "decode_params.h"
 #include "host_util.h"
@@ -18,6 +22,27 @@
 namespace pkv {
 
 constexpr float kLog2eR = 1.4426950408889634f;
+
+// Slots of sequence s: [0, npre) and [slot_split, slot_split + nsuf).
+__device__ __forceinline__ void row_slots(const int32_t* context_lens, const int32_t* prefix_blocks,
+                                          int s, int partition_size, int block_size,
+                                          int prefix_partition, int slot_split, int np_max,
+                                          int* err, bool report, int& npre, int& nsuf) {
+  const int ctx = context_lens[s];
+  npre = 0;
+  nsuf = ctx > 0 ? (ctx + partition_size - 1) / partition_size : 0;
+  if (prefix_blocks != nullptr) {
+    const int ptok = prefix_blocks[s] * block_size;
+    npre = (ptok + prefix_partition - 1) / prefix_partition;
+    nsuf = ctx > ptok ? (ctx - ptok + partition_size - 1) / partition_size : 0;
+  }
+  if (slot_split + nsuf > np_max || npre > slot_split) {
+    if (report) report_error(err, PKV_DEVERR_CONTEXT);
+    npre = min(npre, slot_split);
+    nsuf = max(0, min(nsuf, np_max - slot_split));
+  }
+}
+
 template <int D, int kReduceWarps>
 __global__ void __launch_bounds__(kReduceWarps * 32) reduce_kernel(
     uint16_t* __restrict__ out, const float* __restrict__ tmp_out,
@@ -34,19 +59,9 @@ __global__ void __launch_bounds__(kReduceWarps * 32) reduce_kernel(
   const int s = blockIdx.y;
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
-  const int ctx = context_lens[s];
-  // slots of this sequence: [0, npre) and [slot_split, slot_split + nsuf)
-  int npre = 0, nsuf = ctx > 0 ? (ctx + partition_size - 1) / partition_size : 0;
-  if (prefix_blocks != nullptr) {
-    const int ptok = prefix_blocks[s] * block_size;
-    npre = (ptok + prefix_partition - 1) / prefix_partition;
-    nsuf = ctx > ptok ? (ctx - ptok + partition_size - 1) / partition_size : 0;
-  }
-  if (slot_split + nsuf > np_max || npre > slot_split) {
-    if (tid == 0) report_error(err, PKV_DEVERR_CONTEXT);
-    npre = min(npre, slot_split);
-    nsuf = max(0, min(nsuf, np_max - slot_split));
-  }
+  int npre, nsuf;
+  row_slots(context_lens, prefix_blocks, s, partition_size, block_size, prefix_partition,
+            slot_split, np_max, err, tid == 0, npre, nsuf);
   const int np = npre + nsuf;
   const int64_t row = static_cast<int64_t>(s) * num_heads + j;
   if (np == 0) {
@@ -144,6 +159,79 @@ __global__ void __launch_bounds__(kReduceWarps * 32) reduce_kernel(
   }
 }
 
+constexpr int kRowWarps = 8;  // rows (warps) per CTA of the narrow merge
+
+template <int D>
+__global__ void __launch_bounds__(kRowWarps * 32) reduce_rows_kernel(
+    uint16_t* __restrict__ out, const float* __restrict__ tmp_out,
+    const float* __restrict__ max_logits, const float* __restrict__ exp_sums,
+    const int32_t* __restrict__ context_lens, int num_rows, int num_heads, int np_max,
+    int partition_size, const int32_t* __restrict__ prefix_blocks, int block_size,
+    int slot_split, int prefix_partition, int* err) {
+  constexpr int V4 = D / 128;  // float4 per lane per partition row
+  const int lane = threadIdx.x & 31;
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * kRowWarps + (threadIdx.x >> 5);
+  if (row >= num_rows) return;
+  const int s = static_cast<int>(row / num_heads);
+  int npre, nsuf;
+  row_slots(context_lens, prefix_blocks, s, partition_size, block_size, prefix_partition,
+            slot_split, np_max, err, lane == 0, npre, nsuf);
+  const int np = npre + nsuf;  // <= np_max <= 32
+  uint2* dst = reinterpret_cast<uint2*>(out + row * D);
+  if (np == 0) {
+#pragma unroll
+    for (int v = 0; v < V4; ++v) dst[lane + 32 * v] = make_uint2(0u, 0u);
+    return;
+  }
+  auto slot_of = [&](int v) { return v < npre ? v : slot_split + (v - npre); };
+  const float m = lane < np ? max_logits[row * np_max + slot_of(lane)] : -INFINITY;
+  const float l = lane < np ? exp_sums[row * np_max + slot_of(lane)] : 0.f;
+  float M = m;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  const float w = lane < np ? l * fast_exp2((m - M) * kLog2eR) : 0.f;
+  float W = w;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) W += __shfl_xor_sync(0xffffffffu, W, off);
+  const float r = w / W;
+
+  const float4* src = reinterpret_cast<const float4*>(tmp_out + row * np_max * D);
+  float4 acc[V4];
+#pragma unroll
+  for (int v = 0; v < V4; ++v) acc[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+  constexpr int U = 4;
+  for (int i0 = 0; i0 < np; i0 += U) {
+    float4 x[U][V4];
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+#pragma unroll
+      for (int v = 0; v < V4; ++v)
+        x[u][v] = i0 + u < np ? src[static_cast<int64_t>(slot_of(i0 + u)) * (D / 4) + lane + 32 * v]
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const float ru = __shfl_sync(0xffffffffu, r, (i0 + u) & 31);
+      if (i0 + u < np) {
+#pragma unroll
+        for (int v = 0; v < V4; ++v) {
+          acc[v].x = fmaf(ru, x[u][v].x, acc[v].x);
+          acc[v].y = fmaf(ru, x[u][v].y, acc[v].y);
+          acc[v].z = fmaf(ru, x[u][v].z, acc[v].z);
+          acc[v].w = fmaf(ru, x[u][v].w, acc[v].w);
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int v = 0; v < V4; ++v) {
+    const uint32_t lo = float_to_bf16_bits(acc[v].x) |
+                        (static_cast<uint32_t>(float_to_bf16_bits(acc[v].y)) << 16);
+    const uint32_t hi = float_to_bf16_bits(acc[v].z) |
+                        (static_cast<uint32_t>(float_to_bf16_bits(acc[v].w)) << 16);
+    dst[lane + 32 * v] = make_uint2(lo, hi);
+  }
+}
+
 }  // namespace pkv
 
 namespace pkv {
@@ -152,47 +240,42 @@ int launch_reduce(void* out, const float* tmp, const float* ml, const float* es,
                   const int32_t* context_lens, int num_seqs, int num_heads, int head_dim,
                   int np_max, int partition_size, const int32_t* prefix_blocks, int block_size,
                   int slot_split, int prefix_partition, cudaStream_t st) {
-  const size_t smem = static_cast<size_t>(np_max > 0 ? np_max : 1) * sizeof(float);
+  const int pp = prefix_partition > 0 ? prefix_partition : partition_size;
+  uint16_t* o = static_cast<uint16_t*>(out);
+  int* err = device_error_ptr();
+  if (np_max <= 32) {
+    // one warp per (sequence, query head) row
+    const int rows = num_seqs * num_heads;
+    const dim3 grid((rows + kRowWarps - 1) / kRowWarps);
+    if (head_dim == 128)
+      reduce_rows_kernel<128><<<grid, kRowWarps * 32, 0, st>>>(
+          o, tmp, ml, es, context_lens, rows, num_heads, np_max, partition_size, prefix_blocks,
+          block_size, slot_split, pp, err);
+    else
+      reduce_rows_kernel<256><<<grid, kRowWarps * 32, 0, st>>>(
+          o, tmp, ml, es, context_lens, rows, num_heads, np_max, partition_size, prefix_blocks,
+          block_size, slot_split, pp, err);
+    return launch_status();
+  }
+  // one 16-warp CTA per row
+  const size_t smem = static_cast<size_t>(np_max) * sizeof(float);
   constexpr size_t kMaxSmem = 160 * 1024;  // plus the static accumulators
   if (smem > kMaxSmem) return PKV_ERR_UNSUPPORTED;
-  dim3 grid(num_heads, num_seqs);
-  const bool wide = np_max > 32;
+  const dim3 grid(num_heads, num_seqs);
   if (head_dim == 128) {
-    if (wide) {
-      static bool done[64] = {false};
-      int rc = ensure_smem(reduce_kernel<128, 16>, kMaxSmem, done, 64);
-      if (rc != PKV_OK) return rc;
-      reduce_kernel<128, 16><<<grid, 16 * 32, smem, st>>>(
-          static_cast<uint16_t*>(out), tmp, ml, es, context_lens, num_heads, np_max,
-          partition_size, prefix_blocks, block_size, slot_split,
-          prefix_partition > 0 ? prefix_partition : partition_size, device_error_ptr());
-    } else {
-      static bool done[64] = {false};
-      int rc = ensure_smem(reduce_kernel<128, 4>, kMaxSmem, done, 64);
-      if (rc != PKV_OK) return rc;
-      reduce_kernel<128, 4><<<grid, 4 * 32, smem, st>>>(
-          static_cast<uint16_t*>(out), tmp, ml, es, context_lens, num_heads, np_max,
-          partition_size, prefix_blocks, block_size, slot_split,
-          prefix_partition > 0 ? prefix_partition : partition_size, device_error_ptr());
-    }
+    static bool done[64] = {false};
+    int rc = ensure_smem(reduce_kernel<128, 16>, kMaxSmem, done, 64);
+    if (rc != PKV_OK) return rc;
+    reduce_kernel<128, 16><<<grid, 16 * 32, smem, st>>>(o, tmp, ml, es, context_lens, num_heads,
+                                                        np_max, partition_size, prefix_blocks,
+                                                        block_size, slot_split, pp, err);
   } else {
-    if (wide) {
-      static bool done[64] = {false};
-      int rc = ensure_smem(reduce_kernel<256, 16>, kMaxSmem, done, 64);
-      if (rc != PKV_OK) return rc;
-      reduce_kernel<256, 16><<<grid, 16 * 32, smem, st>>>(
-          static_cast<uint16_t*>(out), tmp, ml, es, context_lens, num_heads, np_max,
-          partition_size, prefix_blocks, block_size, slot_split,
-          prefix_partition > 0 ? prefix_partition : partition_size, device_error_ptr());
-    } else {
-      static bool done[64] = {false};
-      int rc = ensure_smem(reduce_kernel<256, 4>, kMaxSmem, done, 64);
-      if (rc != PKV_OK) return rc;
-      reduce_kernel<256, 4><<<grid, 4 * 32, smem, st>>>(
-          static_cast<uint16_t*>(out), tmp, ml, es, context_lens, num_heads, np_max,
-          partition_size, prefix_blocks, block_size, slot_split,
-          prefix_partition > 0 ? prefix_partition : partition_size, device_error_ptr());
-    }
+    static bool done[64] = {false};
+    int rc = ensure_smem(reduce_kernel<256, 16>, kMaxSmem, done, 64);
+    if (rc != PKV_OK) return rc;
+    reduce_kernel<256, 16><<<grid, 16 * 32, smem, st>>>(o, tmp, ml, es, context_lens, num_heads,
+                                                        np_max, partition_size, prefix_blocks,
+                                                        block_size, slot_split, pp, err);
   }
   return launch_status();
 }
