@@ -1,5 +1,6 @@
 """Parity at the full workload sizes, in the launch configuration the
-benchmark times (split decode + reduce, every layer). The oracle checks a
+benchmark times (split decode + reduce, every layer; the shared-prefix decode
+replayed from a CUDA graph for the copy-on-write rollouts). The oracle checks a
 seeded sample of sequences one by one; copy-on-write clones are checked bit
 for bit."""
 import numpy as np
@@ -85,7 +86,18 @@ def test_cow_rollouts(prompt_len, _lib):
                 assert np.array_equal(got, want)
     out = _step(pw)[0]
     seqs = _sample(w.num_seqs, 30, 4)
-    assert_close(out[seqs], expected(w, 0, seqs), "cow %d" % prompt_len)
+    ref = expected(w, 0, seqs)
+    assert_close(out[seqs], ref, "cow %d" % prompt_len)
+    # the shared-prefix decode as the benchmark runs it (a replayed CUDA graph)
+    groups = workload.prefix_groups(pw)
+    P = w.partition_size
+    ws = pkv.shared_prefix_workspace(w.num_seqs, w.num_heads, w.head_dim, pw.max_context,
+                                     groups[2] * w.block_size, P)
+    sp = [torch.empty_like(pw.layers[0].q)]
+    g = workload.capture_step(pw, sp, ws, P, groups=groups)
+    g.replay()
+    torch.cuda.synchronize()
+    assert_close(sp[0].cpu()[seqs], ref, "cow %d shared prefix" % prompt_len)
     assert int(_lib.item()) == 0
 
 
