@@ -8,9 +8,11 @@
 //
 // Data movement (the part that sets the speed, decode being bound by HBM):
 // - a producer warp reads the block table and loads every (block, head) page
-//   of K and V with TMA tensor copies (cp.async.bulk.tensor, one 128-byte x B
-//   box per 64 head-dim columns, 128-byte swizzle) into a ring of shared
-//   memory stages; an mbarrier per stage counts the bytes in;
+//   of K and V with TMA tensor copies into a ring of shared memory stages, one
+//   3-D box per page (cp.async.bulk.tensor over a [128-byte chunk][row][128 B]
+//   view of the pool, 128-byte swizzle), which lands as [chunk][B rows][128 B];
+//   an mbarrier per stage counts the bytes in. One instruction per page
+//   instead of one per chunk measured 0.1-0.7 % faster across the workloads;
 // - the swizzle makes the row-strided fragment loads below bank-conflict
 //   free although a page row is 256 or 512 bytes long.
 //
@@ -47,8 +49,6 @@ struct TcGeom {
   static_assert(NST % NW == 0, "stages must be private to a consumer warp");
   static constexpr int kEsz = FP8 ? 1 : 2;
   static constexpr int kPage = BS * D * kEsz;
-  static constexpr int kChunks = D * kEsz / 128;  // TMA boxes per page
-  static constexpr int kBoxCols = 128 / kEsz;     // elements per box row
   static constexpr int kStage = 2 * kPage;
   static constexpr int kRing = NST * kStage;
   // warp states [NW][8][D] + max/sum, then the CTA state [8][D] + max/sum
@@ -137,11 +137,8 @@ __global__ void __launch_bounds__(TcGeom<D, BS, FP8, NW, NST>::kThreads)
         const uint32_t kdst = ring + st * G::kStage;
         const int y = (pb * p.num_kv_heads + h) * BS;
         mbar_arrive_expect_tx(&full[st], 2 * PAGE);
-#pragma unroll
-        for (int c = 0; c < G::kChunks; ++c) {
-          tma_load_2d(kdst + c * BS * 128, &tmk, c * G::kBoxCols, y, &full[st]);
-          tma_load_2d(kdst + PAGE + c * BS * 128, &tmv, c * G::kBoxCols, y, &full[st]);
-        }
+        tma_load_page(kdst, &tmk, y, &full[st]);
+        tma_load_page(kdst + PAGE, &tmv, y, &full[st]);
       }
     }
   } else {
@@ -587,9 +584,9 @@ int launch_decode_tc(const DecodeParams& p, const void* k_cache, const void* v_c
                      int head_dim, int block_size, bool fp8, dim3 grid, cudaStream_t st) {
   const int64_t rows = static_cast<int64_t>(p.num_blocks) * p.num_kv_heads * block_size;
   CUtensorMap tk, tv;
-  int rc = pool_tensor_map(&tk, k_cache, rows, head_dim, block_size, fp8);
+  int rc = pool_tensor_map(&tk, k_cache, rows, head_dim, block_size, fp8, true);
   if (rc != PKV_OK) return rc;
-  rc = pool_tensor_map(&tv, v_cache, rows, head_dim, block_size, fp8);
+  rc = pool_tensor_map(&tv, v_cache, rows, head_dim, block_size, fp8, true);
   if (rc != PKV_OK) return rc;
   return fp8 ? dispatch_tc<true>(p, tk, tv, head_dim, block_size, grid, st)
              : dispatch_tc<false>(p, tk, tv, head_dim, block_size, grid, st);
