@@ -388,6 +388,16 @@ int pkv_alloc_stats(const pkv_allocator* a, int* free_blocks, int* used_blocks,
  *   3. give every running request one slot for this iteration's token; if the
  *      pool runs dry, the most recently admitted request is preempted (freed
  *      and put back at the head of the queue, to be recomputed).
+ * Swap mode (pkv_sched_set_preemption(s, PKV_PREEMPT_SWAP); [Dissect]
+ * "Continuous Batching: Breaking the Sequence Barrier" and "FAQ": preempted
+ * sequences' blocks go to CPU RAM): a preempted request keeps its progress;
+ * its block list is reported (event 3, pkv_sched_swap_blocks) and the caller
+ * copies those blocks out (pkv_swap_out) before anything is written in this
+ * iteration, since the blocks are already free. Swapped requests are resumed
+ * first, before step 2, when the free blocks cover their length plus one
+ * token: fresh blocks for the whole length are reported (event 4,
+ * pkv_sched_swap_blocks) and the caller copies the saved blocks back
+ * (pkv_swap_in) before this iteration's writes. Nothing is recomputed.
  * After a step, the running batch (admission order) is read with
  * pkv_sched_running / pkv_sched_block_tables; context_len counts the token of
  * this iteration. The scheduler uses the allocator through its public calls;
@@ -415,10 +425,24 @@ int pkv_sched_block_tables(const pkv_scheduler* s, int32_t* tables, int max_bloc
 /* Prompt slots of a request admitted in the last step (n = prompt length). */
 int pkv_sched_prompt_slots(const pkv_scheduler* s, int64_t request_id,
                            int64_t* slots, int cap, int* n);
-/* Ids of the last step's events: kind 0 admitted, 1 finished, 2 preempted. */
+/* Ids of the last step's events: kind 0 admitted, 1 finished, 2 preempted,
+ * 3 swapped out, 4 swapped in (resumed). A request resumed and preempted
+ * again in the same step appears in neither 3 nor 4 (its saved copy stays
+ * valid). */
 int pkv_sched_events(const pkv_scheduler* s, int kind, int64_t* ids, int cap, int* n);
+/* waiting counts queued and swapped-out requests. */
 int pkv_sched_counts(const pkv_scheduler* s, int* waiting, int* running,
                      long long* steps);
+
+#define PKV_PREEMPT_RECOMPUTE 0
+#define PKV_PREEMPT_SWAP 1
+/* Preemption policy (default PKV_PREEMPT_RECOMPUTE). */
+int pkv_sched_set_preemption(pkv_scheduler* s, int mode);
+/* Block list (logical order) of a request swapped out or in during the last
+ * step: the blocks to copy to host memory, or the fresh blocks to copy back
+ * into. n = number of blocks; PKV_ERR_NOT_FOUND for any other request. */
+int pkv_sched_swap_blocks(const pkv_scheduler* s, int64_t request_id, int32_t* blocks,
+                          int cap, int* n);
 
 #ifdef __cplusplus
 }

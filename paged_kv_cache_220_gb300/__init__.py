@@ -35,6 +35,8 @@ PKV_ERR_NOT_FOUND = -5
 PKV_ERR_DEVICE_CHECK = -6
 PKV_DTYPE_BF16 = 0
 PKV_DTYPE_FP8_E4M3 = 1
+PKV_PREEMPT_RECOMPUTE = 0
+PKV_PREEMPT_SWAP = 1
 
 DEVERR_NONE = 0
 DEVERR_BLOCK_ID = 1
@@ -98,6 +100,8 @@ SIGNATURES = {
     "pkv_sched_block_tables": (_I, [_P, _P, _I, _I]),
     "pkv_sched_prompt_slots": (_I, [_P, ctypes.c_int64, _P, _I, ctypes.POINTER(_I)]),
     "pkv_sched_events": (_I, [_P, _I, _P, _I, ctypes.POINTER(_I)]),
+    "pkv_sched_set_preemption": (_I, [_P, _I]),
+    "pkv_sched_swap_blocks": (_I, [_P, ctypes.c_int64, _P, _I, ctypes.POINTER(_I)]),
     "pkv_sched_counts": (_I, [_P, ctypes.POINTER(_I), ctypes.POINTER(_I),
                               ctypes.POINTER(ctypes.c_longlong)]),
 }
@@ -511,8 +515,26 @@ class Scheduler:
                                             ctypes.byref(n)), "sched_prompt_slots")
         return out[:n.value]
 
+    def set_preemption(self, mode: int) -> None:
+        """PKV_PREEMPT_RECOMPUTE (default) or PKV_PREEMPT_SWAP."""
+        _check(lib().pkv_sched_set_preemption(self._h, int(mode)), "sched_set_preemption")
+
+    def swap_blocks(self, request_id: int) -> np.ndarray:
+        """Block list of a request swapped out (blocks to save) or in (blocks
+        to restore) in the last step, int32, logical order."""
+        n = ctypes.c_int()
+        rc = lib().pkv_sched_swap_blocks(self._h, int(request_id), None, 0, ctypes.byref(n))
+        if rc not in (PKV_OK, PKV_ERR_INVALID_ARG):
+            _check(rc, "sched_swap_blocks")
+        out = np.empty(max(n.value, 1), np.int32)
+        _check(lib().pkv_sched_swap_blocks(self._h, int(request_id),
+                                           out.ctypes.data_as(ctypes.c_void_p), out.size,
+                                           ctypes.byref(n)), "sched_swap_blocks")
+        return out[:n.value]
+
     def events(self, kind: int) -> np.ndarray:
-        """kind 0: admitted, 1: finished, 2: preempted (in the last step)."""
+        """kind 0: admitted, 1: finished, 2: preempted, 3: swapped out,
+        4: swapped in (in the last step)."""
         n = ctypes.c_int()
         buf = np.empty(4096, np.int64)
         _check(lib().pkv_sched_events(self._h, int(kind), buf.ctypes.data_as(ctypes.c_void_p),

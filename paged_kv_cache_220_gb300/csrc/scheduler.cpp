@@ -21,7 +21,14 @@
 //   3. grow: every running request takes one slot for this iteration's token.
 //      If the pool cannot supply a block, the most recently admitted running
 //      request is preempted: its sequence is freed and it goes back to the
-//      front of the queue to be recomputed from its prompt later.
+//      front of the queue to be recomputed from its prompt later, or, in swap
+//      mode, its block list is reported so the caller can copy the blocks to
+//      host memory before they are reused ("Dissecting vLLM ...", sections
+//      "Continuous Batching: Breaking the Sequence Barrier" and "FAQ": the
+//      preempted sequence's blocks go to CPU RAM and come back later).
+// Swapped requests are resumed before new ones are admitted: a resumed
+// request gets fresh blocks for its whole length (reported, for the copy
+// back) and continues where it stopped; nothing is recomputed.
 // EOS is a request's own token budget (max_new_tokens), known up front.
 #include <algorithm>
 #include <cstdint>
@@ -40,6 +47,7 @@ struct Req {
   int generated;  // tokens produced so far (the one of this iteration included)
   int seq;        // allocator sequence id while running
   std::vector<int64_t> prompt_slots;  // reported in the admitting iteration
+  std::vector<int32_t> swap_blocks;   // swap mode: blocks to copy out / back in
 };
 
 }  // namespace
@@ -55,6 +63,10 @@ struct pkv_scheduler {
   std::vector<int64_t> admitted;            // ids admitted in the last step
   std::vector<int64_t> new_slots;           // per running request, last step
   int64_t steps = 0;
+  int preempt_mode = PKV_PREEMPT_RECOMPUTE;
+  std::deque<Req> swapped;                  // swapped-out requests, resume order
+  std::vector<Req> swapped_out;             // swapped out in the last step (for their blocks)
+  std::vector<int64_t> swapped_in;          // ids resumed in the last step
 };
 
 extern "C" int pkv_sched_create(pkv_allocator* alloc, int block_size, int max_num_seqs,
@@ -102,15 +114,44 @@ int growth_blocks(const pkv_scheduler* s) {
   return n;
 }
 
-void preempt_last(pkv_scheduler* s) {
+int preempt_last(pkv_scheduler* s) {
   Req r = std::move(s->running.back());
   s->running.pop_back();
-  pkv_seq_free(s->alloc, r.seq);
   s->preempted.push_back(r.id);
+  r.prompt_slots.clear();
+  if (s->preempt_mode == PKV_PREEMPT_SWAP) {
+    // resumed in this very step: its blocks were never filled and the host
+    // copy is still the valid one, so it goes back without a copy-out
+    auto it = std::find(s->swapped_in.begin(), s->swapped_in.end(), r.id);
+    if (it != s->swapped_in.end()) {
+      s->swapped_in.erase(it);
+      pkv_seq_free(s->alloc, r.seq);
+      r.seq = -1;
+      r.swap_blocks.clear();
+      s->swapped.push_front(std::move(r));
+      return PKV_OK;
+    }
+    // the block list in logical order: the caller copies these blocks out
+    // before anything is written this iteration
+    const int64_t len = static_cast<int64_t>(r.prompt_len) + r.generated;
+    const int nb = blocks_for(len, s->block_size);
+    r.swap_blocks.assign(nb > 0 ? nb : 1, -1);
+    int n = 0;
+    const int rc = pkv_seq_block_table(s->alloc, r.seq, r.swap_blocks.data(), nb > 0 ? nb : 1, &n);
+    if (rc != PKV_OK) return rc;
+    r.swap_blocks.resize(n);
+    pkv_seq_free(s->alloc, r.seq);
+    r.seq = -1;
+    s->swapped_out.push_back(r);  // keeps the block list for pkv_sched_swap_blocks
+    r.swap_blocks.clear();
+    s->swapped.push_front(std::move(r));
+    return PKV_OK;
+  }
+  pkv_seq_free(s->alloc, r.seq);
   r.seq = -1;
   r.generated = 0;  // recomputed from the prompt when it is admitted again
-  r.prompt_slots.clear();
   s->waiting.push_front(std::move(r));
+  return PKV_OK;
 }
 
 }  // namespace
@@ -122,6 +163,8 @@ extern "C" int pkv_sched_step(pkv_scheduler* s, int* num_running, int* num_admit
     s->finished.clear();
     s->preempted.clear();
     s->admitted.clear();
+    s->swapped_out.clear();
+    s->swapped_in.clear();
     // 1. eject
     std::vector<Req> keep;
     keep.reserve(s->running.size());
@@ -135,8 +178,38 @@ extern "C" int pkv_sched_step(pkv_scheduler* s, int* num_running, int* num_admit
       }
     }
     s->running.swap(keep);
-    // 2. admit
-    while (!s->waiting.empty() && static_cast<int>(s->running.size()) < s->max_num_seqs) {
+    // 2a. resume swapped requests first: fresh blocks for their whole length
+    while (!s->swapped.empty() && static_cast<int>(s->running.size()) < s->max_num_seqs) {
+      Req& w = s->swapped.front();
+      const int64_t len = static_cast<int64_t>(w.prompt_len) + w.generated;
+      const int need = blocks_for(len + 1, s->block_size);
+      if (need + growth_blocks(s) > free_blocks(s)) break;
+      Req r = std::move(w);
+      s->swapped.pop_front();
+      int sid = -1;
+      int rc = pkv_seq_new(s->alloc, &sid);
+      if (rc != PKV_OK) return rc;
+      r.seq = sid;
+      if (len > 0) {
+        std::vector<int64_t> slots(static_cast<size_t>(len));
+        rc = pkv_seq_append(s->alloc, sid, static_cast<int>(len), slots.data(), nullptr, nullptr);
+        if (rc != PKV_OK) {
+          pkv_seq_free(s->alloc, sid);
+          return rc;
+        }
+      }
+      const int nb = blocks_for(len, s->block_size);
+      r.swap_blocks.assign(nb > 0 ? nb : 1, -1);
+      int n = 0;
+      rc = pkv_seq_block_table(s->alloc, sid, r.swap_blocks.data(), nb > 0 ? nb : 1, &n);
+      if (rc != PKV_OK) return rc;
+      r.swap_blocks.resize(n);
+      s->swapped_in.push_back(r.id);
+      s->running.push_back(std::move(r));
+    }
+    // 2b. admit
+    while (s->swapped.empty() && !s->waiting.empty() &&
+           static_cast<int>(s->running.size()) < s->max_num_seqs) {
       Req& w = s->waiting.front();
       const int need = blocks_for(static_cast<int64_t>(w.prompt_len) + 1, s->block_size);
       if (need + growth_blocks(s) > free_blocks(s)) break;
@@ -173,15 +246,20 @@ extern "C" int pkv_sched_step(pkv_scheduler* s, int* num_running, int* num_admit
       if (rc != PKV_ERR_OUT_OF_BLOCKS) return rc;
       // the request being grown may itself be the newest one
       const bool self = (i + 1 == s->running.size());
-      preempt_last(s);
+      const int prc = preempt_last(s);
+      if (prc != PKV_OK) return prc;
       if (self) break;
     }
-    // a preempted request may have been admitted in this very step
-    std::vector<int64_t> adm;
-    for (int64_t id : s->admitted)
-      for (const Req& r : s->running)
-        if (r.id == id) adm.push_back(id);
-    s->admitted.swap(adm);
+    // a preempted request may have been admitted or resumed in this very step
+    auto still_running = [&](std::vector<int64_t>& ids) {
+      std::vector<int64_t> keep_ids;
+      for (int64_t id : ids)
+        for (const Req& r : s->running)
+          if (r.id == id) keep_ids.push_back(id);
+      ids.swap(keep_ids);
+    };
+    still_running(s->admitted);
+    still_running(s->swapped_in);
   } catch (...) {
     return PKV_ERR_OUT_OF_BLOCKS;
   }
@@ -237,9 +315,15 @@ extern "C" int pkv_sched_prompt_slots(const pkv_scheduler* s, int64_t request_id
 extern "C" int pkv_sched_events(const pkv_scheduler* s, int kind, int64_t* ids, int cap,
                                 int* n) {
   if (!s || !n) return PKV_ERR_INVALID_ARG;
+  std::vector<int64_t> out_ids;
   const std::vector<int64_t>* v = kind == 0 ? &s->admitted
                                   : kind == 1 ? &s->finished
-                                  : kind == 2 ? &s->preempted : nullptr;
+                                  : kind == 2 ? &s->preempted
+                                  : kind == 4 ? &s->swapped_in : nullptr;
+  if (kind == 3) {
+    for (const Req& r : s->swapped_out) out_ids.push_back(r.id);
+    v = &out_ids;
+  }
   if (!v) return PKV_ERR_INVALID_ARG;
   *n = static_cast<int>(v->size());
   if (cap < *n || (*n > 0 && !ids)) return PKV_ERR_INVALID_ARG;
@@ -247,10 +331,34 @@ extern "C" int pkv_sched_events(const pkv_scheduler* s, int kind, int64_t* ids, 
   return PKV_OK;
 }
 
+extern "C" int pkv_sched_set_preemption(pkv_scheduler* s, int mode) {
+  if (!s || (mode != PKV_PREEMPT_RECOMPUTE && mode != PKV_PREEMPT_SWAP)) return PKV_ERR_INVALID_ARG;
+  s->preempt_mode = mode;
+  return PKV_OK;
+}
+
+extern "C" int pkv_sched_swap_blocks(const pkv_scheduler* s, int64_t request_id,
+                                     int32_t* blocks, int cap, int* n) {
+  if (!s || !n) return PKV_ERR_INVALID_ARG;
+  const std::vector<int32_t>* v = nullptr;
+  for (const Req& r : s->swapped_out)
+    if (r.id == request_id) v = &r.swap_blocks;
+  if (!v)
+    for (int64_t id : s->swapped_in)
+      if (id == request_id)
+        for (const Req& r : s->running)
+          if (r.id == request_id) v = &r.swap_blocks;
+  if (!v) return PKV_ERR_NOT_FOUND;
+  *n = static_cast<int>(v->size());
+  if (cap < *n || (*n > 0 && !blocks)) return PKV_ERR_INVALID_ARG;
+  std::copy(v->begin(), v->end(), blocks);
+  return PKV_OK;
+}
+
 extern "C" int pkv_sched_counts(const pkv_scheduler* s, int* waiting, int* running,
                                 long long* steps) {
   if (!s) return PKV_ERR_INVALID_ARG;
-  if (waiting) *waiting = static_cast<int>(s->waiting.size());
+  if (waiting) *waiting = static_cast<int>(s->waiting.size() + s->swapped.size());
   if (running) *running = static_cast<int>(s->running.size());
   if (steps) *steps = s->steps;
   return PKV_OK;

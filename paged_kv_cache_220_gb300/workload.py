@@ -252,11 +252,17 @@ class ContinuousBatch:
     request the slot of this iteration's token; then the new K/V rows are
     written and the split decode + merge runs over the running batch. K/V rows
     and queries come from per-request streams (synth.request_rows /
-    request_query), so any iteration can be checked on the host."""
+    request_query), so any iteration can be checked on the host.
+
+    preemption="swap": a request preempted under memory pressure keeps its
+    progress: its blocks are copied to pinned host memory (swap_out) before
+    anything is written in that iteration, and copied back into fresh blocks
+    (swap_in) when it is resumed; without it, preempted requests are
+    recomputed from their prompts."""
 
     def __init__(self, seed, requests, num_blocks, block_size=32, num_heads=24,
                  num_kv_heads=4, head_dim=256, max_num_seqs=64, partition_size=512,
-                 device="cuda", alloc_seed=None):
+                 device="cuda", alloc_seed=None, preemption="recompute"):
         self.seed = seed
         self.B = block_size
         self.Hq, self.Hk, self.D = num_heads, num_kv_heads, head_dim
@@ -265,6 +271,13 @@ class ContinuousBatch:
         self.alloc = pkv.BlockAllocator(num_blocks, block_size,
                                         seed=seed if alloc_seed is None else alloc_seed)
         self.sched = pkv.Scheduler(self.alloc, max_num_seqs)
+        if preemption not in ("recompute", "swap"):
+            raise ValueError("preemption: 'recompute' or 'swap'")
+        if preemption == "swap":
+            self.sched.set_preemption(pkv.PKV_PREEMPT_SWAP)
+        self.saved = {}       # request id -> pinned host (K, V) blocks
+        self.retired = []     # host buffers whose swap_in may still be in flight
+        self.swaps = 0
         self.max_num_seqs = max_num_seqs
         self.max_context = max(p + g for _, p, g in requests)
         self.max_blocks = -(-self.max_context // block_size)
@@ -289,9 +302,26 @@ class ContinuousBatch:
         """One iteration; returns (request_ids, context_lens, out[:n]) or None
         when nothing is running."""
         n, na, _ = self.sched.step()
+        dev = self.device
+        if self.retired:
+            torch.cuda.current_stream(dev).synchronize()
+            self.retired.clear()
+        # swapped-out blocks are already free: save them before any write
+        for rid in self.sched.events(3):
+            blocks = torch.as_tensor(self.sched.swap_blocks(int(rid)), device=dev)
+            shape = (blocks.numel(),) + tuple(self.k_cache.shape[1:])
+            kb = torch.empty(shape, dtype=self.k_cache.dtype, pin_memory=True)
+            vb = torch.empty(shape, dtype=self.v_cache.dtype, pin_memory=True)
+            pkv.swap_out(self.k_cache, self.v_cache, blocks, kb, vb)
+            self.saved[int(rid)] = (kb, vb)
+            self.swaps += 1
+        for rid in self.sched.events(4):
+            blocks = torch.as_tensor(self.sched.swap_blocks(int(rid)), device=dev)
+            kb, vb = self.saved.pop(int(rid))
+            pkv.swap_in(self.k_cache, self.v_cache, blocks, kb, vb)
+            self.retired.append((kb, vb))
         if n == 0:
             return None
-        dev = self.device
         for rid in self.sched.events(0):
             slots = self.sched.prompt_slots(int(rid))
             if len(slots) == 0:

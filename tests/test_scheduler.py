@@ -117,3 +117,68 @@ def test_bad_arguments():
         sched.add_request(0, 10, 0)
     with pytest.raises(pkv.PagedKVError):
         sched.prompt_slots(5)
+
+
+def test_swap_preemption_keeps_progress_and_cache_contents():
+    """Swap mode on a host model of the pool: every slot holds the identity
+    of the token written there. Swapped-out blocks are saved before this
+    iteration's writes, restored into the fresh blocks on resume, and every
+    running request's table always reads back its own tokens 0..ctx-1; no
+    request is admitted (prefilled) twice."""
+    B = 16
+    NB = 40
+    alloc = pkv.BlockAllocator(NB, B, seed=5)
+    sched = pkv.Scheduler(alloc, max_num_seqs=8)
+    sched.set_preemption(pkv.PKV_PREEMPT_SWAP)
+    reqs = synth.request_mix(11, 24, prompt_lo=16, prompt_hi=200, gen_lo=16, gen_hi=300)
+    for rid, p, g in reqs:
+        sched.add_request(rid, p, g)
+    pool = np.full((NB, B), -1, dtype=np.int64)
+    saved = {}
+
+    def tok(rid, pos):
+        return int(rid) * 1_000_000 + int(pos)
+
+    admitted, done = [], set()
+    swaps_out = swaps_in = 0
+    for _ in range(20000):
+        n, _, _ = sched.step()
+        for rid in sched.events(3):
+            blocks = sched.swap_blocks(int(rid))
+            saved[int(rid)] = pool[blocks].copy()
+            swaps_out += 1
+        for rid in sched.events(4):
+            blocks = sched.swap_blocks(int(rid))
+            rows = saved.pop(int(rid))
+            assert rows.shape[0] == len(blocks)
+            pool[blocks] = rows
+            swaps_in += 1
+        for rid in sched.events(0):
+            admitted.append(int(rid))
+            for pos, slot in enumerate(sched.prompt_slots(int(rid))):
+                pool[slot // B, slot % B] = tok(rid, pos)
+        done |= set(sched.events(1).tolist())
+        if n:
+            ids, ctx, slots = sched.running()
+            for rid, c, slot in zip(ids, ctx, slots):
+                pool[slot // B, slot % B] = tok(rid, c - 1)
+            tables = sched.block_tables(4096)
+            for i, (rid, c) in enumerate(zip(ids, ctx)):
+                got = [pool[tables[i][pos // B], pos % B] for pos in range(int(c))]
+                assert got == [tok(rid, pos) for pos in range(int(c))]
+            _check(alloc, sched, B)
+        if n == 0 and sched.counts()["waiting"] == 0:
+            break
+    assert done == set(range(24))
+    assert swaps_out > 0 and swaps_in == swaps_out and not saved
+    assert sorted(admitted) == list(range(24))       # nothing prefilled twice
+    assert alloc.stats()["free_blocks"] == NB
+
+
+def test_swap_mode_arguments():
+    alloc = pkv.BlockAllocator(8, 16)
+    sched = pkv.Scheduler(alloc, 4)
+    with pytest.raises(pkv.PagedKVError):
+        sched.set_preemption(7)
+    with pytest.raises(pkv.PagedKVError):
+        sched.swap_blocks(3)
