@@ -448,6 +448,17 @@ def main():
     }
     if w.prefix_len > 0:
         line["unique_bytes_gbs"] = round(unique_decode_bytes(w) * L * world / (ms_per_step / 1e3) / 1e9, 2)
+    if traffic:
+        line["roofline"]["traffic_over_bytes"] = round(traffic / dec_bytes, 4)
+    # the pages' memory claims, on this workload's allocation: slots held in
+    # partly filled blocks, and the slots a contiguous max-length reservation
+    # per sequence would take
+    st = pw.alloc.stats()
+    held = st["used_blocks"] * w.block_size
+    line["memory"] = {
+        "internal_fragmentation": round(1 - st["used_slots"] / held, 4) if held else 0.0,
+        "contiguous_over_paged_slots": round(w.num_seqs * pw.max_context / held, 3) if held else None,
+    }
     print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
