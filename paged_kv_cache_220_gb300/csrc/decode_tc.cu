@@ -16,19 +16,26 @@
 // - the swizzle makes the row-strided fragment loads below bank-conflict
 //   free although a page row is 256 or 512 bytes long.
 //
-// Arithmetic, per 16-token slice of a page (one consumer warp per page):
-// - S^T[16 tokens x 8] = K_slice[16 x D] . Q^T[D x 8] with mma.m16n8k16
-//   (bf16 in, fp32 out); tokens are the M side, the padded query group the N
-//   side, Q's fragments stay in registers for the whole CTA;
+// Arithmetic, per 16-token slice of a page; the NW consumer warps all work on
+// every page, warp w on head-dim columns [w*D/NW, (w+1)*D/NW):
+// - partial S^T[16 tokens x 8] = K_slice[16 x D/NW] . Q^T[D/NW x 8] with
+//   mma.m16n8k16 (bf16 in, fp32 out); tokens are the M side, the padded
+//   query group the N side, Q's fragments stay in registers for the whole CTA;
+// - the warps exchange the partials through shared memory (an mbarrier per
+//   slice parity) and sum them in warp order, so every warp holds the same
+//   logits and softmax state;
 // - online softmax on the accumulator fragment (base 2, logit scale applied
 //   in fp32); per-query maxima across the 16 tokens by three xor shuffles;
 // - the probabilities are split into a bf16 high part and a bf16 remainder
 //   (P = P_hi + P_lo to ~16 bits), turned into the B operand of the next
 //   product with movmatrix (an 8x8 transpose in registers);
-// - O^T[D x 8] += V_slice^T[D x 16] . P^T[16 x 8] with mma.m16n8k16, V^T's
-//   fragments read by ldmatrix.trans from the swizzled page.
-// At the end the consumer warps' states are merged in a fixed order, so the
-// result depends on logical positions only.
+// - O^T[D/NW x 8] += V_slice^T[D/NW x 16] . P^T[16 x 8] with mma.m16n8k16,
+//   V^T's fragments read by ldmatrix.trans from the swizzled page.
+// Every warp writes its own columns of the result; the summation order is a
+// function of logical positions only. (Against one page per consumer warp
+// with the warp states merged at the end, measured on GB300: Qwen-like step
+// 5.002 -> 4.952 ms, long FP8 0.3815 -> 0.3725, mixed lengths equal, the
+// copy-on-write rollouts' short own parts 0.2388 -> 0.2442 ms.)
 #include <cmath>
 #include <cudaTypedefs.h>
 #include <mutex>
@@ -40,21 +47,30 @@
 
 namespace pkv {
 
-// NST is a multiple of NW: page `it` goes to consumer warp it % NW and to
-// stage it % NST, so every stage belongs to one warp. A warp therefore waits
-// on a stage's phase k only after it released phase k-1 itself, and the
-// parity test of the wait cannot alias an older phase.
+// NW consumer warps share every page: warp w owns head-dim columns
+// [w*D/NW, (w+1)*D/NW). For each 16-token slice it computes the logits'
+// partial sum over its columns, the warps exchange the partials through
+// shared memory (summed in warp order, so every warp holds the same logits
+// and the same softmax state) and each warp accumulates P.V for its own
+// columns. A page's stage is released when all NW warps are done with it.
+// Spreading one page over NW warps shortens the time a stage is held, so
+// more of the ring is in flight (a probe that only streams pages reads
+// 7.4 TB/s; the stage hold time is what keeps the decode below that).
 template <int D, int BS, bool FP8, int NW, int NST>
 struct TcGeom {
-  static_assert(NST % NW == 0, "stages must be private to a consumer warp");
   static constexpr int kEsz = FP8 ? 1 : 2;
   static constexpr int kPage = BS * D * kEsz;
   static constexpr int kStage = 2 * kPage;
   static constexpr int kRing = NST * kStage;
-  // warp states [NW][8][D] + max/sum, then the CTA state [8][D] + max/sum
-  static constexpr int kMerge = NW * 8 * D * 4 + 2 * NW * 8 * 4 + 8 * D * 4 + 2 * 8 * 4;
+  static constexpr int kDW = D / NW;       // head-dim columns per consumer warp
+  static constexpr int kKW = kDW / 16;     // their k-steps (and 16-row tiles of O^T)
+  static_assert(kKW >= 1 && (!FP8 || kKW % 2 == 0), "consumer warp column slice");
+  // logit partials of one slice, double buffered: [2][NW][32 lanes] float4
+  static constexpr int kXchg = 2 * NW * 32 * 16;
+  // cluster merge: CTA state [8][D] + max/sum
+  static constexpr int kMerge = 8 * D * 4 + 2 * 8 * 4;
   static constexpr int kSmem = 1024 /*barriers*/ + 1024 /*alignment*/ +
-                               (kRing > kMerge ? kRing : kMerge);
+                               (kRing > kMerge ? kRing : kMerge) + kXchg;
   static constexpr int kThreads = (NW + 1) * 32;
 };
 
@@ -65,15 +81,18 @@ __global__ void __launch_bounds__(TcGeom<D, BS, FP8, NW, NST>::kThreads)
   using G = TcGeom<D, BS, FP8, NW, NST>;
   constexpr int PAGE = G::kPage;
   constexpr int ESZ = G::kEsz;
-  constexpr int KT = D / 16;  // k-steps of Q.K^T == 16-row tiles of O^T
+  constexpr int KW = G::kKW;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* sbase = smem_raw + (base - raw);
   uint64_t* full = reinterpret_cast<uint64_t*>(sbase);
   uint64_t* empty = full + NST;
+  uint64_t* xfull = empty + NST;  // [2] logit partials of a slice are in
   const uint32_t ring = base + 1024;
   float* ring_f = reinterpret_cast<float*>(sbase + 1024);
+  constexpr int kRegion = G::kRing > G::kMerge ? G::kRing : G::kMerge;
+  float4* xs = reinterpret_cast<float4*>(sbase + 1024 + kRegion);
 
   const int part = blockIdx.x;
   const int h = blockIdx.y;
@@ -109,16 +128,20 @@ __global__ void __launch_bounds__(TcGeom<D, BS, FP8, NW, NST>::kThreads)
   if (threadIdx.x == 0) {
     for (int i = 0; i < NST; ++i) {
       mbar_init(&full[i], 1);
-      mbar_init(&empty[i], 1);
+      mbar_init(&empty[i], NW);
     }
+    mbar_init(&xfull[0], NW * 32);
+    mbar_init(&xfull[1], NW * 32);
     fence_mbar_init();
   }
   __syncthreads();
 
   int issued = 0;  // producer lane 0 only
   // per-thread softmax state for queries q0 = 2*(lane%4), q1 = q0 + 1
+  // (the same in every consumer warp)
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-  float o[KT][4];
+  float o[KW][4];  // O^T tiles of this warp's columns
+  const int kw0 = warp * KW;  // first k-step of this warp
 
   if (warp == NW) {
     // ---------------- producer: block table walk, TMA tensor copies
@@ -143,83 +166,106 @@ __global__ void __launch_bounds__(TcGeom<D, BS, FP8, NW, NST>::kThreads)
     }
   } else {
     // ---------------- consumers
-    // Q^T fragments (B operand of m16n8k16), n = lane/4 (zero for n >= g).
+    // Q^T fragments of this warp's k-steps (B operand of m16n8k16), n = lane/4
+    // (zero for n >= g).
     // bf16: b0 = Q[n][16k + 2(lane%4) + {0,1}], b1 = the same 8 columns on.
     // FP8 (f16 operands): the contraction index of k-step k is permuted so that
     // plain ldmatrix rows of the FP8 page line up with it: b0 = Q[n][16k +
     // 4(lane%4) + {0,1}], b1 = Q[n][16k + 4(lane%4) + {2,3}].
-    uint32_t bq[KT][2];
+    uint32_t bq[KW][2];
     {
       const int n = lane >> 2;
       const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
           p.q + (static_cast<int64_t>(s) * p.num_heads + h * g + n) * D);
 #pragma unroll
-      for (int k = 0; k < KT; ++k) {
+      for (int kk = 0; kk < KW; ++kk) {
+        const int k = kw0 + kk;
         if constexpr (!FP8) {
-          bq[k][0] = n < g ? __ldg(qrow + (k * 16 + (lane & 3) * 2) / 2) : 0u;
-          bq[k][1] = n < g ? __ldg(qrow + (k * 16 + 8 + (lane & 3) * 2) / 2) : 0u;
+          bq[kk][0] = n < g ? __ldg(qrow + (k * 16 + (lane & 3) * 2) / 2) : 0u;
+          bq[kk][1] = n < g ? __ldg(qrow + (k * 16 + 8 + (lane & 3) * 2) / 2) : 0u;
         } else {
           const uint32_t w0 = n < g ? __ldg(qrow + (k * 16 + (lane & 3) * 4) / 2) : 0u;
           const uint32_t w1 = n < g ? __ldg(qrow + (k * 16 + (lane & 3) * 4 + 2) / 2) : 0u;
-          bq[k][0] = pack_f16(bf16lo(w0), bf16hi(w0));
-          bq[k][1] = pack_f16(bf16lo(w1), bf16hi(w1));
+          bq[kk][0] = pack_f16(bf16lo(w0), bf16hi(w0));
+          bq[kk][1] = pack_f16(bf16lo(w1), bf16hi(w1));
         }
       }
     }
 #pragma unroll
-    for (int k = 0; k < KT; ++k) o[k][0] = o[k][1] = o[k][2] = o[k][3] = 0.f;
+    for (int kk = 0; kk < KW; ++kk) o[kk][0] = o[kk][1] = o[kk][2] = o[kk][3] = 0.f;
     float qs = p.qscale;
     if constexpr (FP8) qs *= p.k_scale[h];
 
-    for (int it = warp; it < nblk; it += NW) {
+    bool ok = true;
+    int slice = 0;  // 16-token slices so far (exchange buffer and phase)
+    for (int it = 0; it < nblk && ok; ++it) {
       const int st = it % NST;
-      if (!mbar_wait(&full[st], (it / NST) & 1, p.err)) break;
+      if (!__all_sync(0xffffffffu, mbar_wait(&full[st], (it / NST) & 1, p.err))) break;
       const uint32_t kp = ring + st * G::kStage;
       const uint32_t vp = kp + PAGE;
       const int ntok = min(BS, ctx - (blk_begin + it) * BS);
       if (ntok < BS) {
-        // slots past the context hold whatever was there: zero their V rows so
-        // the zero probabilities cannot meet a NaN in the product
+        // slots past the context hold whatever was there: zero this warp's
+        // columns of their V rows so the zero probabilities cannot meet a NaN
         for (int r = ntok; r < BS; ++r)
-          for (int c = lane * 16; c < D * ESZ; c += 512)
-            asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(swz_bytes<BS>(vp, r, c)),
+          for (int c = lane * 16; c < G::kDW * ESZ; c += 512)
+            asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(
+                             swz_bytes<BS>(vp, r, warp * G::kDW * ESZ + c)),
                          "r"(0u)
                          : "memory");
         __syncwarp();
       }
 #pragma unroll 1
-      for (int r0 = 0; r0 < BS; r0 += 16) {
-        // ---- S^T = K_slice . Q^T (two accumulators halve the dependency chain)
+      for (int r0 = 0; r0 < BS; r0 += 16, ++slice) {
+        // ---- partial S^T = K_slice . Q^T over this warp's columns
         float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
         const int arow = r0 + (lane & 7) + ((lane >> 3) & 1) * 8;
         if constexpr (!FP8) {
           const int acol = (lane >> 4) * 16;  // bytes
 #pragma unroll
-          for (int k = 0; k < KT; ++k) {
+          for (int kk = 0; kk < KW; ++kk) {
             uint32_t a0, a1, a2, a3;
-            ldsm_x4(swz_bytes<BS>(kp, arow, k * 32 + acol), a0, a1, a2, a3);
-            mma_bf16((k & 1) ? sb : sa, a0, a1, a2, a3, bq[k][0], bq[k][1]);
+            ldsm_x4(swz_bytes<BS>(kp, arow, (kw0 + kk) * 32 + acol), a0, a1, a2, a3);
+            mma_bf16((kk & 1) ? sb : sa, a0, a1, a2, a3, bq[kk][0], bq[kk][1]);
           }
         } else {
           // one x4 load covers 16 rows x 32 codes = two k-steps; each b16 lane
           // element holds two codes, converted exactly to f16
           const int acol = (lane >> 4) * 16;
 #pragma unroll
-          for (int k = 0; k < KT; k += 2) {
+          for (int kk = 0; kk < KW; kk += 2) {
             uint32_t m0r, m1r, m2r, m3r;
-            ldsm_x4(swz_bytes<BS>(kp, arow, k * 16 + acol), m0r, m1r, m2r, m3r);
+            ldsm_x4(swz_bytes<BS>(kp, arow, (kw0 + kk) * 16 + acol), m0r, m1r, m2r, m3r);
             mma_f16(sa, e4m3x2_f16x2(m0r, 0), e4m3x2_f16x2(m1r, 0), e4m3x2_f16x2(m0r, 1),
-                    e4m3x2_f16x2(m1r, 1), bq[k][0], bq[k][1]);
+                    e4m3x2_f16x2(m1r, 1), bq[kk][0], bq[kk][1]);
             mma_f16(sb, e4m3x2_f16x2(m2r, 0), e4m3x2_f16x2(m3r, 0), e4m3x2_f16x2(m2r, 1),
-                    e4m3x2_f16x2(m3r, 1), bq[k + 1][0], bq[k + 1][1]);
+                    e4m3x2_f16x2(m3r, 1), bq[kk + 1][0], bq[kk + 1][1]);
           }
+        }
+        // ---- exchange: every warp sums the NW partials in warp order
+        const int xb = slice & 1;
+        xs[(xb * NW + warp) * 32 + lane] =
+            make_float4(sa[0] + sb[0], sa[1] + sb[1], sa[2] + sb[2], sa[3] + sb[3]);
+        mbar_arrive(&xfull[xb]);
+        if (!__all_sync(0xffffffffu, mbar_wait(&xfull[xb], (slice >> 1) & 1, p.err))) {
+          ok = false;
+          break;
+        }
+        float sv[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int w = 0; w < NW; ++w) {
+          const float4 x = xs[(xb * NW + w) * 32 + lane];
+          sv[0] += x.x;
+          sv[1] += x.y;
+          sv[2] += x.z;
+          sv[3] += x.w;
         }
         // ---- online softmax on the fragment: rows = tokens, cols = queries
         const int t0 = r0 + (lane >> 2), t1 = t0 + 8;
-        const float s00 = t0 < ntok ? (sa[0] + sb[0]) * qs : -INFINITY;
-        const float s01 = t0 < ntok ? (sa[1] + sb[1]) * qs : -INFINITY;
-        const float s10 = t1 < ntok ? (sa[2] + sb[2]) * qs : -INFINITY;
-        const float s11 = t1 < ntok ? (sa[3] + sb[3]) * qs : -INFINITY;
+        const float s00 = t0 < ntok ? sv[0] * qs : -INFINITY;
+        const float s01 = t0 < ntok ? sv[1] * qs : -INFINITY;
+        const float s10 = t1 < ntok ? sv[2] * qs : -INFINITY;
+        const float s11 = t1 < ntok ? sv[3] * qs : -INFINITY;
         float mx0 = fmaxf(s00, s10), mx1 = fmaxf(s01, s11);
 #pragma unroll
         for (int off = 4; off < 32; off <<= 1) {
@@ -232,22 +278,21 @@ __global__ void __launch_bounds__(TcGeom<D, BS, FP8, NW, NST>::kThreads)
           l0 *= c0;
           l1 *= c1;
 #pragma unroll
-          for (int k = 0; k < KT; ++k) {
-            o[k][0] *= c0;
-            o[k][1] *= c1;
-            o[k][2] *= c0;
-            o[k][3] *= c1;
+          for (int kk = 0; kk < KW; ++kk) {
+            o[kk][0] *= c0;
+            o[kk][1] *= c1;
+            o[kk][2] *= c0;
+            o[kk][3] *= c1;
           }
           m0 = mn0;
           m1 = mn1;
         }
-        // every slice has a valid token in row 0 of the warp's first page, so
+        // every slice has a valid token in row 0 of the CTA's first page, so
         // m is finite from the first slice on and masked logits give p = 0
         const float p00 = fast_exp2(s00 - m0), p01 = fast_exp2(s01 - m1);
         const float p10 = fast_exp2(s10 - m0), p11 = fast_exp2(s11 - m1);
         l0 += p00 + p10;
         l1 += p01 + p11;
-        const int vrow = r0 + (lane & 7) + ((lane >> 4) & 1) * 8;
         if constexpr (!FP8) {
           // ---- P = P_hi + P_lo in bf16, transposed into the B operand
           const uint32_t hi_t = pack_bf16(p00, p01), hi_b = pack_bf16(p10, p11);
@@ -257,14 +302,16 @@ __global__ void __launch_bounds__(TcGeom<D, BS, FP8, NW, NST>::kThreads)
           const uint32_t lo_b = pack_bf16(p10 - __low2float(hb), p11 - __high2float(hb));
           const uint32_t bh0 = movm_t(hi_t), bh1 = movm_t(hi_b);
           const uint32_t bl0 = movm_t(lo_t), bl1 = movm_t(lo_b);
-          // ---- O^T += V_slice^T . P^T, V^T fragments by ldmatrix.trans
+          // ---- O^T += V_slice^T . P^T over this warp's columns, V^T
+          // fragments by ldmatrix.trans
+          const int vrow = r0 + (lane & 7) + ((lane >> 4) & 1) * 8;
           const int vcol = ((lane >> 3) & 1) * 16;  // bytes
 #pragma unroll
-          for (int k = 0; k < KT; ++k) {
+          for (int kk = 0; kk < KW; ++kk) {
             uint32_t a0, a1, a2, a3;
-            ldsm_x4_t(swz_bytes<BS>(vp, vrow, k * 32 + vcol), a0, a1, a2, a3);
-            mma_bf16(o[k], a0, a1, a2, a3, bh0, bh1);
-            mma_bf16(o[k], a0, a1, a2, a3, bl0, bl1);
+            ldsm_x4_t(swz_bytes<BS>(vp, vrow, (kw0 + kk) * 32 + vcol), a0, a1, a2, a3);
+            mma_bf16(o[kk], a0, a1, a2, a3, bh0, bh1);
+            mma_bf16(o[kk], a0, a1, a2, a3, bl0, bl1);
           }
         } else {
           // ---- P in f16 (11-bit mantissa), transposed into the B operand
@@ -277,15 +324,14 @@ __global__ void __launch_bounds__(TcGeom<D, BS, FP8, NW, NST>::kThreads)
           const int vrow2 = r0 + (lane & 7) + ((lane >> 3) & 1) * 8;
           const int vcol = (lane >> 4) * 16;
 #pragma unroll
-          for (int k = 0; k < KT; k += 2) {
+          for (int kk = 0; kk < KW; kk += 2) {
             uint32_t m0r, m1r, m2r, m3r;
-            ldsm_x4(swz_bytes<BS>(vp, vrow2, k * 16 + vcol), m0r, m1r, m2r, m3r);
-            mma_f16(o[k], movm_t(e4m3x2_f16x2(m0r, 0)), movm_t(e4m3x2_f16x2(m0r, 1)),
+            ldsm_x4(swz_bytes<BS>(vp, vrow2, (kw0 + kk) * 16 + vcol), m0r, m1r, m2r, m3r);
+            mma_f16(o[kk], movm_t(e4m3x2_f16x2(m0r, 0)), movm_t(e4m3x2_f16x2(m0r, 1)),
                     movm_t(e4m3x2_f16x2(m1r, 0)), movm_t(e4m3x2_f16x2(m1r, 1)), b0, b1);
-            mma_f16(o[k + 1], movm_t(e4m3x2_f16x2(m2r, 0)), movm_t(e4m3x2_f16x2(m2r, 1)),
+            mma_f16(o[kk + 1], movm_t(e4m3x2_f16x2(m2r, 0)), movm_t(e4m3x2_f16x2(m2r, 1)),
                     movm_t(e4m3x2_f16x2(m3r, 0)), movm_t(e4m3x2_f16x2(m3r, 1)), b0, b1);
           }
-          (void)vrow;
         }
       }
       if (ntok < BS) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -309,58 +355,33 @@ __global__ void __launch_bounds__(TcGeom<D, BS, FP8, NW, NST>::kThreads)
   }
   __syncthreads();
 
-  // ---------------- merge the warp states in a fixed order
-  float* mo = ring_f;                   // [NW][8][D]
-  float* mm = mo + NW * 8 * D;          // [NW][8]
-  float* ml = mm + NW * 8;              // [NW][8]
-  if (warp < NW) {
-    const int q0 = (lane & 3) * 2;
-    // head-dim offsets of the two accumulator rows this lane holds
-    const int r_lo = FP8 ? fp8_row_offset(lane >> 2) : (lane >> 2);
-    const int r_hi = FP8 ? fp8_row_offset((lane >> 2) + 8) : (lane >> 2) + 8;
-#pragma unroll
-    for (int k = 0; k < KT; ++k) {
-      mo[(warp * 8 + q0) * D + k * 16 + r_lo] = o[k][0];
-      mo[(warp * 8 + q0 + 1) * D + k * 16 + r_lo] = o[k][1];
-      mo[(warp * 8 + q0) * D + k * 16 + r_hi] = o[k][2];
-      mo[(warp * 8 + q0 + 1) * D + k * 16 + r_hi] = o[k][3];
-    }
-    if (lane < 4) {
-      mm[warp * 8 + q0] = m0;
-      mm[warp * 8 + q0 + 1] = m1;
-      ml[warp * 8 + q0] = l0;
-      ml[warp * 8 + q0 + 1] = l1;
-    }
-  }
-  __syncthreads();
   const float vsc = FP8 ? p.v_scale[h] : 1.f;
+  const int q0 = (lane & 3) * 2;
+  // head-dim offsets of the two accumulator rows this lane holds in a tile
+  const int r_lo = FP8 ? fp8_row_offset(lane >> 2) : (lane >> 2);
+  const int r_hi = FP8 ? fp8_row_offset((lane >> 2) + 8) : (lane >> 2) + 8;
   if (p.cluster > 1) {
     // ---- CTA state (max, sum, unnormalised output per query), then the
     // cluster merges: rank r combines the head-dim slice [r*D/C, (r+1)*D/C)
     // of every rank's state, read through distributed shared memory, in rank
     // order.
-    float* cs_o = mm + 2 * NW * 8;  // [8][D]
+    float* cs_o = ring_f;           // [8][D]
     float* cs_m = cs_o + 8 * D;     // [8]
     float* cs_l = cs_m + 8;         // [8]
-    for (int idx = threadIdx.x; idx < g * D; idx += G::kThreads) {
-      const int j = idx / D;
-      const int c = idx % D;
-      float M = -INFINITY;
+    if (warp < NW) {
 #pragma unroll
-      for (int w = 0; w < NW; ++w) M = fmaxf(M, mm[w * 8 + j]);
-      float L = 0.f, O = 0.f;
-      if (M != -INFINITY) {
-#pragma unroll
-        for (int w = 0; w < NW; ++w) {
-          const float a = fast_exp2(mm[w * 8 + j] - M);
-          L = fmaf(ml[w * 8 + j], a, L);
-          O = fmaf(mo[(w * 8 + j) * D + c], a, O);
-        }
+      for (int kk = 0; kk < KW; ++kk) {
+        const int c0 = (kw0 + kk) * 16;
+        cs_o[q0 * D + c0 + r_lo] = o[kk][0];
+        cs_o[(q0 + 1) * D + c0 + r_lo] = o[kk][1];
+        cs_o[q0 * D + c0 + r_hi] = o[kk][2];
+        cs_o[(q0 + 1) * D + c0 + r_hi] = o[kk][3];
       }
-      cs_o[j * D + c] = O;
-      if (c == 0) {
-        cs_m[j] = M;
-        cs_l[j] = L;
+      if (warp == 0 && lane < 4) {
+        cs_m[q0] = m0;
+        cs_m[q0 + 1] = m1;
+        cs_l[q0] = l0;
+        cs_l[q0 + 1] = l1;
       }
     }
     cluster_sync_all();
@@ -387,32 +408,34 @@ __global__ void __launch_bounds__(TcGeom<D, BS, FP8, NW, NST>::kThreads)
     cluster_sync_all();  // keep this CTA's state alive until every rank has read it
     return;
   }
-  for (int idx = threadIdx.x; idx < g * D; idx += G::kThreads) {
-    const int j = idx / D;
-    const int c = idx % D;
-    float M = -INFINITY;
+  if (warp >= NW) return;
+  // ---- this warp's columns of the result: one pass -> out (bf16), split ->
+  // the partition's partial (normalised output, max, sum)
 #pragma unroll
-    for (int w = 0; w < NW; ++w) M = fmaxf(M, mm[w * 8 + j]);
-    float L = 0.f, O = 0.f;
-    if (M != -INFINITY) {
+  for (int e = 0; e < 2; ++e) {
+    const int j = q0 + e;
+    if (j >= g) continue;
+    const float L = e ? l1 : l0;
+    const float M = e ? m1 : m0;
+    const int64_t hq = static_cast<int64_t>(s) * p.num_heads + h * g + j;
 #pragma unroll
-      for (int w = 0; w < NW; ++w) {
-        const float a = fast_exp2(mm[w * 8 + j] - M);
-        L = fmaf(ml[w * 8 + j], a, L);
-        O = fmaf(mo[(w * 8 + j) * D + c], a, O);
+    for (int kk = 0; kk < KW; ++kk) {
+      const int c0 = (kw0 + kk) * 16;
+      const float lo = L > 0.f ? (o[kk][e] / L) * vsc : 0.f;
+      const float hi = L > 0.f ? (o[kk][2 + e] / L) * vsc : 0.f;
+      if (p.partition_blocks == 0) {
+        p.out[hq * D + c0 + r_lo] = float_to_bf16_bits(lo);
+        p.out[hq * D + c0 + r_hi] = float_to_bf16_bits(hi);
+      } else {
+        float* dst = p.tmp_out + (hq * p.np_max + p.slot_offset + part) * D;
+        dst[c0 + r_lo] = lo;
+        dst[c0 + r_hi] = hi;
       }
     }
-    const float res = L > 0.f ? (O / L) * vsc : 0.f;
-    const int64_t hq = static_cast<int64_t>(s) * p.num_heads + h * g + j;
-    if (p.partition_blocks == 0) {
-      p.out[hq * D + c] = float_to_bf16_bits(res);
-    } else {
-      const int slot = p.slot_offset + part;
-      p.tmp_out[(hq * p.np_max + slot) * D + c] = res;
-      if (c == 0) {
-        p.max_logits[hq * p.np_max + slot] = M * kLn2Tc;
-        p.exp_sums[hq * p.np_max + slot] = L;
-      }
+    if (p.partition_blocks > 0 && warp == 0 && (lane >> 2) == 0) {
+      const int64_t idx = hq * p.np_max + p.slot_offset + part;
+      p.max_logits[idx] = M * kLn2Tc;
+      p.exp_sums[idx] = L;
     }
   }
 }
@@ -574,10 +597,10 @@ template <bool FP8>
 static int dispatch_tc(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
                        int head_dim, int block_size, dim3 grid, cudaStream_t st) {
   // (consumer warps, ring stages): about 64-128 KB of stages per CTA
-  if (head_dim == 256 && block_size == 16) return launch_tc<256, 16, FP8, 2, 4>(p, tk, tv, grid, st);
-  if (head_dim == 256 && block_size == 32) return launch_tc<256, 32, FP8, 2, FP8 ? 4 : 2>(p, tk, tv, grid, st);
+  if (head_dim == 256 && block_size == 16) return launch_tc<256, 16, FP8, 2, 2>(p, tk, tv, grid, st);
+  if (head_dim == 256 && block_size == 32) return launch_tc<256, 32, FP8, FP8 ? 4 : 2, 2>(p, tk, tv, grid, st);
   if (head_dim == 128 && block_size == 16) return launch_tc<128, 16, FP8, 4, 8>(p, tk, tv, grid, st);
-  return launch_tc<128, 32, FP8, 2, 4>(p, tk, tv, grid, st);
+  return launch_tc<128, 32, FP8, 4, 4>(p, tk, tv, grid, st);
 }
 
 int launch_decode_tc(const DecodeParams& p, const void* k_cache, const void* v_cache,
