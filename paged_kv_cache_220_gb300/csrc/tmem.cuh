@@ -1,8 +1,8 @@
 // tcgen05 (5th-generation tensor core) helpers: shared-memory operand
-// descriptors, instruction descriptors, MMA issue and commit, tensor memory
-// allocation and loads/stores. Used by the shared-prefix kernel, whose
-// query-group product (up to 128 query rows) is the one contraction on the
-// decode path large enough for the 128-row MMA.
+// descriptors, instruction descriptors, MMA issue (A from tensor memory) and
+// commit, tensor memory allocation and loads/stores. Used by the shared-prefix
+// kernel, whose query-group product (up to 128 query rows) is the one
+// contraction on the decode path large enough for the 128-row MMA.
 #pragma once
 
 #include <cstdint>
@@ -29,16 +29,6 @@ __device__ __forceinline__ uint64_t umma_sdesc(uint32_t saddr, uint32_t lbo, uin
 __host__ __device__ constexpr uint32_t umma_idesc_bf16(int M, int N, bool b_mn_major) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
          (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
-}
-
-// D[tmem] (+)= A[smem] . B[smem]; issued by one thread.
-__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
-                                          uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
-      : "memory");
 }
 
 // D[tmem] (+)= A[tmem] . B[smem]; issued by one thread. A (M = 128 rows x K)
@@ -141,15 +131,8 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float* v) {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
-// 8 or 16 consecutive 32-bit columns of this thread's lane, stored without
+// 16 consecutive 32-bit columns of this thread's lane, stored without
 // waiting (call tmem_wait_st before the values are consumed elsewhere).
-__device__ __forceinline__ void tmem_st8_nowait(uint32_t taddr, const uint32_t* v) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr),
-      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
-      : "memory");
-}
-
 __device__ __forceinline__ void tmem_st16_nowait(uint32_t taddr, const uint32_t* v) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
