@@ -9,9 +9,10 @@
 // the weight sum are xor-shuffle trees, and every lane accumulates its 16-byte
 // column slices over the partitions in order, with the loads of four
 // partitions in flight. Rows with more partitions (long contexts) take one
-// 16-warp CTA each: the weights go once into shared memory (block-wide max
-// and sum in a fixed tree order), warp w accumulates the partitions
-// p = w, w + 16, ... and the warp sums are added in warp order. Normalising
+// 16-warp CTA per 128 columns: the weights go into shared memory (block-wide
+// max and sum in a fixed tree order), warp w accumulates the partitions
+// p = w, w + 16, ... (eight partitions' loads in flight per lane) and the warp
+// sums are added in warp order. Normalising
 // the weights before the products makes a single partition reproduce its
 // output exactly. The work is HBM-bound: (d + 2) * 4 bytes per partition
 // read, d * 2 bytes written.
@@ -51,10 +52,11 @@ __global__ void __launch_bounds__(kReduceWarps * 32) reduce_kernel(
     const int32_t* __restrict__ prefix_blocks, int block_size, int slot_split,
     int prefix_partition, int* err) {
   constexpr int kReduceThreads = kReduceWarps * 32;
-  constexpr int V4 = D / 128;  // float4 per lane per partition row
+  // this CTA's 128 columns (blockIdx.z selects them): one float4 per lane
+  const int c4 = blockIdx.z * 32;  // first float4 column
   extern __shared__ float wsh[];  // [np_max] normalised weights
   __shared__ float red[kReduceWarps];
-  __shared__ float4 acc_sh[kReduceWarps][D / 4];
+  __shared__ float4 acc_sh[kReduceWarps][32];
   const int j = blockIdx.x;
   const int s = blockIdx.y;
   const int tid = threadIdx.x;
@@ -65,7 +67,7 @@ __global__ void __launch_bounds__(kReduceWarps * 32) reduce_kernel(
   const int np = npre + nsuf;
   const int64_t row = static_cast<int64_t>(s) * num_heads + j;
   if (np == 0) {
-    if (tid < D / 4) reinterpret_cast<uint2*>(out + row * D)[tid] = make_uint2(0u, 0u);
+    if (tid < 32) reinterpret_cast<uint2*>(out + row * D)[c4 + tid] = make_uint2(0u, 0u);
     return;
   }
   const float* ml = max_logits + row * np_max;
@@ -100,48 +102,37 @@ __global__ void __launch_bounds__(kReduceWarps * 32) reduce_kernel(
   for (int i = tid; i < np; i += kReduceThreads) wsh[i] = wsh[i] / W;
   __syncthreads();
 
-  // sum_p r_p o_p: warp w takes p = w, w + 16, ...; lane owns float4 columns
-  // lane + 32 v (v < V4)
-  const float4* src = reinterpret_cast<const float4*>(tmp_out + row * np_max * D);
-  float4 acc[V4];
-#pragma unroll
-  for (int v = 0; v < V4; ++v) acc[v] = make_float4(0.f, 0.f, 0.f, 0.f);
-  constexpr int U = 4;
+  // sum_p r_p o_p: warp w takes p = w, w + 16, ...; lane owns float4 column
+  // c4 + lane
+  const float4* src = reinterpret_cast<const float4*>(tmp_out + row * np_max * D) + c4 + lane;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  constexpr int U = 8;
   int i = warp;
   for (; i + (U - 1) * kReduceWarps < np; i += U * kReduceWarps) {
-    float4 x[U][V4];
+    float4 x[U];
 #pragma unroll
     for (int u = 0; u < U; ++u)
-#pragma unroll
-      for (int v = 0; v < V4; ++v)
-        x[u][v] = src[static_cast<int64_t>(slot_of(i + u * kReduceWarps)) * (D / 4) + lane + 32 * v];
+      x[u] = src[static_cast<int64_t>(slot_of(i + u * kReduceWarps)) * (D / 4)];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const float r = wsh[i + u * kReduceWarps];
-#pragma unroll
-      for (int v = 0; v < V4; ++v) {
-        acc[v].x = fmaf(r, x[u][v].x, acc[v].x);
-        acc[v].y = fmaf(r, x[u][v].y, acc[v].y);
-        acc[v].z = fmaf(r, x[u][v].z, acc[v].z);
-        acc[v].w = fmaf(r, x[u][v].w, acc[v].w);
-      }
+      acc.x = fmaf(r, x[u].x, acc.x);
+      acc.y = fmaf(r, x[u].y, acc.y);
+      acc.z = fmaf(r, x[u].z, acc.z);
+      acc.w = fmaf(r, x[u].w, acc.w);
     }
   }
   for (; i < np; i += kReduceWarps) {
     const float r = wsh[i];
-#pragma unroll
-    for (int v = 0; v < V4; ++v) {
-      const float4 x = src[static_cast<int64_t>(slot_of(i)) * (D / 4) + lane + 32 * v];
-      acc[v].x = fmaf(r, x.x, acc[v].x);
-      acc[v].y = fmaf(r, x.y, acc[v].y);
-      acc[v].z = fmaf(r, x.z, acc[v].z);
-      acc[v].w = fmaf(r, x.w, acc[v].w);
-    }
+    const float4 x = src[static_cast<int64_t>(slot_of(i)) * (D / 4)];
+    acc.x = fmaf(r, x.x, acc.x);
+    acc.y = fmaf(r, x.y, acc.y);
+    acc.z = fmaf(r, x.z, acc.z);
+    acc.w = fmaf(r, x.w, acc.w);
   }
-#pragma unroll
-  for (int v = 0; v < V4; ++v) acc_sh[warp][lane + 32 * v] = acc[v];
+  acc_sh[warp][lane] = acc;
   __syncthreads();
-  if (tid < D / 4) {
+  if (tid < 32) {
     float4 a = acc_sh[0][tid];
 #pragma unroll
     for (int w = 1; w < kReduceWarps; ++w) {
@@ -155,7 +146,7 @@ __global__ void __launch_bounds__(kReduceWarps * 32) reduce_kernel(
                         (static_cast<uint32_t>(float_to_bf16_bits(a.y)) << 16);
     const uint32_t hi = float_to_bf16_bits(a.z) |
                         (static_cast<uint32_t>(float_to_bf16_bits(a.w)) << 16);
-    reinterpret_cast<uint2*>(out + row * D)[tid] = make_uint2(lo, hi);
+    reinterpret_cast<uint2*>(out + row * D)[c4 + tid] = make_uint2(lo, hi);
   }
 }
 
@@ -257,11 +248,11 @@ int launch_reduce(void* out, const float* tmp, const float* ml, const float* es,
           block_size, slot_split, pp, err);
     return launch_status();
   }
-  // one 16-warp CTA per row
+  // one 16-warp CTA per row and 128 columns
   const size_t smem = static_cast<size_t>(np_max) * sizeof(float);
   constexpr size_t kMaxSmem = 160 * 1024;  // plus the static accumulators
   if (smem > kMaxSmem) return PKV_ERR_UNSUPPORTED;
-  const dim3 grid(num_heads, num_seqs);
+  const dim3 grid(num_heads, num_seqs, head_dim / 128);
   if (head_dim == 128) {
     static bool done[64] = {false};
     int rc = ensure_smem(reduce_kernel<128, 16>, kMaxSmem, done, 64);
