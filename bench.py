@@ -88,10 +88,36 @@ def peaks():
     return 6800.0, "fallback"
 
 
+def strip_comments(src: str) -> str:
+    """C/C++ source without comments and blank space, so that comment-only
+    edits leave the hash of the code alone (string and character literals
+    are kept as they are)."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def source_hash(paths) -> str:
+    """Hash of the code (comments and spacing ignored) of the given sources."""
     h = hashlib.sha256()
     for rel in paths:
-        h.update(open(os.path.join(ROOT, rel), "rb").read())
+        h.update(strip_comments(open(os.path.join(ROOT, rel), encoding="utf-8").read()).encode())
     return h.hexdigest()[:16]
 
 
