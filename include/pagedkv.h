@@ -370,6 +370,17 @@ int pkv_block_refcount(const pkv_allocator* a, int block, int* refcount);
  * counted once per physical slot (shared slots count once). */
 int pkv_alloc_stats(const pkv_allocator* a, int* free_blocks, int* used_blocks,
                     long long* used_slots);
+/* Checkpoint / resume of the allocator (the pages have no counterpart; with
+ * pkv_swap_out of the used blocks it saves a whole cache state, e.g. before
+ * moving a batch off the GPU). pkv_alloc_save writes the complete state (free
+ * list order, refcounts, fill, every sequence's table and length, next id)
+ * as a flat record of *n bytes into buf (host memory, cap bytes); with buf
+ * NULL it only reports *n. pkv_alloc_load creates an allocator from such a
+ * record; it checks the record against itself (sizes, ranges, each block
+ * free exactly once or held by exactly refcount tables) and returns
+ * PKV_ERR_INVALID_ARG, creating nothing, on any mismatch. */
+int pkv_alloc_save(const pkv_allocator* a, void* buf, size_t cap, size_t* n);
+int pkv_alloc_load(const void* buf, size_t n, pkv_allocator** out);
 
 /* ------------------------------------------------------------------------ *
  * Iteration-level (continuous) batching scheduler over an allocator

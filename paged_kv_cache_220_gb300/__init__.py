@@ -92,6 +92,8 @@ SIGNATURES = {
     "pkv_block_refcount": (_I, [_P, _I, ctypes.POINTER(_I)]),
     "pkv_alloc_stats": (_I, [_P, ctypes.POINTER(_I), ctypes.POINTER(_I),
                              ctypes.POINTER(ctypes.c_longlong)]),
+    "pkv_alloc_save": (_I, [_P, _P, ctypes.c_size_t, ctypes.POINTER(ctypes.c_size_t)]),
+    "pkv_alloc_load": (_I, [_P, ctypes.c_size_t, ctypes.POINTER(_P)]),
     "pkv_sched_create": (_I, [_P, _I, _I, ctypes.POINTER(_P)]),
     "pkv_sched_destroy": (None, [_P]),
     "pkv_sched_add_request": (_I, [_P, ctypes.c_int64, _I, _I]),
@@ -393,6 +395,27 @@ class BlockAllocator:
             self.close()
         except Exception:
             pass
+
+    def save(self) -> bytes:
+        """The allocator's complete state as a flat record (pkv_alloc_save)."""
+        n = ctypes.c_size_t()
+        _check(lib().pkv_alloc_save(self._h, None, 0, ctypes.byref(n)), "alloc_save")
+        buf = ctypes.create_string_buffer(n.value)
+        _check(lib().pkv_alloc_save(self._h, buf, n, ctypes.byref(n)), "alloc_save")
+        return buf.raw[:n.value]
+
+    @classmethod
+    def load(cls, record: bytes) -> "BlockAllocator":
+        """An allocator restored from a record of save() (pkv_alloc_load)."""
+        h = ctypes.c_void_p()
+        buf = ctypes.create_string_buffer(bytes(record), len(record))
+        _check(lib().pkv_alloc_load(buf, len(record), ctypes.byref(h)), "alloc_load")
+        self = cls.__new__(cls)
+        self._h = h
+        words = np.frombuffer(bytes(record), dtype="<i8")
+        self.num_blocks = int(words[2])
+        self.block_size = int(words[3])
+        return self
 
     def new_seq(self) -> int:
         sid = ctypes.c_int()

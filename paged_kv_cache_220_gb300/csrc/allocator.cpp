@@ -15,7 +15,9 @@
 //
 // Every call is transactional: it checks everything it needs (free blocks,
 // output room) before it changes any state.
+#include <algorithm>
 #include <cstdint>
+#include <cstring>
 #include <new>
 #include <random>
 #include <unordered_map>
@@ -206,5 +208,147 @@ extern "C" int pkv_alloc_stats(const pkv_allocator* a, int* free_blocks, int* us
       if (a->refcount[b] > 0) u += a->fill[b];
     *used_slots = u;
   }
+  return PKV_OK;
+}
+
+// ---------------------------------------------------------------- checkpoint
+//
+// The whole allocator state as a flat little-endian int64 record:
+//   magic, version, num_blocks, block_size, next_id,
+//   free list size, free list (bottom to top),
+//   refcount[num_blocks], fill[num_blocks],
+//   number of sequences, then per sequence (ascending id):
+//   id, length, table size, table.
+// Loading checks the record against itself (sizes, ranges, every block either
+// free with refcount 0 or held by exactly refcount tables, fill within the
+// block) and returns PKV_ERR_INVALID_ARG otherwise, building nothing.
+
+namespace {
+
+constexpr int64_t kMagic = 0x31414b5650LL;  // "PVKA1"
+
+void put(std::vector<int64_t>& v, int64_t x) { v.push_back(x); }
+
+}  // namespace
+
+extern "C" int pkv_alloc_save(const pkv_allocator* a, void* buf, size_t cap, size_t* n) {
+  if (!a || !n) return PKV_ERR_INVALID_ARG;
+  std::vector<int64_t> r;
+  try {
+    put(r, kMagic);
+    put(r, 1);
+    put(r, a->num_blocks);
+    put(r, a->block_size);
+    put(r, a->next_id);
+    put(r, static_cast<int64_t>(a->free_list.size()));
+    for (int32_t b : a->free_list) put(r, b);
+    for (int32_t c : a->refcount) put(r, c);
+    for (int32_t f : a->fill) put(r, f);
+    std::vector<int> ids;
+    ids.reserve(a->seqs.size());
+    for (const auto& kv : a->seqs) ids.push_back(kv.first);
+    std::sort(ids.begin(), ids.end());
+    put(r, static_cast<int64_t>(ids.size()));
+    for (int id : ids) {
+      const pkv_allocator::Seq& q = a->seqs.at(id);
+      put(r, id);
+      put(r, q.len);
+      put(r, static_cast<int64_t>(q.table.size()));
+      for (int32_t b : q.table) put(r, b);
+    }
+  } catch (...) {
+    return PKV_ERR_OUT_OF_BLOCKS;
+  }
+  *n = r.size() * sizeof(int64_t);
+  if (!buf) return PKV_OK;  // size query
+  if (cap < *n) return PKV_ERR_INVALID_ARG;
+  std::memcpy(buf, r.data(), *n);
+  return PKV_OK;
+}
+
+extern "C" int pkv_alloc_load(const void* buf, size_t n, pkv_allocator** out) {
+  if (!buf || !out || n % sizeof(int64_t) != 0) return PKV_ERR_INVALID_ARG;
+  *out = nullptr;
+  const size_t words = n / sizeof(int64_t);
+  std::vector<int64_t> r(words);
+  std::memcpy(r.data(), buf, n);
+  size_t i = 0;
+  auto get = [&](int64_t* x) -> bool {
+    if (i >= words) return false;
+    *x = r[i++];
+    return true;
+  };
+  int64_t magic, version, nb, bs, next_id, nfree;
+  if (!get(&magic) || !get(&version) || !get(&nb) || !get(&bs) || !get(&next_id) ||
+      !get(&nfree))
+    return PKV_ERR_INVALID_ARG;
+  if (magic != kMagic || version != 1 || nb <= 0 || nb > INT32_MAX || bs <= 0 || bs > INT32_MAX ||
+      next_id < 0 || next_id > INT32_MAX || nfree < 0 || nfree > nb)
+    return PKV_ERR_INVALID_ARG;
+  pkv_allocator* a = new (std::nothrow) pkv_allocator();
+  if (!a) return PKV_ERR_OUT_OF_BLOCKS;
+  auto fail = [&](int rc) {
+    delete a;
+    return rc;
+  };
+  try {
+    a->num_blocks = static_cast<int>(nb);
+    a->block_size = static_cast<int>(bs);
+    a->next_id = static_cast<int>(next_id);
+    a->free_list.resize(nfree);
+    a->refcount.resize(nb);
+    a->fill.resize(nb);
+    for (int64_t k = 0; k < nfree; ++k) {
+      int64_t b;
+      if (!get(&b) || b < 0 || b >= nb) return fail(PKV_ERR_INVALID_ARG);
+      a->free_list[k] = static_cast<int32_t>(b);
+    }
+    for (int64_t k = 0; k < nb; ++k) {
+      int64_t c;
+      if (!get(&c) || c < 0 || c > INT32_MAX) return fail(PKV_ERR_INVALID_ARG);
+      a->refcount[k] = static_cast<int32_t>(c);
+    }
+    for (int64_t k = 0; k < nb; ++k) {
+      int64_t f;
+      if (!get(&f) || f < 0 || f > bs) return fail(PKV_ERR_INVALID_ARG);
+      a->fill[k] = static_cast<int32_t>(f);
+    }
+    int64_t nseq;
+    if (!get(&nseq) || nseq < 0) return fail(PKV_ERR_INVALID_ARG);
+    std::vector<int64_t> held(nb, 0);
+    for (int64_t k = 0; k < nseq; ++k) {
+      int64_t id, len, nt;
+      if (!get(&id) || !get(&len) || !get(&nt)) return fail(PKV_ERR_INVALID_ARG);
+      if (id < 0 || id >= next_id || a->seqs.count(static_cast<int>(id)) || len < 0 || nt < 0 ||
+          nt > nb || nt != (len + bs - 1) / bs)
+        return fail(PKV_ERR_INVALID_ARG);
+      pkv_allocator::Seq q;
+      q.len = len;
+      q.table.resize(nt);
+      for (int64_t t = 0; t < nt; ++t) {
+        int64_t b;
+        if (!get(&b) || b < 0 || b >= nb) return fail(PKV_ERR_INVALID_ARG);
+        q.table[t] = static_cast<int32_t>(b);
+        ++held[b];
+      }
+      a->seqs.emplace(static_cast<int>(id), std::move(q));
+    }
+    if (i != words) return fail(PKV_ERR_INVALID_ARG);
+    // every block: free (refcount 0, on the free list once) or held by
+    // exactly refcount tables
+    std::vector<char> on_free(nb, 0);
+    for (int32_t b : a->free_list) {
+      if (on_free[b] || a->refcount[b] != 0) return fail(PKV_ERR_INVALID_ARG);
+      on_free[b] = 1;
+    }
+    for (int64_t b = 0; b < nb; ++b) {
+      if (!on_free[b] && (a->refcount[b] == 0 || held[b] != a->refcount[b]))
+        return fail(PKV_ERR_INVALID_ARG);
+      if (on_free[b] && held[b] != 0) return fail(PKV_ERR_INVALID_ARG);
+    }
+  } catch (...) {
+    return fail(PKV_ERR_OUT_OF_BLOCKS);
+  }
+  *out = a;
   return PKV_OK;
 }

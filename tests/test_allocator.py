@@ -209,3 +209,83 @@ def test_mixed_lengths_internal_fragmentation():
     frag = 1 - st["used_slots"] / (st["used_blocks"] * w.block_size)
     assert st["used_slots"] == sum(w.ctx)
     assert frag < 0.04
+
+
+def _churn(a, rng, seqs, steps):
+    """Random appends, forks and frees; returns the live sequences."""
+    for _ in range(steps):
+        op = rng.integers(0, 10)
+        try:
+            if op < 5 and seqs:
+                a.append(seqs[int(rng.integers(0, len(seqs)))], int(rng.integers(1, 40)))
+            elif op < 7 and seqs:
+                seqs.append(a.fork(seqs[int(rng.integers(0, len(seqs)))]))
+            elif op < 8 and seqs:
+                a.free(seqs.pop(int(rng.integers(0, len(seqs)))))
+            else:
+                seqs.append(a.new_seq())
+        except pkv.PagedKVError:
+            pass                                 # pool exhausted: state unchanged
+    return seqs
+
+
+def test_checkpoint_round_trip_continues_identically():
+    """A restored allocator holds the same tables, lengths, refcounts and
+    free-list order: the same operations afterwards give the same slots and
+    copy-on-write pairs on both."""
+    rng = np.random.default_rng(21)
+    a = pkv.BlockAllocator(96, 16, seed=9)
+    seqs = _churn(a, rng, [], 300)
+    rec = a.save()
+    b = pkv.BlockAllocator.load(rec)
+    assert b.save() == rec
+    assert b.stats() == a.stats()
+    for s in seqs:
+        assert np.array_equal(a.block_table(s), b.block_table(s))
+        assert a.seq_len(s) == b.seq_len(s)
+    for blk in range(a.num_blocks):
+        assert a.refcount(blk) == b.refcount(blk)
+    _check_invariants(b, seqs)
+    # identical futures
+    def try_append(x, s, n):
+        try:
+            slots, pairs = x.append(s, n)
+            return slots.tolist(), pairs.tolist()
+        except pkv.PagedKVError as e:
+            return str(e)
+
+    for step in range(200):
+        if not seqs:
+            break
+        s = seqs[step % len(seqs)]
+        assert try_append(a, s, 1 + step % 7) == try_append(b, s, 1 + step % 7)
+        if step % 50 == 49:
+            a.free(seqs[0])
+            b.free(seqs[0])
+            seqs.pop(0)
+    assert a.save() == b.save()
+
+
+def test_checkpoint_rejects_inconsistent_records():
+    a = pkv.BlockAllocator(32, 16, seed=2)
+    s = a.new_seq()
+    a.append(s, 40)
+    a.fork(s)
+    rec = np.frombuffer(a.save(), dtype="<i8").copy()
+
+    def load(words):
+        return pkv.BlockAllocator.load(words.astype("<i8").tobytes())
+
+    load(rec)                                    # the record itself is fine
+    bad = []
+    r = rec.copy(); r[0] ^= 1; bad.append(r)                      # magic
+    r = rec.copy(); r[2] = 0; bad.append(r)                       # num_blocks
+    nfree = int(rec[5])
+    r = rec.copy(); r[6] = rec[7]; bad.append(r)                  # a block free twice
+    r = rec.copy(); r[6 + nfree + int(rec[6 + nfree - 1] if nfree else 0)] += 1; bad.append(r)
+    r = rec.copy(); r[6 + nfree] += 1; bad.append(r)              # refcount of a block
+    bad.append(rec[:-1])                                          # truncated
+    bad.append(np.concatenate([rec, [0]]))                        # trailing data
+    for r in bad:
+        with pytest.raises(pkv.PagedKVError):
+            load(r)
