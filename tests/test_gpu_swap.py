@@ -64,3 +64,39 @@ def workload_step(pw):
     workload.step(pw, out, None, 0)
     torch.cuda.synchronize()
     return out[0].clone()
+
+
+def test_whole_cache_checkpoint_and_resume():
+    """Checkpoint of a whole cache state: the allocator record plus every used
+    block (shared blocks once) swapped to pinned host memory; the pools are
+    wiped and the allocator dropped; a loaded allocator and a swap-in into the
+    same block ids give the same decode output bit for bit."""
+    pkv_build.build()
+    flag = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pkv.set_device_check(flag)
+    w = synth.cow(prompt_len=40, prompts=2, rollouts=4)
+    pw = workload.build(w)
+    st = pw.layers[0]
+    out0 = workload_step(pw)
+    record = pw.alloc.save()
+    used = sorted({int(b) for s in pw.seqs for b in pw.alloc.block_table(s)})
+    blocks = torch.as_tensor(used, dtype=torch.int32).pin_memory()
+    kb = torch.empty((len(used),) + tuple(st.k_cache.shape[1:]), dtype=st.k_cache.dtype).pin_memory()
+    vb = torch.empty_like(kb).pin_memory()
+    pkv.swap_out(st.k_cache, st.v_cache, blocks, kb, vb)
+    torch.cuda.synchronize()
+    st.k_cache.zero_()
+    st.v_cache.zero_()
+    pw.alloc.close()
+    alloc = pkv.BlockAllocator.load(record)
+    tables = alloc.block_tables(pw.seqs, pw.block_tables.shape[1])
+    assert np.array_equal(tables, pw.block_tables.cpu().numpy())
+    pkv.swap_in(st.k_cache, st.v_cache, blocks, kb, vb)
+    out1 = torch.empty_like(st.q)
+    pkv.paged_attention_decode(out1, st.q, st.k_cache, st.v_cache,
+                               torch.as_tensor(tables, device="cuda"), pw.context_lens, w.scale,
+                               pw.max_context, 0, None, st.k_scale, st.v_scale)
+    torch.cuda.synchronize()
+    assert torch.equal(out1.view(torch.int16), out0.view(torch.int16))
+    assert int(flag.item()) == 0
+    pkv.set_device_check(None)
