@@ -100,6 +100,11 @@ __global__ void __launch_bounds__(TcGeom<D, BS, FP8, NW, NST>::kThreads)
   // overlapped with the kernel before it: thread 0 of CTA (0, 0, 0), which
   // every launch has, keeps the grid alive until that kernel has completed
   PrerequisiteTail tail{p.overlap_prev != 0 && threadIdx.x == 0 && part == 0 && h == 0 && s == 0};
+  // launched as a programmatic dependent of the kernel before it (e.g. the
+  // cache write): nothing below reads global memory before that kernel has
+  // completed, except in the overlapped shared-prefix form, whose inputs the
+  // earlier kernel does not write
+  if (p.overlap_prev == 0) wait_prerequisite();
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int g = p.group;
@@ -354,6 +359,9 @@ __global__ void __launch_bounds__(TcGeom<D, BS, FP8, NW, NST>::kThreads)
       if (!mbar_wait(&full[it % NST], (it / NST) & 1, p.err)) break;
   }
   __syncthreads();
+  // the merge launched next may be scheduled once every CTA got here; it
+  // waits for this grid's completion before reading the partials
+  allow_dependents();
 
   const float vsc = FP8 ? p.v_scale[h] : 1.f;
   const int q0 = (lane & 3) * 2;
@@ -525,23 +533,10 @@ static int launch_tc(const DecodeParams& p_in, const CUtensorMap& tk, const CUte
   if (rc != PKV_OK) return rc;
   DecodeParams p = p_in;
   if (p.partition_blocks > 0 || p.cluster <= 1) {
+    // programmatic dependent launch: the CTAs may be scheduled while the
+    // kernel before them finishes (see wait_prerequisite in the kernel)
     p.cluster = 1;
-    if (p.overlap_prev) {
-      cudaLaunchConfig_t cfg = {};
-      cudaLaunchAttribute attr[1];
-      cfg.gridDim = grid;
-      cfg.blockDim = dim3(G::kThreads);
-      cfg.dynamicSmemBytes = G::kSmem;
-      cfg.stream = st;
-      attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-      attr[0].val.programmaticStreamSerializationAllowed = 1;
-      cfg.attrs = attr;
-      cfg.numAttrs = 1;
-      if (cudaLaunchKernelEx(&cfg, kern, tk, tv, p) != cudaSuccess) return PKV_ERR_CUDA;
-      return launch_status();
-    }
-    kern<<<grid, G::kThreads, G::kSmem, st>>>(tk, tv, p);
-    return launch_status();
+    return launch_dependent(kern, grid, dim3(G::kThreads), G::kSmem, st, tk, tv, p);
   }
   p.overlap_prev = 0;
   // One pass: a cluster of C CTAs per (KV head, sequence), C a power of two

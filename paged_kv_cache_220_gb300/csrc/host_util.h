@@ -4,6 +4,7 @@
 #include <cstddef>
 #include <cstdint>
 #include <cuda_runtime.h>
+#include <utility>
 
 #include "../../include/pagedkv.h"
 
@@ -30,6 +31,27 @@ inline int check_cache_desc(const pkv_cache_desc& c) {
 inline int launch_status() {
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+// Launch as a programmatic dependent of the kernel before it on the stream:
+// the CTAs may be scheduled before that kernel completes, and the kernel must
+// call wait_prerequisite() before reading anything that kernel wrote.
+template <typename... Params, typename... Args>
+inline int launch_dependent(void (*kern)(Params...), dim3 grid, dim3 block, size_t smem,
+                            cudaStream_t st, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...) != cudaSuccess)
+    return PKV_ERR_CUDA;
+  return launch_status();
 }
 
 // Raise a kernel's dynamic shared-memory limit once per device.

@@ -22,6 +22,9 @@ __global__ void __launch_bounds__(1024) kv_cache_write_kernel(
     uint8_t* __restrict__ v_cache, int num_blocks, int block_size, int num_kv_heads,
     int head_dim, const float* __restrict__ k_scale, const float* __restrict__ v_scale,
     int* err) {
+  // the decode launched next may start its set-up now; it waits for this
+  // grid's completion before it reads the cache
+  allow_dependents();
   const int token = blockIdx.x;
   const int64_t slot = slot_mapping[token];
   if (slot < 0) return;

@@ -57,6 +57,7 @@ __global__ void __launch_bounds__(kReduceWarps * 32) reduce_kernel(
   extern __shared__ float wsh[];  // [np_max] normalised weights
   __shared__ float red[kReduceWarps];
   __shared__ float4 acc_sh[kReduceWarps][32];
+  wait_prerequisite();  // the partials come from the decode launched before
   const int j = blockIdx.x;
   const int s = blockIdx.y;
   const int tid = threadIdx.x;
@@ -160,6 +161,7 @@ __global__ void __launch_bounds__(kRowWarps * 32) reduce_rows_kernel(
     int partition_size, const int32_t* __restrict__ prefix_blocks, int block_size,
     int slot_split, int prefix_partition, int* err) {
   constexpr int V4 = D / 128;  // float4 per lane per partition row
+  wait_prerequisite();  // the partials come from the decode launched before
   const int lane = threadIdx.x & 31;
   const int64_t row = static_cast<int64_t>(blockIdx.x) * kRowWarps + (threadIdx.x >> 5);
   if (row >= num_rows) return;
@@ -239,14 +241,12 @@ int launch_reduce(void* out, const float* tmp, const float* ml, const float* es,
     const int rows = num_seqs * num_heads;
     const dim3 grid((rows + kRowWarps - 1) / kRowWarps);
     if (head_dim == 128)
-      reduce_rows_kernel<128><<<grid, kRowWarps * 32, 0, st>>>(
-          o, tmp, ml, es, context_lens, rows, num_heads, np_max, partition_size, prefix_blocks,
-          block_size, slot_split, pp, err);
-    else
-      reduce_rows_kernel<256><<<grid, kRowWarps * 32, 0, st>>>(
-          o, tmp, ml, es, context_lens, rows, num_heads, np_max, partition_size, prefix_blocks,
-          block_size, slot_split, pp, err);
-    return launch_status();
+      return launch_dependent(reduce_rows_kernel<128>, grid, dim3(kRowWarps * 32), 0, st, o, tmp,
+                              ml, es, context_lens, rows, num_heads, np_max, partition_size,
+                              prefix_blocks, block_size, slot_split, pp, err);
+    return launch_dependent(reduce_rows_kernel<256>, grid, dim3(kRowWarps * 32), 0, st, o, tmp, ml,
+                            es, context_lens, rows, num_heads, np_max, partition_size,
+                            prefix_blocks, block_size, slot_split, pp, err);
   }
   // one 16-warp CTA per row and 128 columns
   const size_t smem = static_cast<size_t>(np_max) * sizeof(float);
@@ -257,16 +257,16 @@ int launch_reduce(void* out, const float* tmp, const float* ml, const float* es,
     static bool done[64] = {false};
     int rc = ensure_smem(reduce_kernel<128, 16>, kMaxSmem, done, 64);
     if (rc != PKV_OK) return rc;
-    reduce_kernel<128, 16><<<grid, 16 * 32, smem, st>>>(o, tmp, ml, es, context_lens, num_heads,
-                                                        np_max, partition_size, prefix_blocks,
-                                                        block_size, slot_split, pp, err);
+    return launch_dependent(reduce_kernel<128, 16>, grid, dim3(16 * 32), smem, st, o, tmp, ml, es,
+                            context_lens, num_heads, np_max, partition_size, prefix_blocks,
+                            block_size, slot_split, pp, err);
   } else {
     static bool done[64] = {false};
     int rc = ensure_smem(reduce_kernel<256, 16>, kMaxSmem, done, 64);
     if (rc != PKV_OK) return rc;
-    reduce_kernel<256, 16><<<grid, 16 * 32, smem, st>>>(o, tmp, ml, es, context_lens, num_heads,
-                                                        np_max, partition_size, prefix_blocks,
-                                                        block_size, slot_split, pp, err);
+    return launch_dependent(reduce_kernel<256, 16>, grid, dim3(16 * 32), smem, st, o, tmp, ml, es,
+                            context_lens, num_heads, np_max, partition_size, prefix_blocks,
+                            block_size, slot_split, pp, err);
   }
   return launch_status();
 }
