@@ -74,7 +74,9 @@ struct TcGeom {
   static constexpr int kThreads = (NW + 1) * 32;
 };
 
-template <int D, int BS, bool FP8, int NW, int NST>
+// BS = rows of a ring page; a pool block holds UPB such pages (UPB = 2 runs a
+// 32-token pool in 16-token pages).
+template <int D, int BS, bool FP8, int NW, int NST, int UPB>
 __global__ void __launch_bounds__(TcGeom<D, BS, FP8, NW, NST>::kThreads)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tmk,
                      const __grid_constant__ CUtensorMap tmv, const DecodeParams p) {
@@ -110,7 +112,7 @@ __global__ void __launch_bounds__(TcGeom<D, BS, FP8, NW, NST>::kThreads)
   const int g = p.group;
 
   int ctx = p.context_lens[s];
-  const int cap = p.max_blocks_per_seq * BS;
+  const int cap = p.max_blocks_per_seq * BS * UPB;
   if (ctx < 0 || ctx > cap) {
     if (threadIdx.x == 0 && part == 0 && h == 0) report_error(p.err, PKV_DEVERR_CONTEXT);
     ctx = ctx < 0 ? 0 : cap;
@@ -118,9 +120,9 @@ __global__ void __launch_bounds__(TcGeom<D, BS, FP8, NW, NST>::kThreads)
   int blk_begin = 0;
   int blk_end = (ctx + BS - 1) / BS;
   if (p.partition_blocks > 0) {
-    blk_begin = part * p.partition_blocks + (p.block_offset ? p.block_offset[s] : 0);
+    blk_begin = (part * p.partition_blocks + (p.block_offset ? p.block_offset[s] : 0)) * UPB;
     if (blk_begin >= blk_end) return;  // partition past the end: nothing to store
-    blk_end = min(blk_end, blk_begin + p.partition_blocks);
+    blk_end = min(blk_end, blk_begin + p.partition_blocks * UPB);
   } else if (p.cluster > 1) {
     // one pass over a cluster: rank r takes an equal share of the pages (it may
     // get none, but it still takes part in the cluster merge below)
@@ -155,7 +157,8 @@ __global__ void __launch_bounds__(TcGeom<D, BS, FP8, NW, NST>::kThreads)
       for (int it = 0; it < nblk; ++it) {
         const int st = it % NST;
         if (it >= NST && !mbar_wait(&empty[st], ((it / NST) - 1) & 1, p.err)) break;
-        const int32_t pb = bt[blk_begin + it];
+        const int u = blk_begin + it;  // page of the sequence
+        const int32_t pb = bt[u / UPB];
         issued = it + 1;
         if (pb < 0 || pb >= p.num_blocks) {
           report_error(p.err, PKV_DEVERR_BLOCK_ID);
@@ -163,7 +166,7 @@ __global__ void __launch_bounds__(TcGeom<D, BS, FP8, NW, NST>::kThreads)
           continue;
         }
         const uint32_t kdst = ring + st * G::kStage;
-        const int y = (pb * p.num_kv_heads + h) * BS;
+        const int y = (pb * p.num_kv_heads + h) * (BS * UPB) + (u % UPB) * BS;
         mbar_arrive_expect_tx(&full[st], 2 * PAGE);
         tma_load_page(kdst, &tmk, y, &full[st]);
         tma_load_page(kdst + PAGE, &tmv, y, &full[st]);
@@ -523,13 +526,20 @@ int pool_tensor_map(CUtensorMap* out, const void* base, int64_t rows, int D, int
   return PKV_OK;
 }
 
-template <int D, int BS, bool FP8, int NW, int NST>
-static int launch_tc(const DecodeParams& p_in, const CUtensorMap& tk, const CUtensorMap& tv,
+template <int D, int BS, bool FP8, int NW, int NST, int UPB = 1>
+static int launch_tc(const DecodeParams& p_in, const void* k_cache, const void* v_cache,
                      dim3 grid, cudaStream_t st) {
   using G = TcGeom<D, BS, FP8, NW, NST>;
+  // whole-page boxes of BS rows over the pool viewed as [NB*Hk*BS*UPB rows][D]
+  const int64_t rows = static_cast<int64_t>(p_in.num_blocks) * p_in.num_kv_heads * BS * UPB;
+  CUtensorMap tk, tv;
+  int rc = pool_tensor_map(&tk, k_cache, rows, D, BS, FP8, true);
+  if (rc != PKV_OK) return rc;
+  rc = pool_tensor_map(&tv, v_cache, rows, D, BS, FP8, true);
+  if (rc != PKV_OK) return rc;
   static bool done[64] = {false};
-  auto kern = decode_tc_kernel<D, BS, FP8, NW, NST>;
-  int rc = ensure_smem(kern, G::kSmem, done, 64);
+  auto kern = decode_tc_kernel<D, BS, FP8, NW, NST, UPB>;
+  rc = ensure_smem(kern, G::kSmem, done, 64);
   if (rc != PKV_OK) return rc;
   DecodeParams p = p_in;
   if (p.partition_blocks > 0 || p.cluster <= 1) {
@@ -589,28 +599,31 @@ static int launch_tc(const DecodeParams& p_in, const CUtensorMap& tk, const CUte
 }
 
 template <bool FP8>
-static int dispatch_tc(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
+static int dispatch_tc(const DecodeParams& p, const void* k_cache, const void* v_cache,
                        int head_dim, int block_size, dim3 grid, cudaStream_t st) {
   // (consumer warps, ring stages). At d = 256 two stages and more CTAs per SM
   // measured best (swept on GB300: bf16 B = 16 (2,2) over (1,2) (2,3) (2,4)
-  // (4,2) (4,3); FP8 B = 32 (4,2) over (4,3) (4,4) (8,2) (8,3) (2,2) (2,4));
-  // the d = 128 shapes keep 64 KB of stages (not swept).
-  if (head_dim == 256 && block_size == 16) return launch_tc<256, 16, FP8, 2, 2>(p, tk, tv, grid, st);
-  if (head_dim == 256 && block_size == 32) return launch_tc<256, 32, FP8, FP8 ? 4 : 2, 2>(p, tk, tv, grid, st);
-  if (head_dim == 128 && block_size == 16) return launch_tc<128, 16, FP8, 4, 8>(p, tk, tv, grid, st);
-  return launch_tc<128, 32, FP8, 4, 4>(p, tk, tv, grid, st);
+  // (4,2) (4,3); FP8 B = 32 (4,2) over (4,1) (4,3) (4,4) (8,2) (8,3) (2,2)
+  // (2,4)); bf16 B = 32 pools run in 16-row pages with the B = 16 tile
+  // (mixed lengths 0.3495 -> 0.3438 ms; FP8 lost with 16-row pages); the
+  // d = 128 shapes keep 64 KB of stages (not swept).
+  if (head_dim == 256 && block_size == 16)
+    return launch_tc<256, 16, FP8, 2, 2>(p, k_cache, v_cache, grid, st);
+  if (head_dim == 256 && block_size == 32) {
+    if constexpr (FP8)
+      return launch_tc<256, 32, FP8, 4, 2>(p, k_cache, v_cache, grid, st);
+    else
+      return launch_tc<256, 16, FP8, 2, 2, 2>(p, k_cache, v_cache, grid, st);
+  }
+  if (head_dim == 128 && block_size == 16)
+    return launch_tc<128, 16, FP8, 4, 8>(p, k_cache, v_cache, grid, st);
+  return launch_tc<128, 32, FP8, 4, 4>(p, k_cache, v_cache, grid, st);
 }
 
 int launch_decode_tc(const DecodeParams& p, const void* k_cache, const void* v_cache,
                      int head_dim, int block_size, bool fp8, dim3 grid, cudaStream_t st) {
-  const int64_t rows = static_cast<int64_t>(p.num_blocks) * p.num_kv_heads * block_size;
-  CUtensorMap tk, tv;
-  int rc = pool_tensor_map(&tk, k_cache, rows, head_dim, block_size, fp8, true);
-  if (rc != PKV_OK) return rc;
-  rc = pool_tensor_map(&tv, v_cache, rows, head_dim, block_size, fp8, true);
-  if (rc != PKV_OK) return rc;
-  return fp8 ? dispatch_tc<true>(p, tk, tv, head_dim, block_size, grid, st)
-             : dispatch_tc<false>(p, tk, tv, head_dim, block_size, grid, st);
+  return fp8 ? dispatch_tc<true>(p, k_cache, v_cache, head_dim, block_size, grid, st)
+             : dispatch_tc<false>(p, k_cache, v_cache, head_dim, block_size, grid, st);
 }
 
 }  // namespace pkv
