@@ -42,7 +42,10 @@
  *   - Every launch is asynchronous on `stream` (a cudaStream_t; NULL = legacy
  *     default stream). PKV_OK means "validated and enqueued". A launch failure
  *     returns PKV_ERR_CUDA. Faults inside a kernel surface at the caller's
- *     next synchronisation.
+ *     next synchronisation. The decode and merge kernels are launched as
+ *     programmatic dependents of the work before them on the stream: their
+ *     CTAs may be scheduled early, but they wait for that work to complete
+ *     before reading global memory, so stream order holds as usual.
  *   - Kernels check every block id and slot they dereference. An out-of-range
  *     id is skipped (the affected output is unspecified) and, if a device
  *     error word was registered with pkv_set_device_check, an error code is
