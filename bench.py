@@ -5,8 +5,9 @@ python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours
 A step is one pass of the whole hot path over the workload's batch: for every
 layer the new token's K/V are written into their slots (kv_cache_write), the
 split decode attends over the paged cache (paged_attention_decode) and the
-partitions are merged (paged_attention_reduce); shared-prefix workloads also
-replay their copy-on-write block copies (copy_blocks) once per step. Inputs
+partitions are merged (paged_attention_reduce); shared-prefix workloads use
+the shared-prefix decode, and their copy-on-write block copies (copy_blocks,
+the divergence iteration's) are timed on their own. Inputs
 are resident in HBM; the default workload (64 sequences x 8192 tokens x 16
 layers, 34 GB of K/V per step) is far larger than L2, smaller workloads flush
 L2 before every step.
@@ -355,6 +356,7 @@ def main():
                 if ev is not None:
                     ev[layer][1].record(stream)
                 continue
+            # the decode kernel alone (the roofline's kernel), then the merge
             pkv.paged_attention_decode(out[layer], st.q, st.k_cache, st.v_cache, pw.block_tables,
                                        pw.context_lens, w.scale, pw.max_context, P, ws,
                                        st.k_scale, st.v_scale)

@@ -182,6 +182,22 @@ int pkv_paged_attention_reduce(void* out, const void* workspace,
                                int partition_size, void* stream);
 
 /* ------------------------------------------------------------------------ *
+ * paged_attention: the decode attention of one step in one call, the result
+ * in `out`: pkv_paged_attention_decode, then (partition_size > 0)
+ * pkv_paged_attention_reduce on the same workspace, both on `stream`.
+ * Arguments as for pkv_paged_attention_decode; `out` is always written.
+ * Errors: those of the two calls (the merge is not launched after a failed
+ * decode).
+ * ------------------------------------------------------------------------ */
+int pkv_paged_attention(void* out, const void* q, const void* k_cache,
+                        const void* v_cache, pkv_cache_desc cache,
+                        const float* k_scale, const float* v_scale,
+                        const int32_t* block_tables, int max_blocks_per_seq,
+                        const int32_t* context_lens, int num_seqs, int num_heads,
+                        int max_context, float scale, int partition_size,
+                        void* workspace, size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------ *
  * paged_attention_decode_shared_prefix: decode for groups of sequences that
  * share a prompt's physical blocks (rollouts forked from one prompt,
  * [HowVLLM] "PagedAttention borrows from operating systems"; [Dissect]

@@ -68,6 +68,8 @@ SIGNATURES = {
     "pkv_paged_attention_decode": (_I, [_P, _P, _P, _P, CacheDesc, _P, _P, _P, _I, _P, _I, _I,
                                         _I, ctypes.c_float, _I, _P, ctypes.c_size_t, _P]),
     "pkv_paged_attention_reduce": (_I, [_P, _P, ctypes.c_size_t, _P, _I, _I, _I, _I, _I, _P]),
+    "pkv_paged_attention": (_I, [_P, _P, _P, _P, CacheDesc, _P, _P, _P, _I, _P, _I, _I, _I,
+                                 ctypes.c_float, _I, _P, ctypes.c_size_t, _P]),
     "pkv_paged_attention_decode_noalloc": (_I, [_P, _P, _P, _P, CacheDesc, _P, _P, _P, _I, _P,
                                                 _I, _I, _I, ctypes.c_float, _I, _P]),
     "pkv_shared_prefix_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I, _I, _I, _I]),
@@ -239,17 +241,26 @@ def paged_attention_reduce(out, workspace, context_lens, max_context, partition_
 def paged_attention(q, k_cache, v_cache, block_tables, context_lens, scale, max_context,
                     partition_size=0, k_scale=None, v_scale=None, out=None, workspace=None,
                     stream=None) -> torch.Tensor:
-    """Decode attention; with partition_size > 0 the split decode is followed
-    by the reduce. Returns out [S, Hq, D] bf16."""
+    """Decode attention in one C call: the one-pass decode, or the split
+    decode followed by the merge of its partitions. Returns out [S, Hq, D]
+    bf16."""
+    desc = cache_desc(k_cache)
+    S, Hq, D = q.shape
     if out is None:
         out = torch.empty_like(q)
     if partition_size > 0 and workspace is None:
-        workspace = alloc_workspace(q.shape[0], q.shape[1], q.shape[2], max(int(max_context), 1),
-                                    partition_size, device=q.device)
-    paged_attention_decode(out, q, k_cache, v_cache, block_tables, context_lens, scale,
-                           max_context, partition_size, workspace, k_scale, v_scale, stream)
-    if partition_size > 0:
-        paged_attention_reduce(out, workspace, context_lens, max_context, partition_size, stream)
+        workspace = alloc_workspace(S, Hq, D, max(int(max_context), 1), partition_size,
+                                    device=q.device)
+    wsb = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    rc = lib().pkv_paged_attention(
+        _dev_ptr(out, "out", torch.bfloat16), _dev_ptr(q, "q", torch.bfloat16),
+        _dev_ptr(k_cache, "k_cache"), _dev_ptr(v_cache, "v_cache"), desc,
+        _dev_ptr(k_scale, "k_scale", torch.float32), _dev_ptr(v_scale, "v_scale", torch.float32),
+        _dev_ptr(block_tables, "block_tables", torch.int32), int(block_tables.shape[1]),
+        _dev_ptr(context_lens, "context_lens", torch.int32), S, Hq, int(max_context),
+        float(scale), int(partition_size), _dev_ptr(workspace, "workspace"), wsb,
+        _stream(stream))
+    _check(rc, "paged_attention")
     return out
 
 

@@ -302,3 +302,21 @@ extern "C" int pkv_paged_attention_reduce(void* out, const void* workspace,
                        partition_size, nullptr, 1, 0, partition_size,
                        static_cast<cudaStream_t>(stream));
 }
+
+// The decode and, for the split form, this merge, as one call.
+extern "C" int pkv_paged_attention(void* out, const void* q, const void* k_cache,
+                                   const void* v_cache, pkv_cache_desc cache,
+                                   const float* k_scale, const float* v_scale,
+                                   const int32_t* block_tables, int max_blocks_per_seq,
+                                   const int32_t* context_lens, int num_seqs, int num_heads,
+                                   int max_context, float scale, int partition_size,
+                                   void* workspace, size_t workspace_bytes, void* stream) {
+  const int rc = pkv_paged_attention_decode(out, q, k_cache, v_cache, cache, k_scale, v_scale,
+                                            block_tables, max_blocks_per_seq, context_lens,
+                                            num_seqs, num_heads, max_context, scale,
+                                            partition_size, workspace, workspace_bytes, stream);
+  if (rc != PKV_OK || partition_size == 0) return rc;
+  return pkv_paged_attention_reduce(out, workspace, workspace_bytes, context_lens, num_seqs,
+                                    num_heads, cache.head_dim, max_context, partition_size,
+                                    stream);
+}

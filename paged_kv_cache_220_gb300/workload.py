@@ -195,12 +195,9 @@ def step(pw: PagedWorkload, out: List[torch.Tensor], workspace: Optional[torch.T
     for layer, st in enumerate(pw.layers):
         pkv.kv_cache_write(st.k_new, st.v_new, pw.slot_mapping, st.k_cache, st.v_cache,
                            st.k_scale, st.v_scale, stream)
-        pkv.paged_attention_decode(out[layer], st.q, st.k_cache, st.v_cache, pw.block_tables,
-                                   pw.context_lens, pw.w.scale, pw.max_context, P, workspace,
-                                   st.k_scale, st.v_scale, stream)
-        if P > 0:
-            pkv.paged_attention_reduce(out[layer], workspace, pw.context_lens, pw.max_context, P,
-                                       stream)
+        pkv.paged_attention(st.q, st.k_cache, st.v_cache, pw.block_tables, pw.context_lens,
+                            pw.w.scale, pw.max_context, P, st.k_scale, st.v_scale,
+                            out=out[layer], workspace=workspace, stream=stream)
 
 
 def capture_step(pw: PagedWorkload, out: List[torch.Tensor], workspace: Optional[torch.Tensor],
@@ -347,10 +344,8 @@ class ContinuousBatch:
         cl = torch.as_tensor(ctx, device=dev)
         out = self.out[:n]
         mc = int(ctx.max())
-        pkv.paged_attention_decode(out, q, self.k_cache, self.v_cache, bt, cl, self.scale, mc,
-                                   self.P, self.ws)
-        if self.P:
-            pkv.paged_attention_reduce(out, self.ws, cl, mc, self.P)
+        pkv.paged_attention(q, self.k_cache, self.v_cache, bt, cl, self.scale, mc, self.P,
+                            out=out, workspace=self.ws)
         self.tokens += n
         return ids, ctx, out
 

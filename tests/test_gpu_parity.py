@@ -360,3 +360,43 @@ def test_context_zero_and_device_check(_lib):
     torch.cuda.synchronize()
     assert int(_lib.item()) == pkv.DEVERR_SLOT
     _lib.zero_()
+
+
+@pytest.mark.parametrize("P", [0, 64, 32, 16])
+def test_one_call_entry_equals_decode_then_reduce(P, _lib):
+    """pkv_paged_attention (decode, then the merge for the split form) gives
+    the bits of the two calls made one after the other, rows with an empty
+    context included (zeros); a failed decode launches no merge."""
+    w = dataclasses.replace(synth.tiny(), ctx=[50, 120, 240, 1024])
+    pw = workload.build(w)
+    st = pw.layers[0]
+    pkv.kv_cache_write(st.k_new, st.v_new, pw.slot_mapping, st.k_cache, st.v_cache)
+    ctx = pw.context_lens.clone()
+    ctx[2] = 0
+    outs = []
+    for one_call in (True, False):
+        ws = pkv.alloc_workspace(4, 8, 128, pw.max_context, P) if P else None
+        if ws is not None:
+            ws.fill_(0xFF)
+        out = torch.full_like(st.q, 3.0)
+        if one_call:
+            pkv.paged_attention(st.q, st.k_cache, st.v_cache, pw.block_tables, ctx, w.scale,
+                                pw.max_context, P, out=out, workspace=ws)
+        else:
+            pkv.paged_attention_decode(out, st.q, st.k_cache, st.v_cache, pw.block_tables, ctx,
+                                       w.scale, pw.max_context, P, ws)
+            if P:
+                pkv.paged_attention_reduce(out, ws, ctx, pw.max_context, P)
+        torch.cuda.synchronize()
+        outs.append(out)
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
+    assert torch.all(outs[0][2] == 0)
+    assert_close(outs[0][[0, 1, 3]].cpu(), expected(w, 0, [0, 1, 3]), "one call P=%d" % P)
+    if P:
+        out = torch.full_like(st.q, 3.0)
+        with pytest.raises(pkv.PagedKVError):
+            pkv.paged_attention(st.q, st.k_cache, st.v_cache, pw.block_tables, ctx, w.scale,
+                                pw.max_context, P + 1, out=out, workspace=ws)
+        torch.cuda.synchronize()
+        assert torch.all(out == 3.0)
+    assert int(_lib.item()) == 0
