@@ -30,7 +30,10 @@
 //   (P = P_hi + P_lo to ~16 bits), turned into the B operand of the next
 //   product with movmatrix (an 8x8 transpose in registers);
 // - O^T[D/NW x 8] += V_slice^T[D/NW x 16] . P^T[16 x 8] with mma.m16n8k16,
-//   V^T's fragments read by ldmatrix.trans from the swizzled page.
+//   V^T's fragments read by ldmatrix.trans from the swizzled page (FP8: the
+//   transposed b16 pairs hold two dims of two tokens; a byte permute and an
+//   exact E4M3 -> f16 conversion give the fragments of the even and of the
+//   odd dims).
 // Every warp writes its own columns of the result; the summation order is a
 // function of logical positions only. (Against one page per consumer warp
 // with the warp states merged at the end, measured on GB300: Qwen-like step
@@ -324,21 +327,24 @@ __global__ void __launch_bounds__(TcGeom<D, BS, FP8, NW, NST>::kThreads)
         } else {
           // ---- P in f16 (11-bit mantissa), transposed into the B operand
           const uint32_t b0 = movm_t(pack_f16(p00, p01)), b1 = movm_t(pack_f16(p10, p11));
-          // ---- O^T += V_slice^T . P^T. A plain x4 load gives rows = tokens,
-          // 16 codes per 8x8 b16 matrix (tokens 0-7 / 8-15, columns 16m / 16m+16);
-          // converting a lane's 4 codes gives two 8x8 f16 fragments (columns
-          // 4c+{0,1} and 4c+{2,3}); movmatrix transposes each into an A-operand
-          // piece whose rows are those head-dim offsets (see fp8_row_offset).
+          // ---- O^T += V_slice^T . P^T. A transposed x4 load of 16 tokens x 32
+          // codes gives each lane, per 8x8 b16 matrix, two tokens (2(lane%4),
+          // +1) of the dim pair (2j, 2j+1), j = lane/4; a byte permute puts
+          // each dim's two tokens in one half, converted exactly to f16x2. The
+          // even dims form one A operand (row j: dim 2j of the 32 columns, row
+          // j+8: dim 16+2j), the odd dims the next one.
           const int vrow2 = r0 + (lane & 7) + ((lane >> 3) & 1) * 8;
           const int vcol = (lane >> 4) * 16;
 #pragma unroll
           for (int kk = 0; kk < KW; kk += 2) {
             uint32_t m0r, m1r, m2r, m3r;
-            ldsm_x4(swz_bytes<BS>(vp, vrow2, (kw0 + kk) * 16 + vcol), m0r, m1r, m2r, m3r);
-            mma_f16(o[kk], movm_t(e4m3x2_f16x2(m0r, 0)), movm_t(e4m3x2_f16x2(m0r, 1)),
-                    movm_t(e4m3x2_f16x2(m1r, 0)), movm_t(e4m3x2_f16x2(m1r, 1)), b0, b1);
-            mma_f16(o[kk + 1], movm_t(e4m3x2_f16x2(m2r, 0)), movm_t(e4m3x2_f16x2(m2r, 1)),
-                    movm_t(e4m3x2_f16x2(m3r, 0)), movm_t(e4m3x2_f16x2(m3r, 1)), b0, b1);
+            ldsm_x4_t(swz_bytes<BS>(vp, vrow2, (kw0 + kk) * 16 + vcol), m0r, m1r, m2r, m3r);
+            const uint32_t t0 = pair_tokens(m0r), t1 = pair_tokens(m1r);
+            const uint32_t t2 = pair_tokens(m2r), t3 = pair_tokens(m3r);
+            mma_f16(o[kk], e4m3x2_f16x2(t0, 0), e4m3x2_f16x2(t2, 0), e4m3x2_f16x2(t1, 0),
+                    e4m3x2_f16x2(t3, 0), b0, b1);
+            mma_f16(o[kk + 1], e4m3x2_f16x2(t0, 1), e4m3x2_f16x2(t2, 1), e4m3x2_f16x2(t1, 1),
+                    e4m3x2_f16x2(t3, 1), b0, b1);
           }
         }
       }
@@ -368,9 +374,13 @@ __global__ void __launch_bounds__(TcGeom<D, BS, FP8, NW, NST>::kThreads)
 
   const float vsc = FP8 ? p.v_scale[h] : 1.f;
   const int q0 = (lane & 3) * 2;
-  // head-dim offsets of the two accumulator rows this lane holds in a tile
-  const int r_lo = FP8 ? fp8_row_offset(lane >> 2) : (lane >> 2);
-  const int r_hi = FP8 ? fp8_row_offset((lane >> 2) + 8) : (lane >> 2) + 8;
+  // head-dim offsets of the two accumulator rows (lane/4, lane/4 + 8) this
+  // lane holds in tile kk: bf16 tiles cover 16 consecutive columns; FP8 tile
+  // pairs cover 32, the even offsets in the first tile, the odd in the second
+  auto col = [&](int kk, int hi) {
+    return FP8 ? (kw0 + (kk & ~1)) * 16 + 2 * (lane >> 2) + (kk & 1) + (hi ? 16 : 0)
+               : (kw0 + kk) * 16 + (lane >> 2) + (hi ? 8 : 0);
+  };
   if (p.cluster > 1) {
     // ---- CTA state (max, sum, unnormalised output per query), then the
     // cluster merges: rank r combines the head-dim slice [r*D/C, (r+1)*D/C)
@@ -382,11 +392,10 @@ __global__ void __launch_bounds__(TcGeom<D, BS, FP8, NW, NST>::kThreads)
     if (warp < NW) {
 #pragma unroll
       for (int kk = 0; kk < KW; ++kk) {
-        const int c0 = (kw0 + kk) * 16;
-        cs_o[q0 * D + c0 + r_lo] = o[kk][0];
-        cs_o[(q0 + 1) * D + c0 + r_lo] = o[kk][1];
-        cs_o[q0 * D + c0 + r_hi] = o[kk][2];
-        cs_o[(q0 + 1) * D + c0 + r_hi] = o[kk][3];
+        cs_o[q0 * D + col(kk, 0)] = o[kk][0];
+        cs_o[(q0 + 1) * D + col(kk, 0)] = o[kk][1];
+        cs_o[q0 * D + col(kk, 1)] = o[kk][2];
+        cs_o[(q0 + 1) * D + col(kk, 1)] = o[kk][3];
       }
       if (warp == 0 && lane < 4) {
         cs_m[q0] = m0;
@@ -431,16 +440,15 @@ __global__ void __launch_bounds__(TcGeom<D, BS, FP8, NW, NST>::kThreads)
     const int64_t hq = static_cast<int64_t>(s) * p.num_heads + h * g + j;
 #pragma unroll
     for (int kk = 0; kk < KW; ++kk) {
-      const int c0 = (kw0 + kk) * 16;
       const float lo = L > 0.f ? (o[kk][e] / L) * vsc : 0.f;
       const float hi = L > 0.f ? (o[kk][2 + e] / L) * vsc : 0.f;
       if (p.partition_blocks == 0) {
-        p.out[hq * D + c0 + r_lo] = float_to_bf16_bits(lo);
-        p.out[hq * D + c0 + r_hi] = float_to_bf16_bits(hi);
+        p.out[hq * D + col(kk, 0)] = float_to_bf16_bits(lo);
+        p.out[hq * D + col(kk, 1)] = float_to_bf16_bits(hi);
       } else {
         float* dst = p.tmp_out + (hq * p.np_max + p.slot_offset + part) * D;
-        dst[c0 + r_lo] = lo;
-        dst[c0 + r_hi] = hi;
+        dst[col(kk, 0)] = lo;
+        dst[col(kk, 1)] = hi;
       }
     }
     if (p.partition_blocks > 0 && warp == 0 && (lane >> 2) == 0) {

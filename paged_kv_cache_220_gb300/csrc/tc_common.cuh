@@ -105,12 +105,14 @@ __device__ __forceinline__ uint32_t e4m3x2_f16x2(uint32_t w, int hi) {
   return d;
 }
 
-// Row of the 16-row output tile that holds head-dimension offset `i` of the
-// FP8 product (see the PV step below): rows 0-7 hold offsets {0,1,4,5,8,9,12,13},
-// rows 8-15 hold {2,3,6,7,10,11,14,15}.
-__device__ __forceinline__ int fp8_row_offset(int row) {
-  const int j = row & 7;
-  return 4 * (j >> 1) + (j & 1) + (row >= 8 ? 2 : 0);
+// Bytes (b0, b2, b1, b3) of w. On a b16 element pair read transposed from an
+// FP8 page (token t: codes of dims 2j, 2j+1; token t+1: the same dims) this
+// gives dim 2j's codes of tokens (t, t+1) in the low half and dim 2j+1's in
+// the high half.
+__device__ __forceinline__ uint32_t pair_tokens(uint32_t w) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, 0, 0x3120;" : "=r"(d) : "r"(w));
+  return d;
 }
 
 // A page is stored as [D*esz/128][B][128 B]: one TMA box per 128-byte column
