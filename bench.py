@@ -339,7 +339,7 @@ def main():
     cascade = None
     if w.prefix_len > 0 and args.shared_prefix and P and not w.fp8:
         cascade = workload.prefix_groups(pw)
-        ws = pkv.shared_prefix_workspace(w.num_seqs, w.num_heads, w.head_dim, pw.max_context,
+        ws = pkv.shared_prefix_workspace(w.num_seqs, w.num_heads, w.head_dim, cascade[3],
                                          cascade[2] * w.block_size, P)
 
     def one_step(ev=None):
@@ -350,7 +350,7 @@ def main():
                 ev[layer][0].record(stream)
             if cascade is not None:
                 pkv.paged_attention_shared_prefix(st.q, st.k_cache, st.v_cache, pw.block_tables,
-                                                  pw.context_lens, w.scale, pw.max_context,
+                                                  pw.context_lens, w.scale, cascade[3],
                                                   cascade[0], cascade[1], cascade[2], P,
                                                   out=out[layer], workspace=ws)
                 if ev is not None:
@@ -583,7 +583,7 @@ def run_e2e(args, pw, w, out, ws, P, per_step_bytes, world, dist, cascade=None):
                                st.v_cache, st.k_scale, st.v_scale)
             if cascade is not None:
                 pkv.paged_attention_shared_prefix(dv[layer]["q"], st.k_cache, st.v_cache, d_bt,
-                                                  d_cl, w.scale, pw.max_context, dm[3], dm[4],
+                                                  d_cl, w.scale, cascade[3], dm[3], dm[4],
                                                   cascade[2], P, out=do[layer], workspace=ws)
             else:
                 pkv.paged_attention(dv[layer]["q"], st.k_cache, st.v_cache, d_bt, d_cl, w.scale,

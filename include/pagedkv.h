@@ -81,7 +81,8 @@ typedef enum { PKV_DTYPE_BF16 = 0, PKV_DTYPE_FP8_E4M3 = 1 } pkv_dtype;
 #define PKV_DEVERR_BLOCK_ID 1    /* block table entry outside [0, num_blocks) */
 #define PKV_DEVERR_SLOT 2        /* slot_mapping entry outside the pool       */
 #define PKV_DEVERR_WAIT_TIMEOUT 3 /* a bounded barrier wait gave up           */
-#define PKV_DEVERR_CONTEXT 4     /* context_len > max_blocks_per_seq*block_size */
+#define PKV_DEVERR_CONTEXT 4     /* context_len outside [0, max_blocks_per_seq*block_size],
+                                    or longer than the call's context bound */
 
 /* Geometry of one layer's K and V pools (both share it). */
 typedef struct {
@@ -214,6 +215,13 @@ int pkv_paged_attention(void* out, const void* q, const void* k_cache,
  *                   blocks only, prefix_blocks[s]*block_size <= context_lens[s];
  *                   0 for a sequence outside every group
  *   max_prefix_blocks : host upper bound of prefix_blocks
+ *   max_own_context : host upper bound of each sequence's own part,
+ *                   context_lens[s] - prefix_blocks[s]*block_size (the whole
+ *                   context for a sequence outside every group); it sizes the
+ *                   own-part grid and slots, so a tight bound saves launching
+ *                   CTAs with no page (a longer own part is reported as
+ *                   PKV_DEVERR_CONTEXT and cut); the other arguments as for
+ *                   pkv_paged_attention_decode
  *   partition_size: split size of each member's own part (multiple of
  *                   block_size, at most 2048 blocks); the shared part uses a
  *                   power-of-two multiple of it chosen by the library (enough
@@ -225,12 +233,12 @@ int pkv_paged_attention(void* out, const void* q, const void* k_cache,
  * the merge combines both. bf16 pools only (PKV_ERR_UNSUPPORTED otherwise).
  * ------------------------------------------------------------------------ */
 size_t pkv_shared_prefix_workspace_bytes(int num_seqs, int num_heads, int head_dim,
-                                         int max_context, int max_prefix_tokens,
+                                         int max_own_context, int max_prefix_tokens,
                                          int partition_size);
 int pkv_paged_attention_decode_shared_prefix(
     void* out, const void* q, const void* k_cache, const void* v_cache,
     pkv_cache_desc cache, const int32_t* block_tables, int max_blocks_per_seq,
-    const int32_t* context_lens, int num_seqs, int num_heads, int max_context,
+    const int32_t* context_lens, int num_seqs, int num_heads, int max_own_context,
     float scale, const int32_t* group_start, int num_groups,
     const int32_t* prefix_blocks, int max_prefix_blocks, int partition_size,
     void* workspace, size_t workspace_bytes, void* stream);

@@ -285,25 +285,27 @@ def paged_attention_decode_noalloc(out, q, k_cache, v_cache, block_tables, conte
     _check(rc, "paged_attention_decode_noalloc")
 
 
-def shared_prefix_workspace(num_seqs, num_heads, head_dim, max_context, max_prefix_tokens,
+def shared_prefix_workspace(num_seqs, num_heads, head_dim, max_own_context, max_prefix_tokens,
                             partition_size, device=None) -> torch.Tensor:
-    n = int(lib().pkv_shared_prefix_workspace_bytes(num_seqs, num_heads, head_dim, max_context,
-                                                    max_prefix_tokens, partition_size))
+    n = int(lib().pkv_shared_prefix_workspace_bytes(num_seqs, num_heads, head_dim,
+                                                    max_own_context, max_prefix_tokens,
+                                                    partition_size))
     return torch.empty(max(n, 16), dtype=torch.uint8, device=device or "cuda")
 
 
 def paged_attention_shared_prefix(q, k_cache, v_cache, block_tables, context_lens, scale,
-                                  max_context, group_start, prefix_blocks, max_prefix_blocks,
+                                  max_own_context, group_start, prefix_blocks, max_prefix_blocks,
                                   partition_size, out=None, workspace=None,
                                   stream=None) -> torch.Tensor:
     """Decode of groups sharing prompt blocks (see the C header): shared pages
-    are read once per group. group_start int32 [G+1], prefix_blocks int32 [S]."""
+    are read once per group. group_start int32 [G+1], prefix_blocks int32 [S];
+    max_own_context bounds context_lens[s] - prefix_blocks[s] * block_size."""
     desc = cache_desc(k_cache)
     S, Hq, D = q.shape
     if out is None:
         out = torch.empty_like(q)
     if workspace is None:
-        workspace = shared_prefix_workspace(S, Hq, D, max(int(max_context), 1),
+        workspace = shared_prefix_workspace(S, Hq, D, max(int(max_own_context), 1),
                                             int(max_prefix_blocks) * desc.block_size,
                                             partition_size, q.device)
     G = int(group_start.shape[0]) - 1
@@ -311,7 +313,7 @@ def paged_attention_shared_prefix(q, k_cache, v_cache, block_tables, context_len
         _dev_ptr(out, "out", torch.bfloat16), _dev_ptr(q, "q", torch.bfloat16),
         _dev_ptr(k_cache, "k_cache"), _dev_ptr(v_cache, "v_cache"), desc,
         _dev_ptr(block_tables, "block_tables", torch.int32), int(block_tables.shape[1]),
-        _dev_ptr(context_lens, "context_lens", torch.int32), S, Hq, int(max_context),
+        _dev_ptr(context_lens, "context_lens", torch.int32), S, Hq, int(max_own_context),
         float(scale), _dev_ptr(group_start, "group_start", torch.int32), G,
         _dev_ptr(prefix_blocks, "prefix_blocks", torch.int32), int(max_prefix_blocks),
         int(partition_size), _dev_ptr(workspace, "workspace"),

@@ -431,34 +431,35 @@ int launch_prefix(const PrefixParams& p, const void* k_cache, const void* v_cach
 }  // namespace pkv
 
 extern "C" size_t pkv_shared_prefix_workspace_bytes(int num_seqs, int num_heads, int head_dim,
-                                                    int max_context, int max_prefix_tokens,
+                                                    int max_own_context, int max_prefix_tokens,
                                                     int partition_size) {
-  if (num_seqs <= 0 || num_heads <= 0 || head_dim <= 0 || max_context <= 0 ||
+  if (num_seqs <= 0 || num_heads <= 0 || head_dim <= 0 || max_own_context <= 0 ||
       partition_size <= 0 || max_prefix_tokens < 0)
     return 0;
   const size_t npp = (static_cast<size_t>(max_prefix_tokens) + partition_size - 1) / partition_size;
-  const size_t nps = (static_cast<size_t>(max_context) + partition_size - 1) / partition_size;
+  const size_t nps = (static_cast<size_t>(max_own_context) + partition_size - 1) / partition_size;
   return static_cast<size_t>(num_seqs) * num_heads * (npp + nps) * (head_dim + 2) * sizeof(float);
 }
 
 extern "C" int pkv_paged_attention_decode_shared_prefix(
     void* out, const void* q, const void* k_cache, const void* v_cache, pkv_cache_desc cache,
     const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
-    int num_seqs, int num_heads, int max_context, float scale, const int32_t* group_start,
+    int num_seqs, int num_heads, int max_own_context, float scale, const int32_t* group_start,
     int num_groups, const int32_t* prefix_blocks, int max_prefix_blocks, int partition_size,
     void* workspace, size_t workspace_bytes, void* stream) {
   using namespace pkv;
   int rc = check_cache_desc(cache);
   if (rc != PKV_OK) return rc;
   if (cache.dtype != PKV_DTYPE_BF16) return PKV_ERR_UNSUPPORTED;
-  if (num_seqs < 0 || num_heads <= 0 || max_context < 0 || max_blocks_per_seq <= 0 ||
+  if (num_seqs < 0 || num_heads <= 0 || max_own_context < 0 || max_blocks_per_seq <= 0 ||
       num_groups < 0 || max_prefix_blocks < 0 || partition_size <= 0)
     return PKV_ERR_INVALID_ARG;
   if (num_heads % cache.num_kv_heads != 0) return PKV_ERR_INVALID_ARG;
   const int g = num_heads / cache.num_kv_heads;
   if (g > 8) return PKV_ERR_UNSUPPORTED;
   if (partition_size % cache.block_size != 0) return PKV_ERR_INVALID_ARG;
-  if (static_cast<int64_t>(max_context) > static_cast<int64_t>(max_blocks_per_seq) * cache.block_size ||
+  if (static_cast<int64_t>(max_own_context) >
+          static_cast<int64_t>(max_blocks_per_seq) * cache.block_size ||
       max_prefix_blocks > max_blocks_per_seq)
     return PKV_ERR_INVALID_ARG;
   if (num_seqs == 0) return PKV_OK;
@@ -471,7 +472,9 @@ extern "C" int pkv_paged_attention_decode_shared_prefix(
   if (static_cast<int64_t>(cache.num_blocks) * cache.num_kv_heads * cache.block_size >=
       (int64_t{1} << 31))
     return PKV_ERR_UNSUPPORTED;
-  const int maxc = max_context > 0 ? max_context : 1;
+  // the own parts' partitions: the grid and the slots after the prefix ones
+  // are sized by the longest own part, not by the longest context
+  const int maxc = max_own_context > 0 ? max_own_context : 1;
   const size_t need = pkv_shared_prefix_workspace_bytes(num_seqs, num_heads, cache.head_dim, maxc,
                                                         max_prefix_blocks * cache.block_size,
                                                         partition_size);

@@ -352,15 +352,18 @@ class ContinuousBatch:
 
 def prefix_groups(pw: PagedWorkload, device="cuda"):
     """Group metadata of a shared-prefix workload: (group_start int32 [G+1],
-    prefix_blocks int32 [S], max_prefix_blocks). The shared prefix of a group
-    is the run of leading full blocks whose physical ids every member's table
-    has in common (a partly filled prompt block is cloned on divergence and
-    so is private)."""
+    prefix_blocks int32 [S], max_prefix_blocks, max_own_context). The shared
+    prefix of a group is the run of leading full blocks whose physical ids
+    every member's table has in common (a partly filled prompt block is
+    cloned on divergence and so is private); max_own_context is the longest
+    context past its sequence's shared prefix."""
     w = pw.w
     S = w.num_seqs
+    ctx = np.asarray(w.ctx, dtype=np.int64)
     if w.prefix_len <= 0:
         return (torch.zeros(1, dtype=torch.int32, device=device),
-                torch.zeros(S, dtype=torch.int32, device=device), 0)
+                torch.zeros(S, dtype=torch.int32, device=device), 0,
+                int(ctx.max()) if S else 0)
     G = w.group
     n_prompt = S // G
     tables = pw.tables_host
@@ -373,20 +376,21 @@ def prefix_groups(pw: PagedWorkload, device="cuda"):
             k += 1
         pre[p * G:(p + 1) * G] = k
     starts = np.arange(0, n_prompt * G + 1, G, dtype=np.int32)
+    own = ctx - pre.astype(np.int64) * w.block_size
     return (torch.as_tensor(starts, device=device), torch.as_tensor(pre, device=device),
-            int(pre.max()) if S else 0)
+            int(pre.max()) if S else 0, int(own.max()) if S else 0)
 
 
 def step_shared_prefix(pw: PagedWorkload, out: List[torch.Tensor], groups, workspace,
                        partition_size: Optional[int] = None, stream=None) -> None:
     """One decode step over every layer with the shared-prefix decode."""
     P = pw.w.partition_size if partition_size is None else partition_size
-    gs, pre, maxpre = groups
+    gs, pre, maxpre, max_own = groups
     for layer, st in enumerate(pw.layers):
         pkv.kv_cache_write(st.k_new, st.v_new, pw.slot_mapping, st.k_cache, st.v_cache,
                            st.k_scale, st.v_scale, stream)
         pkv.paged_attention_shared_prefix(st.q, st.k_cache, st.v_cache, pw.block_tables,
-                                          pw.context_lens, pw.w.scale, pw.max_context, gs, pre,
+                                          pw.context_lens, pw.w.scale, max_own, gs, pre,
                                           maxpre, P, out=out[layer], workspace=workspace,
                                           stream=stream)
 

@@ -91,7 +91,7 @@ def test_cow_rollouts(prompt_len, _lib):
     # the shared-prefix decode as the benchmark runs it (a replayed CUDA graph)
     groups = workload.prefix_groups(pw)
     P = w.partition_size
-    ws = pkv.shared_prefix_workspace(w.num_seqs, w.num_heads, w.head_dim, pw.max_context,
+    ws = pkv.shared_prefix_workspace(w.num_seqs, w.num_heads, w.head_dim, groups[3],
                                      groups[2] * w.block_size, P)
     sp = [torch.empty_like(pw.layers[0].q)]
     g = workload.capture_step(pw, sp, ws, P, groups=groups)

@@ -58,7 +58,7 @@ def test_shared_prefix_mixed_with_ungrouped_and_exact_prefix(_lib):
     w = synth.cow(prompt_len=64, prompts=2, rollouts=4)
     w = dataclasses.replace(w, ctx=[65, 66, 90, 65, 70, 71, 72, 200])
     pw = workload.build(w)
-    gs, pre, mp = workload.prefix_groups(pw)
+    gs, pre, mp, _ = workload.prefix_groups(pw)
     # split the second prompt's group into singletons without a shared prefix
     gs2 = torch.tensor([0, 4], dtype=torch.int32, device="cuda")
     pre2 = pre.clone()
@@ -82,7 +82,7 @@ def test_shared_prefix_graph_replay_matches_eager(_lib):
     pw = workload.build(w)
     groups = workload.prefix_groups(pw)
     P = w.partition_size
-    ws = pkv.shared_prefix_workspace(w.num_seqs, w.num_heads, w.head_dim, pw.max_context,
+    ws = pkv.shared_prefix_workspace(w.num_seqs, w.num_heads, w.head_dim, groups[3],
                                      groups[2] * w.block_size, P)
     eager = [torch.empty_like(pw.layers[0].q)]
     workload.step_shared_prefix(pw, eager, groups, ws, P)
@@ -97,3 +97,30 @@ def test_shared_prefix_graph_replay_matches_eager(_lib):
         assert torch.equal(out[0].view(torch.int16), ref.view(torch.int16))
     assert_close(out[0].cpu(), expected(w, 0, range(w.num_seqs)), "shared prefix graph")
     assert int(_lib.item()) == 0
+
+
+def test_shared_prefix_own_part_bound(_lib):
+    """max_own_context sizes the own-part grid: the longest own part gives
+    the bits of the loose bound (the longest context); a bound below an own
+    part is reported (PKV_DEVERR_CONTEXT), and nothing past the launched
+    partitions is read."""
+    w = synth.cow(prompt_len=2040, prompts=2, rollouts=16)
+    pw = workload.build(w)
+    gs, pre, mp, own = workload.prefix_groups(pw)
+    assert own < pw.max_context - 2000
+    P = w.partition_size
+    st = pw.layers[0]
+    pkv.kv_cache_write(st.k_new, st.v_new, pw.slot_mapping, st.k_cache, st.v_cache)
+    outs = [pkv.paged_attention_shared_prefix(st.q, st.k_cache, st.v_cache, pw.block_tables,
+                                              pw.context_lens, w.scale, bound, gs, pre, mp, P)
+            for bound in (own, pw.max_context)]
+    torch.cuda.synchronize()
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
+    assert int(_lib.item()) == 0
+    assert_close(outs[0].cpu(), expected(w, 0, range(w.num_seqs)), "own-part bound")
+    short = pkv.paged_attention_shared_prefix(st.q, st.k_cache, st.v_cache, pw.block_tables,
+                                              pw.context_lens, w.scale, own - P, gs, pre, mp, P)
+    torch.cuda.synchronize()
+    assert int(_lib.item()) == pkv.DEVERR_CONTEXT
+    assert torch.isfinite(short.float()).all()
+    _lib.zero_()
