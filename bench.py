@@ -424,6 +424,7 @@ def main():
     cow_copy = None
     if cow is not None and len(pw.cow_pairs_host):
         cow_copy = time_copy_blocks(pw, args)
+    host = host_iteration_timing(w) if rank == 0 else None
 
     # end to end through the public API with host buffers
     e2e = None
@@ -470,7 +471,7 @@ def main():
                                "paged_attention_decode_shared_prefix (3 kernels, unique bytes)",
                      "bytes_per_launch": dec_bytes, "launch_ms": round(dec_avg_ms, 5),
                      "traffic": traffic},
-        "cpu_baseline": cpu, "e2e": e2e, "copy_blocks": cow_copy,
+        "cpu_baseline": cpu, "e2e": e2e, "copy_blocks": cow_copy, "host": host,
         "gpu_launches": launches_per_step * K,
         "clocks": clk.summary(),
     }
@@ -491,6 +492,38 @@ def main():
     if dist is not None:
         dist.destroy_process_group()
     return 0
+
+
+def host_iteration_timing(w, iters: int = 100):
+    """Host side of a decode iteration on this workload's batch, off the GPU
+    clock: the scheduler step (one new slot per running sequence, a block
+    taken from the free list when one fills) and the export of the batch's
+    block tables, on a scheduler of its own holding the workload's lengths."""
+    import paged_kv_cache_220_gb300 as pkv
+    B = w.block_size
+    S = w.num_seqs
+    mb = max(-(-(c + iters + 1) // B) for c in w.ctx)
+    blocks = sum(-(-(c + iters + 1) // B) for c in w.ctx) + S
+    alloc = pkv.BlockAllocator(blocks, B, seed=7)
+    sched = pkv.Scheduler(alloc, S)
+    for i, c in enumerate(w.ctx):
+        sched.add_request(i, max(c - 1, 1), iters + 10)
+    sched.step()  # admits every prompt
+    t_step, t_tab = [], []
+    for _ in range(iters):
+        t0 = time.perf_counter()
+        sched.step()
+        t1 = time.perf_counter()
+        sched.block_tables(mb)
+        t_tab.append(time.perf_counter() - t1)
+        t_step.append(t1 - t0)
+    running = sched.counts()["running"]
+    sched.close()
+    alloc.close()
+    return {"sched_step_us": round(statistics.median(t_step) * 1e6, 2),
+            "block_tables_us": round(statistics.median(t_tab) * 1e6, 2),
+            "running": running, "iterations": iters,
+            "note": "median host time per iteration (Python call included)"}
 
 
 def time_copy_blocks(pw, args):
