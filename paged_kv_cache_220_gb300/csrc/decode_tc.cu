@@ -611,15 +611,17 @@ static int dispatch_tc(const DecodeParams& p, const void* k_cache, const void* v
                        int head_dim, int block_size, dim3 grid, cudaStream_t st) {
   // (consumer warps, ring stages). At d = 256 two stages and more CTAs per SM
   // measured best (swept on GB300: bf16 B = 16 (2,2) over (1,2) (2,3) (2,4)
-  // (4,2) (4,3); FP8 B = 32 (4,2) over (4,1) (4,3) (4,4) (8,2) (8,3) (2,2)
-  // (2,4)); bf16 B = 32 pools run in 16-row pages with the B = 16 tile
-  // (mixed lengths 0.3495 -> 0.3438 ms; FP8 lost with 16-row pages); the
-  // d = 128 shapes keep 64 KB of stages (not swept).
+  // (4,2) (4,3); FP8 B = 32 (2,2) over (1,2) (1,3) (2,3) (4,2), after the V
+  // fragments went to transposed byte-pair loads; before that (4,2) had won
+  // over (4,1) (4,3) (4,4) (8,2) (8,3) (2,2) (2,4)); bf16 B = 32 pools run in
+  // 16-row pages with the B = 16 tile (mixed lengths 0.3495 -> 0.3438 ms; FP8
+  // lost with 16-row pages); the d = 128 shapes keep 64 KB of stages (not
+  // swept).
   if (head_dim == 256 && block_size == 16)
     return launch_tc<256, 16, FP8, 2, 2>(p, k_cache, v_cache, grid, st);
   if (head_dim == 256 && block_size == 32) {
     if constexpr (FP8)
-      return launch_tc<256, 32, FP8, 4, 2>(p, k_cache, v_cache, grid, st);
+      return launch_tc<256, 32, FP8, 2, 2>(p, k_cache, v_cache, grid, st);
     else
       return launch_tc<256, 16, FP8, 2, 2, 2>(p, k_cache, v_cache, grid, st);
   }
