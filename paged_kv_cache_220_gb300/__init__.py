@@ -37,6 +37,8 @@ PKV_DTYPE_BF16 = 0
 PKV_DTYPE_FP8_E4M3 = 1
 PKV_PREEMPT_RECOMPUTE = 0
 PKV_PREEMPT_SWAP = 1
+PKV_BATCH_ADMISSION = 0
+PKV_BATCH_LONGEST_FIRST = 1
 
 DEVERR_NONE = 0
 DEVERR_BLOCK_ID = 1
@@ -105,6 +107,7 @@ SIGNATURES = {
     "pkv_sched_prompt_slots": (_I, [_P, ctypes.c_int64, _P, _I, ctypes.POINTER(_I)]),
     "pkv_sched_events": (_I, [_P, _I, _P, _I, ctypes.POINTER(_I)]),
     "pkv_sched_set_preemption": (_I, [_P, _I]),
+    "pkv_sched_set_batch_order": (_I, [_P, _I]),
     "pkv_sched_swap_blocks": (_I, [_P, ctypes.c_int64, _P, _I, ctypes.POINTER(_I)]),
     "pkv_sched_counts": (_I, [_P, ctypes.POINTER(_I), ctypes.POINTER(_I),
                               ctypes.POINTER(ctypes.c_longlong)]),
@@ -550,6 +553,11 @@ class Scheduler:
                                             out.ctypes.data_as(ctypes.c_void_p), out.size,
                                             ctypes.byref(n)), "sched_prompt_slots")
         return out[:n.value]
+
+    def set_batch_order(self, order: int) -> None:
+        """Row order of running() / block_tables(): PKV_BATCH_ADMISSION
+        (default) or PKV_BATCH_LONGEST_FIRST."""
+        _check(lib().pkv_sched_set_batch_order(self._h, int(order)), "sched_set_batch_order")
 
     def set_preemption(self, mode: int) -> None:
         """PKV_PREEMPT_RECOMPUTE (default) or PKV_PREEMPT_SWAP."""

@@ -67,7 +67,27 @@ struct pkv_scheduler {
   std::deque<Req> swapped;                  // swapped-out requests, resume order
   std::vector<Req> swapped_out;             // swapped out in the last step (for their blocks)
   std::vector<int64_t> swapped_in;          // ids resumed in the last step
+  int batch_order = PKV_BATCH_ADMISSION;    // row order of the exported batch
 };
+
+namespace {
+
+// Rows of the exported batch: indices into running, in admission order or
+// by decreasing context length (ties in admission order).
+std::vector<int> export_order(const pkv_scheduler* s) {
+  std::vector<int> idx(s->running.size());
+  for (size_t i = 0; i < idx.size(); ++i) idx[i] = static_cast<int>(i);
+  if (s->batch_order == PKV_BATCH_LONGEST_FIRST) {
+    std::stable_sort(idx.begin(), idx.end(), [s](int a, int b) {
+      const Req& x = s->running[a];
+      const Req& y = s->running[b];
+      return x.prompt_len + x.generated > y.prompt_len + y.generated;
+    });
+  }
+  return idx;
+}
+
+}  // namespace
 
 extern "C" int pkv_sched_create(pkv_allocator* alloc, int block_size, int max_num_seqs,
                                 pkv_scheduler** out) {
@@ -275,11 +295,16 @@ extern "C" int pkv_sched_running(const pkv_scheduler* s, int64_t* request_ids,
   if (!s) return PKV_ERR_INVALID_ARG;
   const int n = static_cast<int>(s->running.size());
   if (cap < n) return PKV_ERR_INVALID_ARG;
-  for (int i = 0; i < n; ++i) {
-    const Req& r = s->running[i];
-    if (request_ids) request_ids[i] = r.id;
-    if (context_lens) context_lens[i] = r.prompt_len + r.generated;
-    if (new_slots) new_slots[i] = s->new_slots[i];
+  try {
+    const std::vector<int> order = export_order(s);
+    for (int i = 0; i < n; ++i) {
+      const Req& r = s->running[order[i]];
+      if (request_ids) request_ids[i] = r.id;
+      if (context_lens) context_lens[i] = r.prompt_len + r.generated;
+      if (new_slots) new_slots[i] = s->new_slots[order[i]];
+    }
+  } catch (...) {
+    return PKV_ERR_OUT_OF_BLOCKS;
   }
   return PKV_OK;
 }
@@ -289,10 +314,16 @@ extern "C" int pkv_sched_block_tables(const pkv_scheduler* s, int32_t* tables, i
   if (!s || !tables || max_blocks <= 0) return PKV_ERR_INVALID_ARG;
   const int n = static_cast<int>(s->running.size());
   if (rows < n) return PKV_ERR_INVALID_ARG;
+  std::vector<int> order;
+  try {
+    order = export_order(s);
+  } catch (...) {
+    return PKV_ERR_OUT_OF_BLOCKS;
+  }
   for (int i = 0; i < n; ++i) {
     int32_t* row = tables + static_cast<int64_t>(i) * max_blocks;
     int nb = 0;
-    const int rc = pkv_seq_block_table(s->alloc, s->running[i].seq, row, max_blocks, &nb);
+    const int rc = pkv_seq_block_table(s->alloc, s->running[order[i]].seq, row, max_blocks, &nb);
     if (rc != PKV_OK) return rc;
     std::fill(row + nb, row + max_blocks, -1);
   }
@@ -334,6 +365,13 @@ extern "C" int pkv_sched_events(const pkv_scheduler* s, int kind, int64_t* ids, 
 extern "C" int pkv_sched_set_preemption(pkv_scheduler* s, int mode) {
   if (!s || (mode != PKV_PREEMPT_RECOMPUTE && mode != PKV_PREEMPT_SWAP)) return PKV_ERR_INVALID_ARG;
   s->preempt_mode = mode;
+  return PKV_OK;
+}
+
+extern "C" int pkv_sched_set_batch_order(pkv_scheduler* s, int order) {
+  if (!s || (order != PKV_BATCH_ADMISSION && order != PKV_BATCH_LONGEST_FIRST))
+    return PKV_ERR_INVALID_ARG;
+  s->batch_order = order;
   return PKV_OK;
 }
 

@@ -255,11 +255,15 @@ class ContinuousBatch:
     progress: its blocks are copied to pinned host memory (swap_out) before
     anything is written in that iteration, and copied back into fresh blocks
     (swap_in) when it is resumed; without it, preempted requests are
-    recomputed from their prompts."""
+    recomputed from their prompts.
+
+    batch_order="longest_first": the scheduler reports the batch by
+    decreasing context length (the decode's longest rows launch first)."""
 
     def __init__(self, seed, requests, num_blocks, block_size=32, num_heads=24,
                  num_kv_heads=4, head_dim=256, max_num_seqs=64, partition_size=512,
-                 device="cuda", alloc_seed=None, preemption="recompute"):
+                 device="cuda", alloc_seed=None, preemption="recompute",
+                 batch_order="admission"):
         self.seed = seed
         self.B = block_size
         self.Hq, self.Hk, self.D = num_heads, num_kv_heads, head_dim
@@ -272,6 +276,10 @@ class ContinuousBatch:
             raise ValueError("preemption: 'recompute' or 'swap'")
         if preemption == "swap":
             self.sched.set_preemption(pkv.PKV_PREEMPT_SWAP)
+        if batch_order not in ("admission", "longest_first"):
+            raise ValueError("batch_order: 'admission' or 'longest_first'")
+        if batch_order == "longest_first":
+            self.sched.set_batch_order(pkv.PKV_BATCH_LONGEST_FIRST)
         self.saved = {}       # request id -> pinned host (K, V) blocks
         self.retired = []     # host buffers whose swap_in may still be in flight
         self.swaps = 0

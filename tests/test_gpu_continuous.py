@@ -25,14 +25,15 @@ def _oracle(cb, ids, ctx):
     return oracle.decode(q, ks, vs, cb.scale)
 
 
-@pytest.mark.parametrize("P,pool", [(512, 400), (0, 160)])
-def test_continuous_batching_iterations_match_oracle(P, pool):
+@pytest.mark.parametrize("P,pool,order", [(512, 400, "admission"), (0, 160, "admission"),
+                                          (512, 400, "longest_first")])
+def test_continuous_batching_iterations_match_oracle(P, pool, order):
     pkv_build.build()
     flag = torch.zeros(1, dtype=torch.int32, device="cuda")
     pkv.set_device_check(flag)
     reqs = synth.request_mix(11, 40, prompt_lo=16, prompt_hi=1500, gen_lo=4, gen_hi=200)
     cb = workload.ContinuousBatch(31, reqs, num_blocks=pool, block_size=32, max_num_seqs=12,
-                                  partition_size=P)
+                                  partition_size=P, batch_order=order)
     it, checked, preempted = 0, 0, 0
     while not cb.done() and it < 5000:
         r = cb.step()
@@ -41,6 +42,8 @@ def test_continuous_batching_iterations_match_oracle(P, pool):
         if r is None:
             continue
         ids, ctx, out = r
+        if order == "longest_first":
+            assert all(int(ctx[k]) >= int(ctx[k + 1]) for k in range(len(ctx) - 1))
         if it % 37 == 1:
             torch.cuda.synchronize()
             assert_close(out.cpu(), _oracle(cb, ids, ctx), "iteration %d" % it)

@@ -182,3 +182,45 @@ def test_swap_mode_arguments():
         sched.set_preemption(7)
     with pytest.raises(pkv.PagedKVError):
         sched.swap_blocks(3)
+
+
+def test_longest_first_batch_order():
+    """Two schedulers on the same requests and the same seeded pool, one
+    reporting in admission order and one longest first: every iteration gives
+    the same rows (request, context, slot, block-table row), the second
+    sorted by decreasing context with ties in admission order; preemption
+    and completion are unchanged."""
+    B = 16
+    reqs = synth.request_mix(11, 30, prompt_lo=16, prompt_hi=400, gen_lo=8, gen_hi=200)
+    runs = []
+    for order in (pkv.PKV_BATCH_ADMISSION, pkv.PKV_BATCH_LONGEST_FIRST):
+        alloc = pkv.BlockAllocator(120, B, seed=5)
+        sched = pkv.Scheduler(alloc, max_num_seqs=12)
+        sched.set_batch_order(order)
+        for rid, p, g in reqs:
+            sched.add_request(rid, p, g)
+        runs.append((alloc, sched))
+    steps = 0
+    while True:
+        rows = []
+        for alloc, sched in runs:
+            n, _, _ = sched.step()
+            ids, ctx, slots = sched.running()
+            tables = sched.block_tables(64)
+            rows.append((n, ids, ctx, slots, tables, sched.events(2).tolist()))
+            if n:
+                _check(alloc, sched, B)
+        (n0, i0, c0, s0, t0, p0), (n1, i1, c1, s1, t1, p1) = rows
+        assert n0 == n1 and p0 == p1
+        if n0 == 0 and runs[0][1].counts()["waiting"] == 0:
+            break
+        key = sorted(range(n0), key=lambda k: -int(c0[k]))  # stable: ties keep admission order
+        assert i1.tolist() == [int(i0[k]) for k in key]
+        assert c1.tolist() == [int(c0[k]) for k in key]
+        assert s1.tolist() == [int(s0[k]) for k in key]
+        assert np.array_equal(t1, t0[key])
+        assert all(c1[k] >= c1[k + 1] for k in range(n1 - 1))
+        steps += 1
+    assert steps > 50
+    with pytest.raises(pkv.PagedKVError):
+        runs[0][1].set_batch_order(7)
