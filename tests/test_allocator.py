@@ -289,3 +289,70 @@ def test_checkpoint_rejects_inconsistent_records():
     for r in bad:
         with pytest.raises(pkv.PagedKVError):
             load(r)
+
+
+def test_random_operations_keep_every_sequence_readable():
+    """A random mix of new / fork / append / free on a small pool, checked
+    against a model of the pool's contents: every slot holds the label of
+    the token last written there, copy-on-write pairs copy whole blocks (as
+    copy_blocks does) before the new token is written, and after every
+    operation each live sequence reads its own tokens through its block
+    table (a fork's shared prefix reads the parent's tokens). A call that
+    fails for lack of blocks leaves the whole state unchanged (compared
+    through the checkpoint record); the invariants hold throughout."""
+    B, NB = 4, 48
+    a = pkv.BlockAllocator(NB, B, seed=13)
+    rng = np.random.default_rng(2024)
+    content = {}          # slot -> token label
+    toks = {}             # live sequence -> its token labels, logical order
+    next_label = [0]
+
+    def label():
+        next_label[0] += 1
+        return next_label[0]
+
+    def check():
+        for s, tl in toks.items():
+            t = a.block_table(s)
+            assert a.seq_len(s) == len(tl)
+            for i, lab in enumerate(tl):
+                assert content.get(int(t[i // B]) * B + i % B) == lab, (s, i)
+        _check_invariants(a, list(toks))
+
+    failed = 0
+    for _ in range(3000):
+        op = rng.integers(0, 10)
+        live = list(toks)
+        if op == 0 or not live:
+            toks[a.new_seq()] = []
+        elif op == 1 and len(live) < 16:
+            p = live[rng.integers(len(live))]
+            toks[a.fork(p)] = list(toks[p])
+        elif op == 2:
+            s = live[rng.integers(len(live))]
+            a.free(s)
+            del toks[s]
+        else:
+            s = live[rng.integers(len(live))]
+            n = int(rng.integers(1, 3 * B))
+            before = a.save()
+            try:
+                slots, pairs = a.append(s, n)
+            except pkv.PagedKVError as e:
+                assert e.status == pkv.PKV_ERR_OUT_OF_BLOCKS
+                assert a.save() == before
+                failed += 1
+                continue
+            for src, dst in pairs.tolist():
+                for r in range(B):
+                    if src * B + r in content:
+                        content[dst * B + r] = content[src * B + r]
+            for sl in slots.tolist():
+                lab = label()
+                content[int(sl)] = lab
+                toks[s].append(lab)
+        check()
+    assert failed > 0 and next_label[0] > 1000
+    for s in list(toks):
+        a.free(s)
+    assert a.stats()["free_blocks"] == NB
