@@ -448,6 +448,21 @@ int pkv_sched_create(pkv_allocator* alloc, int block_size, int max_num_seqs,
 void pkv_sched_destroy(pkv_scheduler* s);
 int pkv_sched_add_request(pkv_scheduler* s, int64_t request_id, int prompt_len,
                           int max_new_tokens);
+/* A request for n sampled continuations of one prompt (n = 1: the call
+ * above). It is admitted as a unit once the batch has room for n rows and
+ * the free blocks cover the prompt plus one block per sample: the prompt is
+ * stored once (its slots reported under request_id) and n - 1 forks share
+ * its blocks ([HowVLLM] "PagedAttention borrows from operating systems";
+ * [Dissect] "PagedAttention: Virtual Memory for KV Cache": copy-on-write
+ * among sequences of one prompt). The samples run as requests request_id,
+ * request_id + 1, ..., request_id + n - 1 (keep other requests' ids apart);
+ * each has the token budget max_new_tokens. A sample that writes into a block
+ * still shared gets a copy (pkv_sched_cow_pairs). A preempted sample comes
+ * back as a request of its own (recompute: from the prompt; swap: its blocks,
+ * shared ones included, are copied out and back into private blocks).
+ * PKV_ERR_INVALID_ARG if n < 1 or n > max_num_seqs. */
+int pkv_sched_add_request_n(pkv_scheduler* s, int64_t request_id, int prompt_len,
+                            int max_new_tokens, int n);
 /* One iteration; reports the batch size, the requests admitted in it and
  * those ejected at its start. */
 int pkv_sched_step(pkv_scheduler* s, int* num_running, int* num_admitted,
@@ -468,6 +483,14 @@ int pkv_sched_prompt_slots(const pkv_scheduler* s, int64_t request_id,
  * again in the same step appears in neither 3 nor 4 (its saved copy stays
  * valid). */
 int pkv_sched_events(const pkv_scheduler* s, int kind, int64_t* ids, int cap, int* n);
+/* Copy-on-write pairs (src, dst) of the last step, host int32 [n][2]: blocks
+ * still shared with other samples that a sample cloned to write this
+ * iteration's token. Within an iteration the caller applies, in this order:
+ * swap-outs (events 3), swap-ins (events 4), the admitted prompts' K/V,
+ * pkv_copy_blocks of these pairs, this iteration's K/V (pkv_kv_cache_write),
+ * then the decode. n = 0 when no block was shared. PKV_ERR_INVALID_ARG if cap
+ * is below n (n is still reported). */
+int pkv_sched_cow_pairs(const pkv_scheduler* s, int32_t* pairs, int cap, int* n);
 /* waiting counts queued and swapped-out requests. */
 int pkv_sched_counts(const pkv_scheduler* s, int* waiting, int* running,
                      long long* steps);

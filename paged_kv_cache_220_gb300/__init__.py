@@ -101,6 +101,8 @@ SIGNATURES = {
     "pkv_sched_create": (_I, [_P, _I, _I, ctypes.POINTER(_P)]),
     "pkv_sched_destroy": (None, [_P]),
     "pkv_sched_add_request": (_I, [_P, ctypes.c_int64, _I, _I]),
+    "pkv_sched_add_request_n": (_I, [_P, ctypes.c_int64, _I, _I, _I]),
+    "pkv_sched_cow_pairs": (_I, [_P, _P, _I, ctypes.POINTER(_I)]),
     "pkv_sched_step": (_I, [_P, ctypes.POINTER(_I), ctypes.POINTER(_I), ctypes.POINTER(_I)]),
     "pkv_sched_running": (_I, [_P, _P, _P, _P, _I]),
     "pkv_sched_block_tables": (_I, [_P, _P, _I, _I]),
@@ -513,9 +515,25 @@ class Scheduler:
         except Exception:
             pass
 
-    def add_request(self, request_id: int, prompt_len: int, max_new_tokens: int) -> None:
-        _check(lib().pkv_sched_add_request(self._h, int(request_id), int(prompt_len),
-                                           int(max_new_tokens)), "sched_add_request")
+    def add_request(self, request_id: int, prompt_len: int, max_new_tokens: int,
+                    n: int = 1) -> None:
+        """n > 1: n samples of one prompt, as requests request_id ..
+        request_id + n - 1 sharing the prompt's blocks."""
+        _check(lib().pkv_sched_add_request_n(self._h, int(request_id), int(prompt_len),
+                                             int(max_new_tokens), int(n)), "sched_add_request")
+
+    def cow_pairs(self) -> np.ndarray:
+        """Copy-on-write pairs (src, dst) of the last step, int32 [k, 2]; apply
+        them with copy_blocks after the admitted prompts' K/V and before this
+        iteration's K/V."""
+        n = ctypes.c_int()
+        rc = lib().pkv_sched_cow_pairs(self._h, None, 0, ctypes.byref(n))
+        if rc not in (PKV_OK, PKV_ERR_INVALID_ARG):
+            _check(rc, "sched_cow_pairs")
+        out = np.empty((max(n.value, 1), 2), np.int32)
+        _check(lib().pkv_sched_cow_pairs(self._h, out.ctypes.data_as(ctypes.c_void_p),
+                                         out.shape[0], ctypes.byref(n)), "sched_cow_pairs")
+        return out[:n.value]
 
     def step(self):
         """One iteration; returns (num_running, num_admitted, num_finished)."""

@@ -48,6 +48,8 @@ struct Req {
   int seq;        // allocator sequence id while running
   std::vector<int64_t> prompt_slots;  // reported in the admitting iteration
   std::vector<int32_t> swap_blocks;   // swap mode: blocks to copy out / back in
+  int samples;    // waiting: sequences to fork from the prompt at admission
+  bool shared_tail = false;  // a sample whose last block is still the shared prompt's
 };
 
 }  // namespace
@@ -68,6 +70,7 @@ struct pkv_scheduler {
   std::vector<Req> swapped_out;             // swapped out in the last step (for their blocks)
   std::vector<int64_t> swapped_in;          // ids resumed in the last step
   int batch_order = PKV_BATCH_ADMISSION;    // row order of the exported batch
+  std::vector<int32_t> cow_pairs;           // (src, dst) of the last step's growth
 };
 
 namespace {
@@ -103,15 +106,21 @@ extern "C" int pkv_sched_create(pkv_allocator* alloc, int block_size, int max_nu
 
 extern "C" void pkv_sched_destroy(pkv_scheduler* s) { delete s; }
 
-extern "C" int pkv_sched_add_request(pkv_scheduler* s, int64_t request_id, int prompt_len,
-                                     int max_new_tokens) {
-  if (!s || prompt_len < 0 || max_new_tokens <= 0) return PKV_ERR_INVALID_ARG;
+extern "C" int pkv_sched_add_request_n(pkv_scheduler* s, int64_t request_id, int prompt_len,
+                                       int max_new_tokens, int n) {
+  if (!s || prompt_len < 0 || max_new_tokens <= 0 || n < 1 || n > s->max_num_seqs)
+    return PKV_ERR_INVALID_ARG;
   try {
-    s->waiting.push_back(Req{request_id, prompt_len, max_new_tokens, 0, -1, {}});
+    s->waiting.push_back(Req{request_id, prompt_len, max_new_tokens, 0, -1, {}, {}, n});
   } catch (...) {
     return PKV_ERR_OUT_OF_BLOCKS;
   }
   return PKV_OK;
+}
+
+extern "C" int pkv_sched_add_request(pkv_scheduler* s, int64_t request_id, int prompt_len,
+                                     int max_new_tokens) {
+  return pkv_sched_add_request_n(s, request_id, prompt_len, max_new_tokens, 1);
 }
 
 namespace {
@@ -129,7 +138,7 @@ int growth_blocks(const pkv_scheduler* s) {
   int n = 0;
   for (const Req& r : s->running) {
     const int64_t len = static_cast<int64_t>(r.prompt_len) + r.generated;
-    if (len % s->block_size == 0) ++n;
+    if (len % s->block_size == 0 || r.shared_tail) ++n;  // a new block or a copy
   }
   return n;
 }
@@ -139,6 +148,16 @@ int preempt_last(pkv_scheduler* s) {
   s->running.pop_back();
   s->preempted.push_back(r.id);
   r.prompt_slots.clear();
+  r.shared_tail = false;
+  // admitted in this very step: its prompt K/V is not stored yet, so there is
+  // nothing to copy out; it waits to be admitted (and prefilled) again
+  if (std::find(s->admitted.begin(), s->admitted.end(), r.id) != s->admitted.end()) {
+    pkv_seq_free(s->alloc, r.seq);
+    r.seq = -1;
+    r.generated = 0;
+    s->waiting.push_front(std::move(r));
+    return PKV_OK;
+  }
   if (s->preempt_mode == PKV_PREEMPT_SWAP) {
     // resumed in this very step: its blocks were never filled and the host
     // copy is still the valid one, so it goes back without a copy-out
@@ -185,6 +204,7 @@ extern "C" int pkv_sched_step(pkv_scheduler* s, int* num_running, int* num_admit
     s->admitted.clear();
     s->swapped_out.clear();
     s->swapped_in.clear();
+    s->cow_pairs.clear();
     // 1. eject
     std::vector<Req> keep;
     keep.reserve(s->running.size());
@@ -227,11 +247,15 @@ extern "C" int pkv_sched_step(pkv_scheduler* s, int* num_running, int* num_admit
       s->swapped_in.push_back(r.id);
       s->running.push_back(std::move(r));
     }
-    // 2b. admit
-    while (s->swapped.empty() && !s->waiting.empty() &&
-           static_cast<int>(s->running.size()) < s->max_num_seqs) {
+    // 2b. admit (a request of n samples: the prompt once, then n - 1 forks
+    // sharing its blocks; each sample's first token may need a block of its
+    // own, a copy of the shared last prompt block or a fresh one)
+    while (s->swapped.empty() && !s->waiting.empty()) {
       Req& w = s->waiting.front();
-      const int need = blocks_for(static_cast<int64_t>(w.prompt_len) + 1, s->block_size);
+      const int n = w.samples;
+      if (static_cast<int>(s->running.size()) + n > s->max_num_seqs) break;
+      const int need = n == 1 ? blocks_for(static_cast<int64_t>(w.prompt_len) + 1, s->block_size)
+                              : blocks_for(w.prompt_len, s->block_size) + n;
       if (need + growth_blocks(s) > free_blocks(s)) break;
       Req r = std::move(w);
       s->waiting.pop_front();
@@ -240,6 +264,7 @@ extern "C" int pkv_sched_step(pkv_scheduler* s, int* num_running, int* num_admit
       if (rc != PKV_OK) return rc;
       r.seq = sid;
       r.generated = 0;
+      r.samples = 1;
       r.prompt_slots.assign(r.prompt_len, -1);
       if (r.prompt_len > 0) {
         rc = pkv_seq_append(s->alloc, sid, r.prompt_len, r.prompt_slots.data(), nullptr, nullptr);
@@ -248,18 +273,42 @@ extern "C" int pkv_sched_step(pkv_scheduler* s, int* num_running, int* num_admit
           return rc;
         }
       }
+      std::vector<Req> forks;
+      for (int k = 1; k < n; ++k) {
+        int child = -1;
+        rc = pkv_seq_fork(s->alloc, sid, &child);
+        if (rc != PKV_OK) {
+          for (Req& f : forks) pkv_seq_free(s->alloc, f.seq);
+          pkv_seq_free(s->alloc, sid);
+          return rc;
+        }
+        forks.push_back(Req{r.id + k, r.prompt_len, r.max_new, 0, child, {}, {}, 1});
+        forks.back().shared_tail = true;
+      }
+      r.shared_tail = n > 1;
       s->admitted.push_back(r.id);
       s->running.push_back(std::move(r));
+      for (Req& f : forks) {
+        s->admitted.push_back(f.id);
+        s->running.push_back(std::move(f));
+      }
     }
     // 3. grow by one token each; preempt the newest on exhaustion
     s->new_slots.clear();
     for (size_t i = 0; i < s->running.size();) {
       Req& r = s->running[i];
       int64_t slot = -1;
-      const int rc = pkv_seq_append(s->alloc, r.seq, 1, &slot, nullptr, nullptr);
+      int32_t pair[2] = {-1, -1};
+      int ncow = 0;
+      const int rc = pkv_seq_append(s->alloc, r.seq, 1, &slot, pair, &ncow);
       if (rc == PKV_OK) {
         ++r.generated;
+        r.shared_tail = false;
         s->new_slots.push_back(slot);
+        if (ncow > 0) {
+          s->cow_pairs.push_back(pair[0]);
+          s->cow_pairs.push_back(pair[1]);
+        }
         ++i;
         continue;
       }
@@ -365,6 +414,14 @@ extern "C" int pkv_sched_events(const pkv_scheduler* s, int kind, int64_t* ids, 
 extern "C" int pkv_sched_set_preemption(pkv_scheduler* s, int mode) {
   if (!s || (mode != PKV_PREEMPT_RECOMPUTE && mode != PKV_PREEMPT_SWAP)) return PKV_ERR_INVALID_ARG;
   s->preempt_mode = mode;
+  return PKV_OK;
+}
+
+extern "C" int pkv_sched_cow_pairs(const pkv_scheduler* s, int32_t* pairs, int cap, int* n) {
+  if (!s || !n) return PKV_ERR_INVALID_ARG;
+  *n = static_cast<int>(s->cow_pairs.size() / 2);
+  if (cap < *n || (*n > 0 && !pairs)) return PKV_ERR_INVALID_ARG;
+  std::copy(s->cow_pairs.begin(), s->cow_pairs.end(), pairs);
   return PKV_OK;
 }
 

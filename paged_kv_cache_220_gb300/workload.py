@@ -258,7 +258,12 @@ class ContinuousBatch:
     recomputed from their prompts.
 
     batch_order="longest_first": the scheduler reports the batch by
-    decreasing context length (the decode's longest rows launch first)."""
+    decreasing context length (the decode's longest rows launch first).
+
+    A request (id, prompt, budget, n) asks for n samples of one prompt: they
+    run as ids id .. id + n - 1, share the prompt's blocks (and rows), and
+    the scheduler's copy-on-write pairs are applied with copy_blocks after
+    the prompts are stored and before the iteration's tokens."""
 
     def __init__(self, seed, requests, num_blocks, block_size=32, num_heads=24,
                  num_kv_heads=4, head_dim=256, max_num_seqs=64, partition_size=512,
@@ -284,10 +289,17 @@ class ContinuousBatch:
         self.retired = []     # host buffers whose swap_in may still be in flight
         self.swaps = 0
         self.max_num_seqs = max_num_seqs
-        self.max_context = max(p + g for _, p, g in requests)
+        # (id, prompt, budget) or (id, prompt, budget, samples): n samples run
+        # as ids id .. id + n - 1 and share the prompt's rows
+        reqs = [tuple(r) + (1,) * (4 - len(r)) for r in requests]
+        self.max_context = max(p + g for _, p, g, _ in reqs)
         self.max_blocks = -(-self.max_context // block_size)
-        for rid, p, g in requests:
-            self.sched.add_request(rid, p, g)
+        self.base_of, self.prompt_of = {}, {}
+        for rid, p, g, n in reqs:
+            self.sched.add_request(rid, p, g, n=n)
+            for k in range(n):
+                self.base_of[rid + k], self.prompt_of[rid + k] = rid, p
+        self.cow_copies = 0
         self.k_cache = torch.zeros(num_blocks, num_kv_heads, block_size, head_dim,
                                    dtype=torch.bfloat16, device=self.device)
         self.v_cache = torch.zeros_like(self.k_cache)
@@ -298,6 +310,20 @@ class ContinuousBatch:
             if partition_size else None
         self.scale = float(torch.tensor(1.0 / (head_dim ** 0.5), dtype=torch.float32))
         self.tokens = 0
+
+    def rows(self, kind, rid, t0, t1, device=None):
+        """K or V rows [t0, t1) of request rid: the prompt's rows (shared by
+        the samples of one prompt) below its prompt length, its own after."""
+        p, base = self.prompt_of[rid], self.base_of[rid]
+        dev = device if device is not None else self.device
+        parts = []
+        if t0 < min(t1, p):
+            parts.append(synth.request_rows(self.seed, kind, 0, base, t0, min(t1, p), self.Hk,
+                                            self.D, dev))
+        if t1 > max(t0, p):
+            parts.append(synth.request_rows(self.seed, kind, 0, rid, max(t0, p), t1, self.Hk,
+                                            self.D, dev))
+        return torch.cat(parts) if len(parts) > 1 else parts[0]
 
     def done(self) -> bool:
         c = self.sched.counts()
@@ -331,18 +357,19 @@ class ContinuousBatch:
             slots = self.sched.prompt_slots(int(rid))
             if len(slots) == 0:
                 continue
-            k = synth.request_rows(self.seed, synth.KIND_K, 0, int(rid), 0, len(slots),
-                                   self.Hk, self.D, dev)
-            v = synth.request_rows(self.seed, synth.KIND_V, 0, int(rid), 0, len(slots),
-                                   self.Hk, self.D, dev)
+            k = self.rows(synth.KIND_K, int(rid), 0, len(slots))
+            v = self.rows(synth.KIND_V, int(rid), 0, len(slots))
             pkv.kv_cache_write(k, v, torch.as_tensor(slots, device=dev), self.k_cache,
                                self.v_cache)
+        # samples writing into a block still shared take a copy of it first
+        pairs = self.sched.cow_pairs()
+        if len(pairs):
+            pkv.copy_blocks(self.k_cache, self.v_cache, torch.as_tensor(pairs, device=dev))
+            self.cow_copies += len(pairs)
         ids, ctx, slots = self.sched.running()
-        k_new = torch.stack([synth.request_rows(self.seed, synth.KIND_K, 0, int(r), int(c) - 1,
-                                                int(c), self.Hk, self.D, dev)[0]
+        k_new = torch.stack([self.rows(synth.KIND_K, int(r), int(c) - 1, int(c))[0]
                              for r, c in zip(ids, ctx)])
-        v_new = torch.stack([synth.request_rows(self.seed, synth.KIND_V, 0, int(r), int(c) - 1,
-                                                int(c), self.Hk, self.D, dev)[0]
+        v_new = torch.stack([self.rows(synth.KIND_V, int(r), int(c) - 1, int(c))[0]
                              for r, c in zip(ids, ctx)])
         q = torch.stack([synth.request_query(self.seed, 0, int(r), int(c) - 1, self.Hq, self.D,
                                              dev) for r, c in zip(ids, ctx)])

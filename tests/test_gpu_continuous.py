@@ -87,3 +87,42 @@ def test_continuous_batching_with_swap_preemption():
     assert cb.alloc.stats()["free_blocks"] == 100
     assert int(flag.item()) == 0
     pkv.set_device_check(None)
+
+
+@pytest.mark.parametrize("preemption", ["recompute", "swap"])
+def test_sampled_requests_share_prompt_blocks(preemption):
+    """Requests of 1-4 samples of one prompt: the samples share the prompt's
+    blocks, copy-on-write clones are made with copy_blocks, and the decode
+    of every checked iteration matches the oracle on each sample's logical
+    rows (the prompt's, then its own), under preemption."""
+    pkv_build.build()
+    flag = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pkv.set_device_check(flag)
+    rng = np.random.default_rng(17)
+    reqs = [(8 * i, int(rng.integers(20, 300)), int(rng.integers(4, 120)),
+             int(rng.integers(1, 5))) for i in range(16)]
+    cb = workload.ContinuousBatch(43, reqs, num_blocks=90, block_size=16, max_num_seqs=12,
+                                  partition_size=64, preemption=preemption)
+    it, checked, preempted = 0, 0, 0
+    while not cb.done() and it < 5000:
+        r = cb.step()
+        it += 1
+        preempted += len(cb.sched.events(2))
+        if r is None:
+            continue
+        ids, ctx, out = r
+        if it % 23 == 1:
+            torch.cuda.synchronize()
+            q = np.stack([bits16(synth.request_query(cb.seed, 0, int(i), int(c) - 1, cb.Hq,
+                                                     cb.D)) for i, c in zip(ids, ctx)])
+            ks = [bits16(cb.rows(synth.KIND_K, int(i), 0, int(c), "cpu"))
+                  for i, c in zip(ids, ctx)]
+            vs = [bits16(cb.rows(synth.KIND_V, int(i), 0, int(c), "cpu"))
+                  for i, c in zip(ids, ctx)]
+            assert_close(out.cpu(), oracle.decode(q, ks, vs, cb.scale), "iteration %d" % it)
+            checked += 1
+    assert cb.done() and checked >= 3
+    assert cb.cow_copies > 0 and preempted > 0
+    assert cb.alloc.stats()["free_blocks"] == 90
+    assert int(flag.item()) == 0
+    pkv.set_device_check(None)

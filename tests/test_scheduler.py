@@ -224,3 +224,82 @@ def test_longest_first_batch_order():
     assert steps > 50
     with pytest.raises(pkv.PagedKVError):
         runs[0][1].set_batch_order(7)
+
+
+@pytest.mark.parametrize("mode", [pkv.PKV_PREEMPT_RECOMPUTE, pkv.PKV_PREEMPT_SWAP])
+def test_sampled_requests_share_the_prompt_with_copy_on_write(mode):
+    """Requests of n samples on a host model of the pool (every slot holds
+    the identity of the token written there), under preemption: the prompt
+    is stored once and shared by the samples' tables; the copy-on-write
+    pairs, applied as whole-block copies after the prompts and before this
+    iteration's tokens, keep every sample reading the prompt's tokens
+    followed by its own through its table, swapped samples included."""
+    B, NB = 8, 48
+    alloc = pkv.BlockAllocator(NB, B, seed=21)
+    sched = pkv.Scheduler(alloc, max_num_seqs=12)
+    sched.set_preemption(mode)
+    rng = np.random.default_rng(5)
+    base_of, plen_of, total = {}, {}, 0
+    for g in range(14):
+        base, p, n = 16 * g, int(rng.integers(3, 40)), int(rng.integers(1, 5))
+        gen = int(rng.integers(4, 120))
+        sched.add_request(base, p, gen, n=n)
+        for k in range(n):
+            base_of[base + k], plen_of[base + k] = base, p
+        total += n
+    pool = np.full((NB, B), -1, dtype=np.int64)
+    saved = {}
+
+    def want(rid, pos):
+        if pos < plen_of[rid]:
+            return -(base_of[rid] * 1_000_000 + pos) - 1   # the shared prompt
+        return rid * 1_000_000 + pos
+
+    done, pairs_seen, shared_seen, prefills, preempted = set(), 0, 0, 0, 0
+    for _ in range(20000):
+        n, _, _ = sched.step()
+        preempted += len(sched.events(2))
+        for rid in sched.events(3):
+            saved[int(rid)] = pool[sched.swap_blocks(int(rid))].copy()
+        for rid in sched.events(4):
+            pool[sched.swap_blocks(int(rid))] = saved.pop(int(rid))
+        for rid in sched.events(0):
+            slots = sched.prompt_slots(int(rid))
+            prefills += len(slots) > 0
+            for pos, slot in enumerate(slots):
+                pool[slot // B, slot % B] = want(int(rid), pos)
+        pairs = sched.cow_pairs()
+        pairs_seen += len(pairs)
+        for src, dst in pairs.tolist():
+            pool[dst] = pool[src]
+        done |= set(sched.events(1).tolist())
+        if n:
+            ids, ctx, slots = sched.running()
+            assert len(set(slots.tolist())) == len(slots)
+            for rid, c, slot in zip(ids, ctx, slots):
+                pool[slot // B, slot % B] = want(int(rid), int(c) - 1)
+            tables = sched.block_tables(256)
+            for i, (rid, c) in enumerate(zip(ids, ctx)):
+                assert len([b for b in tables[i] if b >= 0]) == -(-int(c) // B)
+                got = [int(pool[tables[i][pos // B], pos % B]) for pos in range(int(c))]
+                assert got == [want(int(rid), pos) for pos in range(int(c))], int(rid)
+            st = alloc.stats()
+            assert st["free_blocks"] + st["used_blocks"] == NB
+            shared_seen += st["used_slots"] < int(ctx.sum())
+        if n == 0 and sched.counts()["waiting"] == 0:
+            break
+    assert done == set(base_of)
+    assert pairs_seen > 0 and shared_seen > 0 and not saved
+    assert prefills >= 14
+    assert sched.counts()["running"] == 0 and alloc.stats()["free_blocks"] == NB
+    assert preempted > 0
+
+
+def test_sampled_request_arguments():
+    alloc = pkv.BlockAllocator(8, 16)
+    sched = pkv.Scheduler(alloc, 4)
+    with pytest.raises(pkv.PagedKVError):
+        sched.add_request(0, 10, 5, n=0)
+    with pytest.raises(pkv.PagedKVError):
+        sched.add_request(0, 10, 5, n=5)        # more samples than batch rows
+    assert sched.cow_pairs().shape == (0, 2)
