@@ -76,6 +76,45 @@ def test_decode_validation(lib):
     assert f(*args(desc=_desc(dt=1))) == pkv.PKV_ERR_INVALID_ARG  # fp8 without scales
 
 
+def test_one_call_and_shared_prefix_validation(lib):
+    """pkv_paged_attention returns the decode's error without launching the
+    merge; the shared-prefix call checks its own-part bound and groups."""
+    f = lib.pkv_paged_attention
+    args = lambda **kw: [FAKE, FAKE, FAKE, FAKE, _desc(), None, None, FAKE, 64, FAKE,
+                         kw.get("S", 4), 8, kw.get("maxc", 1024), 0.088, kw.get("P", 512),
+                         kw.get("ws", None), kw.get("wsb", 0), None]
+    assert f(*args(S=0)) == pkv.PKV_OK
+    assert f(*args()) == pkv.PKV_ERR_INVALID_ARG                 # no workspace
+    assert f(*args(P=24)) == pkv.PKV_ERR_INVALID_ARG             # not a multiple of B
+    assert f(*args(maxc=1025)) == pkv.PKV_ERR_INVALID_ARG        # beyond the table
+    g = lib.pkv_paged_attention_decode_shared_prefix
+    sp = lambda **kw: [FAKE, FAKE, FAKE, FAKE, _desc(), FAKE, 64, FAKE, kw.get("S", 4), 8,
+                       kw.get("own", 100), 0.088, FAKE, kw.get("G", 1), FAKE,
+                       kw.get("mp", 2), kw.get("P", 64), kw.get("ws", None), 0, None]
+    assert g(*sp(S=0)) == pkv.PKV_OK
+    assert g(*sp(own=64 * 16 + 1)) == pkv.PKV_ERR_INVALID_ARG    # own part beyond the table
+    assert g(*sp(mp=65)) == pkv.PKV_ERR_INVALID_ARG              # prefix beyond the table
+    assert g(*sp(P=24)) == pkv.PKV_ERR_INVALID_ARG
+    assert g(*sp()) == pkv.PKV_ERR_INVALID_ARG                   # no workspace
+    assert g(*sp(own=-1)) == pkv.PKV_ERR_INVALID_ARG
+    n_own = lib.pkv_shared_prefix_workspace_bytes(4, 8, 128, 100, 32, 64)
+    n_all = lib.pkv_shared_prefix_workspace_bytes(4, 8, 128, 1000, 32, 64)
+    assert n_own == 4 * 8 * (1 + 2) * (128 + 2) * 4 and n_all > n_own
+
+
+def test_scheduler_pair_export_validation(lib):
+    a = pkv.BlockAllocator(16, 4, seed=1)
+    s = pkv.Scheduler(a, 4)
+    s.add_request(0, 6, 3, n=3)                # 6 tokens: the last prompt block half full
+    s.step()
+    n = ctypes.c_int()
+    assert lib.pkv_sched_cow_pairs(s._h, None, 0, ctypes.byref(n)) == pkv.PKV_ERR_INVALID_ARG
+    assert n.value == 2                         # two samples copy, the last writes in place
+    pairs = s.cow_pairs()
+    assert pairs.shape == (2, 2) and len(set(pairs[:, 0].tolist())) == 1
+    assert lib.pkv_sched_cow_pairs(None, None, 0, ctypes.byref(n)) == pkv.PKV_ERR_INVALID_ARG
+
+
 def test_workspace_size(lib):
     # [S][Hq][NP] partial outputs of D floats plus max and sum
     n = pkv.decode_workspace_bytes(8, 24, 256, 131072, 512)
