@@ -81,12 +81,40 @@ def unique_decode_bytes(w) -> int:
     return decode_bytes(w) - sum(w.ctx) * per_tok + tokens * per_tok
 
 
+NOMINAL_HBM_GBS = 8000.0    # GB300 HBM3e, nominal (~8 TB/s)
+
+
 def peaks():
+    """The roofline's HBM peak: the measured copy bandwidth of this machine's
+    GB300s (MEASURED_PEAKS.json), else the profiling fallback of 6.8 TB/s."""
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         d = json.load(open(p))
         return float(d["hbm_gbs"]), "measured"
     return 6800.0, "fallback"
+
+
+def cpu_model() -> str:
+    """The host CPU as /proc/cpuinfo names it (x86: model name; Arm: the
+    implementer and part numbers, with the part's name where known)."""
+    arm_parts = {"0xd4f": "Neoverse-V2", "0xd40": "Neoverse-V1", "0xd0c": "Neoverse-N1",
+                 "0xd49": "Neoverse-N2", "0xd8e": "Neoverse-N3", "0xd84": "Neoverse-V3"}
+    try:
+        info = open("/proc/cpuinfo").read()
+    except OSError:
+        return "unknown"
+    fields = {}
+    for line in info.splitlines():
+        if ":" in line:
+            k, v = line.split(":", 1)
+            fields.setdefault(k.strip(), v.strip())
+    if "model name" in fields:
+        return fields["model name"]
+    imp, part = fields.get("CPU implementer"), fields.get("CPU part")
+    if imp or part:
+        name = arm_parts.get(part, "")
+        return ("Arm implementer %s part %s %s" % (imp, part, name)).strip()
+    return "unknown"
 
 
 def strip_comments(src: str) -> str:
@@ -152,7 +180,7 @@ class ClockSampler:
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.idx), "--query-gpu=" + self.Q,
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=self.fh, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
@@ -194,7 +222,20 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(rows)}
 
 
-def run_reference(args, w, rank):
+def fp8_scales_host(w, layer=0):
+    """Per-KV-head E4M3 scales from every row of every sequence of the layer:
+    fp32 max |x| / 448 (an IEEE fp32 quotient), as the GPU arm's cache uses."""
+    import numpy as np
+    from paged_kv_cache_220_gb300 import synth
+    amax = [np.zeros(w.num_kv_heads, dtype=np.float32) for _ in range(2)]
+    for s in range(w.num_seqs):
+        for i, kind in enumerate((synth.KIND_K, synth.KIND_V)):
+            r = w.rows(kind, layer, s, 0, w.ctx[s], "cpu").float().abs().amax(dim=(0, 2))
+            amax[i] = np.maximum(amax[i], r.numpy())
+    return amax[0] / np.float32(448.0), amax[1] / np.float32(448.0)
+
+
+def run_reference(args, w, rank, single_thread=False):
     """The CPU oracle on a bounded sample of the workload (same metric)."""
     import numpy as np
     import oracle
@@ -214,13 +255,12 @@ def run_reference(args, w, rank):
     q = bits(w.q(0, "cpu"))[seqs]
     ks, vs = [], []
     ksc = vsc = None
+    if w.fp8:
+        ksc, vsc = fp8_scales_host(w, 0)
     for s in seqs:
         K = w.rows(synth.KIND_K, 0, s, 0, w.ctx[s], "cpu")
         V = w.rows(synth.KIND_V, 0, s, 0, w.ctx[s], "cpu")
         if w.fp8:
-            if ksc is None:
-                ksc = (K.float().abs().amax(dim=(0, 2)) / 448.0).numpy()
-                vsc = (V.float().abs().amax(dim=(0, 2)) / 448.0).numpy()
             ks.append(oracle.e4m3_encode_bf16(bits(K), ksc))
             vs.append(oracle.e4m3_encode_bf16(bits(V), vsc))
         else:
@@ -229,29 +269,164 @@ def run_reference(args, w, rank):
     import dataclasses
     sub = dataclasses.replace(w, ctx=[w.ctx[s] for s in seqs])
     sample_bytes = decode_bytes(sub)
-    # the reference arm times K steps; the baseline inside our own line
-    # repeats the sample until about 10 s of CPU work have been timed
-    times = []
-    target_s = 0.0 if args.impl == "reference" else 10.0
-    while True:
-        t0 = time.perf_counter()
+
+    def one():
         if w.fp8:
             oracle.decode(q, ks, vs, w.scale, ksc.astype(np.float64), vsc.astype(np.float64))
         else:
             oracle.decode(q, ks, vs, w.scale)
-        times.append(time.perf_counter() - t0)
-        if args.impl == "reference" and len(times) >= args.steps:
-            break
-        if args.impl != "reference" and (sum(times) >= target_s or len(times) >= 200):
-            break
+
+    def timed(target_s, max_reps, min_reps):
+        times = []
+        while True:
+            t0 = time.perf_counter()
+            one()
+            times.append(time.perf_counter() - t0)
+            if len(times) >= min_reps and (sum(times) >= target_s or len(times) >= max_reps):
+                return times
+
+    # the reference arm times K steps; the baseline inside our own line
+    # repeats the sample until about 10 s of CPU work have been timed
+    cores = oracle.num_threads()
+    if args.impl == "reference":
+        times = timed(0.0, args.steps, args.steps)
+    else:
+        times = timed(10.0, 200, 1)
     t = sum(times) / len(times)
-    gbs = sample_bytes / t / 1e9
-    return {
-        "value": round(gbs, 4), "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
+    out = {
+        "value": round(sample_bytes / t / 1e9, 4), "unit": "GB/s", "cores": cores,
+        "kind": "oracle",
         "sample": "layer 0, sequences %d..%d (%d tokens) of the workload, fp64 C oracle, "
                   "%d repetition(s), %.3f s each" % (seqs[0], seqs[-1], tok, len(times), t),
-        "seconds": round(t, 4),
+        "seconds": round(t, 4), "nproc": os.cpu_count(), "cpu_model": cpu_model(),
     }
+    if single_thread:
+        # the same sample on one thread (at most ~10 s)
+        oracle.set_num_threads(1)
+        try:
+            t1 = timed(5.0, 3, 1)
+        finally:
+            oracle.set_num_threads(cores)
+        t1 = sum(t1) / len(t1)
+        out["single_thread"] = {"value": round(sample_bytes / t1 / 1e9, 4), "unit": "GB/s",
+                                "cores": 1, "seconds": round(t1, 4)}
+    return out
+
+
+def make_step(pw, out, ws, cascade, stream):
+    """One step of the hot path over every layer: the cache write of the new
+    token, then the decode (shared-prefix decode with `cascade`) and, for the
+    split decode, the merge. With ev, events are recorded on `stream` around
+    each layer's decode launch (the roofline's kernel)."""
+    import paged_kv_cache_220_gb300 as pkv
+    w = pw.w
+    P = w.partition_size
+
+    def one_step(ev=None):
+        for layer, st in enumerate(pw.layers):
+            pkv.kv_cache_write(st.k_new, st.v_new, pw.slot_mapping, st.k_cache, st.v_cache,
+                               st.k_scale, st.v_scale)
+            if ev is not None:
+                ev[layer][0].record(stream)
+            if cascade is not None:
+                pkv.paged_attention_shared_prefix(st.q, st.k_cache, st.v_cache, pw.block_tables,
+                                                  pw.context_lens, w.scale,
+                                                  cascade.max_own_context, cascade.group_start,
+                                                  cascade.prefix_blocks,
+                                                  cascade.max_prefix_blocks, P,
+                                                  cascade.max_group_members,
+                                                  out=out[layer], workspace=ws)
+                if ev is not None:
+                    ev[layer][1].record(stream)
+                continue
+            # the decode kernel alone (the roofline's kernel), then the merge
+            pkv.paged_attention_decode(out[layer], st.q, st.k_cache, st.v_cache, pw.block_tables,
+                                       pw.context_lens, w.scale, pw.max_context, P, ws,
+                                       st.k_scale, st.v_scale)
+            if ev is not None:
+                ev[layer][1].record(stream)
+            if P:
+                pkv.paged_attention_reduce(out[layer], ws, pw.context_lens, pw.max_context, P)
+    return one_step
+
+
+def step_launches(pw, cascade):
+    """Kernels of one step: per layer the cache write and the decode, plus the
+    merge of a split decode; the shared-prefix decode is three kernels."""
+    L = len(pw.layers)
+    P = pw.w.partition_size
+    return L * ((4 if cascade is not None else 2) + (1 if P and cascade is None else 0))
+
+
+def measure_other(name, steps=10, warmup=3):
+    """A short run of another workload, for the same JSON line: device-timed
+    step (graph replay) after `warmup` steps, the decode kernel's launch time
+    from an eager pass, clocks sampled during the timed steps."""
+    import torch
+    import paged_kv_cache_220_gb300 as pkv
+    from paged_kv_cache_220_gb300 import workload
+    w = workload_for(name)
+    pw = workload.build(w)
+    L = len(pw.layers)
+    P = w.partition_size
+    out = [torch.empty_like(st.q) for st in pw.layers]
+    ws = pkv.alloc_workspace(w.num_seqs, w.num_heads, w.head_dim, pw.max_context, P) if P else None
+    cascade = None
+    if w.prefix_len > 0 and P and not w.fp8:
+        cascade = workload.prefix_groups(pw)
+        ws = pkv.shared_prefix_workspace(w.num_seqs, w.num_heads, w.head_dim,
+                                         cascade.max_own_context,
+                                         cascade.max_prefix_blocks * w.block_size, P)
+    stream = torch.cuda.current_stream()
+    one_step = make_step(pw, out, ws, cascade, stream)
+    step_bytes = decode_bytes(w) * L
+    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device="cuda") \
+        if step_bytes < 4 * L2_BYTES else None
+    for _ in range(warmup):
+        one_step()
+    evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(L)]
+           for _ in range(steps)]
+    torch.cuda.synchronize()
+    for i in range(steps):
+        if flush is not None:
+            flush.fill_(i & 0xFF)
+        one_step(evs[i])
+    torch.cuda.synchronize()
+    dec_ms = sum(evs[i][l][0].elapsed_time(evs[i][l][1]) for i in range(steps)
+                 for l in range(L)) / (steps * L)
+    graph = workload.capture_step(pw, out, ws, P, groups=cascade)
+    for _ in range(warmup):
+        graph.replay()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+    torch.cuda.synchronize()
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        for i in range(steps):
+            if flush is not None:
+                flush.fill_(i & 0xFF)
+            ev[i][0].record(stream)
+            graph.replay()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+    ms = sum(a.elapsed_time(b) for a, b in ev) / steps
+    peak, peak_kind = peaks()
+    dec_bytes = decode_bytes(w) if cascade is None else unique_decode_bytes(w)
+    achieved = dec_bytes / (dec_ms / 1e3) / 1e9
+    r = {"workload": w.name, "steps": steps, "warmup": warmup, "ms_per_step": round(ms, 4),
+         "value": round(step_bytes / (ms / 1e3) / 1e9, 2), "unit": "GB/s",
+         "roofline": {"kernel": "paged_attention_decode" if cascade is None else
+                      "paged_attention_decode_shared_prefix (3 kernels, unique bytes)",
+                      "achieved": round(achieved, 2), "peak": peak, "peak_kind": peak_kind,
+                      "frac": round(achieved / peak, 4), "bytes_per_launch": dec_bytes,
+                      "launch_ms": round(dec_ms, 5)},
+         "gpu_launches": step_launches(pw, cascade) * steps,
+         "l2": "flushed before every step" if flush is not None else "inputs larger than L2",
+         "clocks": clk.summary()}
+    if w.prefix_len > 0:
+        r["unique_bytes_gbs"] = round(unique_decode_bytes(w) * L / (ms / 1e3) / 1e9, 2)
+        r["unique_frac_of_peak"] = round(unique_decode_bytes(w) * L / (ms / 1e3) / 1e9 / peak, 4)
+    del graph, pw, out, ws
+    torch.cuda.empty_cache()
+    return r
 
 
 def main():
@@ -263,6 +438,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--other-configs", default="mixed,cow2040,long_fp8",
+                    help="comma list of workloads timed briefly (10 steps) after the main one "
+                         "and reported under other_configs ('' for none; 1 GPU only)")
     ap.add_argument("--shared-prefix", type=int, default=1,
                     help="1: workloads with shared prompts use the shared-prefix decode")
     ap.add_argument("--graph", type=int, default=1,
@@ -297,7 +475,8 @@ def main():
                 "ms_per_step": round(cb["seconds"] * 1000, 3), "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
                 "config": {"workload": w.name, "sample": cb["sample"]},
-                "cpu_baseline": {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")},
+                "cpu_baseline": {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample",
+                                                    "nproc", "cpu_model")},
                 "e2e": {"value": cb["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}}
         print(json.dumps(line), flush=True)
@@ -339,33 +518,13 @@ def main():
     cascade = None
     if w.prefix_len > 0 and args.shared_prefix and P and not w.fp8:
         cascade = workload.prefix_groups(pw)
-        ws = pkv.shared_prefix_workspace(w.num_seqs, w.num_heads, w.head_dim, cascade[3],
-                                         cascade[2] * w.block_size, P)
+        ws = pkv.shared_prefix_workspace(w.num_seqs, w.num_heads, w.head_dim,
+                                         cascade.max_own_context,
+                                         cascade.max_prefix_blocks * w.block_size, P)
 
-    def one_step(ev=None):
-        for layer, st in enumerate(pw.layers):
-            pkv.kv_cache_write(st.k_new, st.v_new, pw.slot_mapping, st.k_cache, st.v_cache,
-                               st.k_scale, st.v_scale)
-            if ev is not None:
-                ev[layer][0].record(stream)
-            if cascade is not None:
-                pkv.paged_attention_shared_prefix(st.q, st.k_cache, st.v_cache, pw.block_tables,
-                                                  pw.context_lens, w.scale, cascade[3],
-                                                  cascade[0], cascade[1], cascade[2], P,
-                                                  out=out[layer], workspace=ws)
-                if ev is not None:
-                    ev[layer][1].record(stream)
-                continue
-            # the decode kernel alone (the roofline's kernel), then the merge
-            pkv.paged_attention_decode(out[layer], st.q, st.k_cache, st.v_cache, pw.block_tables,
-                                       pw.context_lens, w.scale, pw.max_context, P, ws,
-                                       st.k_scale, st.v_scale)
-            if ev is not None:
-                ev[layer][1].record(stream)
-            if P:
-                pkv.paged_attention_reduce(out[layer], ws, pw.context_lens, pw.max_context, P)
+    one_step = make_step(pw, out, ws, cascade, stream)
 
-    launches_per_step = L * ((4 if cascade is not None else 2) + (1 if P and cascade is None else 0))
+    launches_per_step = step_launches(pw, cascade)
     for _ in range(args.warmup):
         one_step()
     torch.cuda.synchronize()
@@ -436,14 +595,21 @@ def main():
             dist.destroy_process_group()
         return 0
 
+    other = None
+    if args.other_configs and world == 1:
+        other = {}
+        for name in args.other_configs.split(","):
+            if name and name != args.config:
+                other[name] = measure_other(name)
     peak, peak_kind = peaks()
     dec_bytes = decode_bytes(w) if cascade is None else unique_decode_bytes(w)
     achieved = dec_bytes / (dec_avg_ms / 1e3) / 1e9
     traffic, traffic_note = ncu_traffic(args.config)
     cpu = None
     if not args.no_cpu_baseline and world == 1:
-        cb = run_reference(args, w, rank)
-        cpu = {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")}
+        cb = run_reference(args, w, rank, single_thread=True)
+        cpu = {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample", "nproc",
+                                  "cpu_model", "single_thread")}
     tok_per_s_layer = w.num_seqs * world / (ms_per_step / 1e3 / L)
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": args.gpus,
@@ -463,6 +629,9 @@ def main():
         },
         "eager_ms_per_step": round(eager_ms / K, 4),
         "pct_of_peak": round(100 * value / world / peak, 2),
+        "pct_of_peak_basis": "%s HBM copy bandwidth %.1f GB/s" % (peak_kind, peak),
+        "pct_of_nominal": round(100 * value / world / NOMINAL_HBM_GBS, 2),
+        "pct_of_nominal_basis": "GB300 nominal HBM3e %.0f GB/s" % NOMINAL_HBM_GBS,
         "tokens_per_s_per_layer": round(tok_per_s_layer, 1),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
@@ -472,6 +641,7 @@ def main():
                      "bytes_per_launch": dec_bytes, "launch_ms": round(dec_avg_ms, 5),
                      "traffic": traffic},
         "cpu_baseline": cpu, "e2e": e2e, "copy_blocks": cow_copy, "host": host,
+        "other_configs": other,
         "gpu_launches": launches_per_step * K,
         "clocks": clk.summary(),
     }
@@ -572,7 +742,7 @@ def run_e2e(args, pw, w, out, ws, P, per_step_bytes, world, dist, cascade=None):
     host = [{k: getattr(st, k).cpu().pin_memory() for k in keys} for st in pw.layers]
     meta = [pw.slot_mapping, pw.block_tables, pw.context_lens]
     if cascade is not None:
-        meta += [cascade[0], cascade[1]]
+        meta += [cascade.group_start, cascade.prefix_blocks]
     h_meta = [t.cpu().pin_memory() for t in meta]
     h_out = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in out]
     # two sets of device buffers: step i uses set i % 2
@@ -616,8 +786,10 @@ def run_e2e(args, pw, w, out, ws, P, per_step_bytes, world, dist, cascade=None):
                                st.v_cache, st.k_scale, st.v_scale)
             if cascade is not None:
                 pkv.paged_attention_shared_prefix(dv[layer]["q"], st.k_cache, st.v_cache, d_bt,
-                                                  d_cl, w.scale, cascade[3], dm[3], dm[4],
-                                                  cascade[2], P, out=do[layer], workspace=ws)
+                                                  d_cl, w.scale, cascade.max_own_context, dm[3],
+                                                  dm[4], cascade.max_prefix_blocks, P,
+                                                  cascade.max_group_members, out=do[layer],
+                                                  workspace=ws)
             else:
                 pkv.paged_attention(dv[layer]["q"], st.k_cache, st.v_cache, d_bt, d_cl, w.scale,
                                     pw.max_context, P, st.k_scale, st.v_scale, out=do[layer],

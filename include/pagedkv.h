@@ -204,11 +204,19 @@ int pkv_paged_attention(void* out, const void* q, const void* k_cache,
  * [HowVLLM] "PagedAttention borrows from operating systems"; [Dissect]
  * "PagedAttention: Virtual Memory for KV Cache"). The result is the same
  * attention as pkv_paged_attention_decode; the shared pages are read once per
- * group instead of once per member.
+ * group (per row tile of a large group, below) instead of once per member.
  *
  *   group_start   : device int32 [num_groups + 1]; group i is the sequences
- *                   [group_start[i], group_start[i+1]) of the batch (at most
- *                   128 / g members); sequences outside every group are fine
+ *                   [group_start[i], group_start[i+1]) of the batch;
+ *                   sequences outside every group are fine
+ *   max_group_members : host bound on the members of any group (>= 1 when
+ *                   num_groups > 0, <= num_seqs). A group's query rows
+ *                   (members x g) are covered by tiles of floor(128/g)
+ *                   members; every tile reads the shared pages (adjacent
+ *                   tiles of a partition run together, so the second read
+ *                   of a page is served by L2). A group larger than the
+ *                   bound is reported as PKV_DEVERR_CONTEXT and its uncovered
+ *                   members get their result without the shared part.
  *   prefix_blocks : device int32 [num_seqs]; the number of leading blocks of
  *                   each sequence that are its group's shared prefix: the same
  *                   value and the same physical ids for every member, full
@@ -222,24 +230,42 @@ int pkv_paged_attention(void* out, const void* q, const void* k_cache,
  *                   CTAs with no page (a longer own part is reported as
  *                   PKV_DEVERR_CONTEXT and cut); the other arguments as for
  *                   pkv_paged_attention_decode
- *   partition_size: split size of each member's own part (multiple of
- *                   block_size, at most 2048 blocks); the shared part uses a
- *                   power-of-two multiple of it chosen by the library (enough
- *                   CTAs to cover the SMs, at most 2048 blocks)
- *   workspace     : at least pkv_shared_prefix_workspace_bytes(...) bytes
- * Per group and KV head, a kernel computes partials of every member's query
- * heads over the shared pages (the members' queries form the rows of one
- * tensor-core product); each member's own blocks go through the split decode;
- * the merge combines both. bf16 pools only (PKV_ERR_UNSUPPORTED otherwise).
+ *   partition_size: split size P of each member's own part (multiple of
+ *                   block_size, at most 2048 blocks); the shared part uses
+ *                   partitions of Pp tokens, a power-of-two multiple of P
+ *                   chosen for the current device (the smallest for which the
+ *                   prefix grid fits the SM count, at most 2048 blocks):
+ *                   pkv_shared_prefix_partition_size returns it
+ *   workspace     : at least pkv_shared_prefix_workspace_bytes(...) bytes.
+ *                   Layout (fp32), with NPP = ceil(max_prefix_blocks *
+ *                   block_size / Pp), NPS = ceil(max_own_context / P),
+ *                   NPT = NPP + NPS and R = num_seqs * num_heads rows:
+ *                   tmp_out [R][NPT][head_dim] | max_logits [R][NPT] |
+ *                   exp_sums [R][NPT]. Slot p < NPP of a row holds the shared
+ *                   partition p (tokens [p*Pp, min((p+1)*Pp, prefix tokens))),
+ *                   slot NPP + p the own partition p (tokens from
+ *                   prefix_blocks[s]*block_size + p*P on), in the form of
+ *                   pkv_paged_attention_decode's partials.
+ * Per group, KV head and row tile, a kernel computes partials of the members'
+ * query heads over the shared pages (the members' queries form the rows of
+ * one tensor-core product); each member's own blocks go through the split
+ * decode; the merge combines both. bf16 pools only (PKV_ERR_UNSUPPORTED
+ * otherwise).
  * ------------------------------------------------------------------------ */
 size_t pkv_shared_prefix_workspace_bytes(int num_seqs, int num_heads, int head_dim,
                                          int max_own_context, int max_prefix_tokens,
                                          int partition_size);
+/* Pp, the shared part's partition size that
+ * pkv_paged_attention_decode_shared_prefix uses on the current device for
+ * these arguments (> 0), or a negative pkv_status. */
+int pkv_shared_prefix_partition_size(int num_groups, int max_group_members, int num_kv_heads,
+                                     int num_heads, int block_size, int max_prefix_blocks,
+                                     int partition_size);
 int pkv_paged_attention_decode_shared_prefix(
     void* out, const void* q, const void* k_cache, const void* v_cache,
     pkv_cache_desc cache, const int32_t* block_tables, int max_blocks_per_seq,
     const int32_t* context_lens, int num_seqs, int num_heads, int max_own_context,
-    float scale, const int32_t* group_start, int num_groups,
+    float scale, const int32_t* group_start, int num_groups, int max_group_members,
     const int32_t* prefix_blocks, int max_prefix_blocks, int partition_size,
     void* workspace, size_t workspace_bytes, void* stream);
 
@@ -283,8 +309,9 @@ int pkv_copy_blocks(void* k_cache, void* v_cache, pkv_cache_desc cache,
  *     partition_size or the workspace form), PKV_ERR_INVALID_ARG for
  *     partition_size <= 0, and every error of the two calls it makes.
  *   - The first call on a device looks up the array's device address (with
- *     that device current) and caches it; make that first call before any
- *     stream capture.
+ *     that device current) and caches it per device and context (a new
+ *     context on the device, e.g. after cudaDeviceReset, looks it up again);
+ *     make that first call before any stream capture.
  *   - All calls in the process share the one array and it keeps the last
  *     call's contents; nothing in it needs to start at zero. Calls whose
  *     kernels may overlap on the GPU (other streams, other host threads)
@@ -455,12 +482,16 @@ int pkv_sched_add_request(pkv_scheduler* s, int64_t request_id, int prompt_len,
  * its blocks ([HowVLLM] "PagedAttention borrows from operating systems";
  * [Dissect] "PagedAttention: Virtual Memory for KV Cache": copy-on-write
  * among sequences of one prompt). The samples run as requests request_id,
- * request_id + 1, ..., request_id + n - 1 (keep other requests' ids apart);
+ * request_id + 1, ..., request_id + n - 1;
  * each has the token budget max_new_tokens. A sample that writes into a block
  * still shared gets a copy (pkv_sched_cow_pairs). A preempted sample comes
  * back as a request of its own (recompute: from the prompt; swap: its blocks,
  * shared ones included, are copied out and back into private blocks).
- * PKV_ERR_INVALID_ARG if n < 1 or n > max_num_seqs. */
+ * PKV_ERR_INVALID_ARG if n < 1 or n > max_num_seqs, if request_id < 0, or if
+ * any id in [request_id, request_id + n) belongs to a request that is
+ * waiting (with its samples' ids), running or swapped out (ids of finished
+ * requests may be reused); the same check applies to
+ * pkv_sched_add_request. */
 int pkv_sched_add_request_n(pkv_scheduler* s, int64_t request_id, int prompt_len,
                             int max_new_tokens, int n);
 /* One iteration; reports the batch size, the requests admitted in it and

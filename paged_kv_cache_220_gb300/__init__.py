@@ -75,9 +75,10 @@ SIGNATURES = {
     "pkv_paged_attention_decode_noalloc": (_I, [_P, _P, _P, _P, CacheDesc, _P, _P, _P, _I, _P,
                                                 _I, _I, _I, ctypes.c_float, _I, _P]),
     "pkv_shared_prefix_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I, _I, _I, _I]),
+    "pkv_shared_prefix_partition_size": (_I, [_I, _I, _I, _I, _I, _I, _I]),
     "pkv_paged_attention_decode_shared_prefix": (_I, [_P, _P, _P, _P, CacheDesc, _P, _I, _P, _I,
-                                                      _I, _I, ctypes.c_float, _P, _I, _P, _I,
-                                                      _I, _P, ctypes.c_size_t, _P]),
+                                                      _I, _I, ctypes.c_float, _P, _I, _I, _P,
+                                                      _I, _I, _P, ctypes.c_size_t, _P]),
     "pkv_copy_blocks": (_I, [_P, _P, CacheDesc, _P, _I, _P]),
     "pkv_swap_out": (_I, [_P, _P, CacheDesc, _P, _I, _P, _P, _P]),
     "pkv_swap_in": (_I, [_P, _P, CacheDesc, _P, _I, _P, _P, _P]),
@@ -298,13 +299,26 @@ def shared_prefix_workspace(num_seqs, num_heads, head_dim, max_own_context, max_
     return torch.empty(max(n, 16), dtype=torch.uint8, device=device or "cuda")
 
 
+def shared_prefix_partition_size(num_groups, max_group_members, num_kv_heads, num_heads,
+                                 block_size, max_prefix_blocks, partition_size) -> int:
+    """Pp, the shared part's partition size on the current device."""
+    rc = lib().pkv_shared_prefix_partition_size(int(num_groups), int(max_group_members),
+                                                int(num_kv_heads), int(num_heads),
+                                                int(block_size), int(max_prefix_blocks),
+                                                int(partition_size))
+    if rc < 0:
+        _check(rc, "shared_prefix_partition_size")
+    return int(rc)
+
+
 def paged_attention_shared_prefix(q, k_cache, v_cache, block_tables, context_lens, scale,
                                   max_own_context, group_start, prefix_blocks, max_prefix_blocks,
-                                  partition_size, out=None, workspace=None,
+                                  partition_size, max_group_members, out=None, workspace=None,
                                   stream=None) -> torch.Tensor:
     """Decode of groups sharing prompt blocks (see the C header): shared pages
     are read once per group. group_start int32 [G+1], prefix_blocks int32 [S];
-    max_own_context bounds context_lens[s] - prefix_blocks[s] * block_size."""
+    max_own_context bounds context_lens[s] - prefix_blocks[s] * block_size;
+    max_group_members bounds the members of a group."""
     desc = cache_desc(k_cache)
     S, Hq, D = q.shape
     if out is None:
@@ -320,8 +334,8 @@ def paged_attention_shared_prefix(q, k_cache, v_cache, block_tables, context_len
         _dev_ptr(block_tables, "block_tables", torch.int32), int(block_tables.shape[1]),
         _dev_ptr(context_lens, "context_lens", torch.int32), S, Hq, int(max_own_context),
         float(scale), _dev_ptr(group_start, "group_start", torch.int32), G,
-        _dev_ptr(prefix_blocks, "prefix_blocks", torch.int32), int(max_prefix_blocks),
-        int(partition_size), _dev_ptr(workspace, "workspace"),
+        int(max_group_members), _dev_ptr(prefix_blocks, "prefix_blocks", torch.int32),
+        int(max_prefix_blocks), int(partition_size), _dev_ptr(workspace, "workspace"),
         workspace.numel() * workspace.element_size(), _stream(stream))
     _check(rc, "paged_attention_decode_shared_prefix")
     return out

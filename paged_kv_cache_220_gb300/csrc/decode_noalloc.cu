@@ -12,6 +12,7 @@
 // The array lives in its own translation unit: the CUDA runtime creates it
 // on a device when this file's module is first used there, and it stays
 // until the process exits.
+#include <cuda.h>
 #include <mutex>
 
 #include "host_util.h"
@@ -22,20 +23,50 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[PKV_NOALLOC_SCR
 
 constexpr int kMaxNoallocDevices = 64;
 static std::mutex g_noalloc_mu;
+// per device: the context the address was looked up in, and the address
+static CUcontext g_noalloc_ctx[kMaxNoallocDevices] = {nullptr};
 static void* g_noalloc_ptr[kMaxNoallocDevices] = {nullptr};
 
-// Device address of the scratch array on the current device. In host code
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+
+// cuCtxGetCurrent through the runtime's driver entry-point query (the
+// library links the runtime only).
+static CtxGetCurrentFn ctx_get_current() {
+  static CtxGetCurrentFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<CtxGetCurrentFn>(f);
+  });
+  return fn;
+}
+
+// Device address of the scratch array in the current context. In host code
 // the array's name is only a host-side stand-in, so the address must be
-// asked from the runtime, once per device, with that device current.
+// asked from the runtime, with the device current. It is looked up once per
+// device and context: a new context on the same device (after
+// cudaDeviceReset, or a context the caller made current) loads the module
+// again, so its array has its own address.
 static int noalloc_scratch_address(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
   if (dev < 0 || dev >= kMaxNoallocDevices) return PKV_ERR_UNSUPPORTED;
+  const CtxGetCurrentFn get = ctx_get_current();
+  if (get == nullptr) return PKV_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  if (g_noalloc_ptr[dev] == nullptr) {
+  CUcontext ctx = nullptr;
+  if (get(&ctx) != CUDA_SUCCESS) return PKV_ERR_CUDA;
+  if (ctx == nullptr || ctx != g_noalloc_ctx[dev] || g_noalloc_ptr[dev] == nullptr) {
+    // the lookup makes the runtime's context current if there was none
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
       return PKV_ERR_CUDA;
+    if (get(&ctx) != CUDA_SUCCESS || ctx == nullptr) return PKV_ERR_CUDA;
+    g_noalloc_ctx[dev] = ctx;
     g_noalloc_ptr[dev] = p;
   }
   *out = g_noalloc_ptr[dev];

@@ -39,6 +39,9 @@ struct PrefixParams {
   int group;                      // g = num_heads / num_kv_heads
   int partition_blocks;
   int np_max;                     // slots per (sequence, head) row of the workspace
+  int tiles;                      // row tiles per group (blockIdx.x = partition * tiles + tile)
+  int members_per_tile;           // floor(128 / g)
+  int max_members;                // the caller's bound on a group's members
   float qscale;
 };
 
@@ -122,19 +125,36 @@ __global__ void __launch_bounds__(TmemPrefixGeom<D, BS>::kThreads)
   // this kernel)
   allow_dependents();
 
-  const int part = blockIdx.x, h = blockIdx.y, gi = blockIdx.z;
+  // a group of more than 128 query rows is covered by several row tiles of
+  // members_per_tile members each; the tiles of one partition are adjacent
+  // in the grid, so the second reader of a page finds it in L2
+  const int part = blockIdx.x / p.tiles, tile = blockIdx.x % p.tiles;
+  const int h = blockIdx.y, gi = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = p.group;
-  const int s0 = p.group_start[gi];
-  const int members = p.group_start[gi + 1] - s0;
+  const int sg = p.group_start[gi];
+  const int members_all = p.group_start[gi + 1] - sg;
+  const int s0 = sg + tile * p.members_per_tile;  // this tile's first member
+  const int members = min(members_all - tile * p.members_per_tile, p.members_per_tile);
   const int R = members * g;
-  if (members <= 0 || R > 128) {
-    if (threadIdx.x == 0 && members > 0) report_error(p.err, PKV_DEVERR_CONTEXT);
-    return;
-  }
+  if (members <= 0) return;
   const int pre = min(p.prefix_blocks[s0], p.max_blocks_per_seq);
   const int blk_begin = part * p.partition_blocks;
   if (blk_begin >= pre) return;
+  if (members_all > p.max_members && tile == p.tiles - 1) {
+    // more members than the caller declared: the ones no tile covers get an
+    // empty partial for this partition (the merge then leaves the shared
+    // part out of their result) and the error word says so
+    if (threadIdx.x == 0 && part == 0 && h == 0) report_error(p.err, PKV_DEVERR_CONTEXT);
+    const int first = sg + p.tiles * p.members_per_tile;
+    const int last = sg + members_all;
+    for (int i = threadIdx.x; i < (last - first) * g; i += blockDim.x) {
+      const int64_t hq = static_cast<int64_t>(first + i / g) * p.num_heads + h * g + i % g;
+      p.max_logits[hq * p.np_max + part] = -INFINITY;
+      p.exp_sums[hq * p.np_max + part] = 0.f;
+      for (int c = 0; c < D; ++c) p.tmp_out[(hq * p.np_max + part) * D + c] = 0.f;
+    }
+  }
   const int blk_end = min(pre, blk_begin + p.partition_blocks);
   const int nblk = blk_end - blk_begin;
   const int nsteps = (nblk + NP - 1) / NP;
@@ -404,10 +424,10 @@ template <int D, int BS>
 static int launch_prefix_tmem_t(const PrefixParams& p, const CUtensorMap& tk,
                                 const CUtensorMap& tv, dim3 grid, cudaStream_t st) {
   using G = TmemPrefixGeom<D, BS>;
-  static bool done[64] = {false};
+  static DeviceFlags done;
   auto kern = prefix_tmem_kernel<D, BS>;
   if (p.partition_blocks <= 0 || p.partition_blocks > G::kMaxIds) return PKV_ERR_UNSUPPORTED;
-  int rc = ensure_smem(kern, G::kSmem + 4 * G::kMaxIds, done, 64);
+  int rc = ensure_smem(kern, G::kSmem + 4 * G::kMaxIds, done);
   if (rc != PKV_OK) return rc;
   const int smem = G::kSmem + ((4 * p.partition_blocks + 15) & ~15);
   kern<<<grid, G::kThreads, smem, st>>>(tk, tv, p);
@@ -430,6 +450,43 @@ int launch_prefix(const PrefixParams& p, const void* k_cache, const void* v_cach
 
 }  // namespace pkv
 
+namespace pkv {
+
+constexpr int kMaxPrefixPartitionBlocks = 2048;  // block ids a prefix CTA holds
+
+// Partition size of the shared pages: Pp >= P, a power-of-two multiple of P,
+// the smallest for which the prefix grid (partitions x row tiles x KV heads x
+// groups) is no larger than the SM count (one prefix CTA fits per SM), so
+// each CTA's set-up (query tile, tensor memory) and epilogue are spread over
+// more pages (measured on GB300 with 2040-token prompts: Pp = 512 / 1024 /
+// 2048 gave a 0.380 / 0.342 / 0.330 ms step). Returns Pp or a pkv_status.
+static int prefix_partition_size(int sms, int num_groups, int tiles, int num_kv_heads,
+                                 int block_size, int max_prefix_blocks, int partition_size) {
+  if (partition_size / block_size > kMaxPrefixPartitionBlocks) return PKV_ERR_UNSUPPORTED;
+  const int pre_tokens = max_prefix_blocks * block_size;
+  int pre_p = partition_size;
+  while (pre_p < pre_tokens && 2 * pre_p / block_size <= kMaxPrefixPartitionBlocks &&
+         static_cast<int64_t>((pre_tokens + pre_p - 1) / pre_p) * tiles * num_kv_heads *
+                 num_groups > sms)
+    pre_p *= 2;
+  return pre_p;
+}
+
+static int tiles_for(int max_group_members, int g) {
+  const int per = 128 / g;
+  return (max_group_members + per - 1) / per;
+}
+
+static int device_sms(int* sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return PKV_ERR_CUDA;
+  return PKV_OK;
+}
+
+}  // namespace pkv
+
 extern "C" size_t pkv_shared_prefix_workspace_bytes(int num_seqs, int num_heads, int head_dim,
                                                     int max_own_context, int max_prefix_tokens,
                                                     int partition_size) {
@@ -441,12 +498,29 @@ extern "C" size_t pkv_shared_prefix_workspace_bytes(int num_seqs, int num_heads,
   return static_cast<size_t>(num_seqs) * num_heads * (npp + nps) * (head_dim + 2) * sizeof(float);
 }
 
+extern "C" int pkv_shared_prefix_partition_size(int num_groups, int max_group_members,
+                                                int num_kv_heads, int num_heads, int block_size,
+                                                int max_prefix_blocks, int partition_size) {
+  using namespace pkv;
+  if (num_groups < 0 || max_group_members <= 0 || num_kv_heads <= 0 || num_heads <= 0 ||
+      num_heads % num_kv_heads != 0 || (block_size != 16 && block_size != 32) ||
+      max_prefix_blocks < 0 || partition_size <= 0 || partition_size % block_size != 0)
+    return PKV_ERR_INVALID_ARG;
+  const int g = num_heads / num_kv_heads;
+  if (g > 8) return PKV_ERR_UNSUPPORTED;
+  int sms = 0;
+  const int rc = device_sms(&sms);
+  if (rc != PKV_OK) return rc;
+  return prefix_partition_size(sms, num_groups, tiles_for(max_group_members, g), num_kv_heads,
+                               block_size, max_prefix_blocks, partition_size);
+}
+
 extern "C" int pkv_paged_attention_decode_shared_prefix(
     void* out, const void* q, const void* k_cache, const void* v_cache, pkv_cache_desc cache,
     const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
     int num_seqs, int num_heads, int max_own_context, float scale, const int32_t* group_start,
-    int num_groups, const int32_t* prefix_blocks, int max_prefix_blocks, int partition_size,
-    void* workspace, size_t workspace_bytes, void* stream) {
+    int num_groups, int max_group_members, const int32_t* prefix_blocks, int max_prefix_blocks,
+    int partition_size, void* workspace, size_t workspace_bytes, void* stream) {
   using namespace pkv;
   int rc = check_cache_desc(cache);
   if (rc != PKV_OK) return rc;
@@ -454,6 +528,7 @@ extern "C" int pkv_paged_attention_decode_shared_prefix(
   if (num_seqs < 0 || num_heads <= 0 || max_own_context < 0 || max_blocks_per_seq <= 0 ||
       num_groups < 0 || max_prefix_blocks < 0 || partition_size <= 0)
     return PKV_ERR_INVALID_ARG;
+  if (num_groups > 0 && max_group_members <= 0) return PKV_ERR_INVALID_ARG;
   if (num_heads % cache.num_kv_heads != 0) return PKV_ERR_INVALID_ARG;
   const int g = num_heads / cache.num_kv_heads;
   if (g > 8) return PKV_ERR_UNSUPPORTED;
@@ -463,6 +538,7 @@ extern "C" int pkv_paged_attention_decode_shared_prefix(
       max_prefix_blocks > max_blocks_per_seq)
     return PKV_ERR_INVALID_ARG;
   if (num_seqs == 0) return PKV_OK;
+  if (num_groups > 0 && max_group_members > num_seqs) return PKV_ERR_INVALID_ARG;
   if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens || !prefix_blocks ||
       (num_groups > 0 && !group_start))
     return PKV_ERR_INVALID_ARG;
@@ -479,30 +555,18 @@ extern "C" int pkv_paged_attention_decode_shared_prefix(
                                                         max_prefix_blocks * cache.block_size,
                                                         partition_size);
   if (!workspace || !aligned16(workspace) || workspace_bytes < need) return PKV_ERR_INVALID_ARG;
-  // The shared pages are split in partitions of Pp >= P tokens (a power-of-two
-  // multiple of P): no more CTAs than SMs (one fits per SM), so each CTA's
-  // set-up (query tile, tensor memory) and epilogue are spread over more pages
-  // (measured on GB300 with 2040-token prompts: Pp = 512 / 1024 / 2048 gave a
-  // 0.380 / 0.342 / 0.330 ms step).
   const int pre_tokens = max_prefix_blocks * cache.block_size;
+  const int tiles = num_groups > 0 ? tiles_for(max_group_members, g) : 1;
   int sms = 0;
-  {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-      return PKV_ERR_CUDA;
-  }
-  constexpr int kMaxPrefixPartitionBlocks = 2048;  // block ids a prefix CTA holds
-  if (partition_size / cache.block_size > kMaxPrefixPartitionBlocks) return PKV_ERR_UNSUPPORTED;
-  int pre_p = partition_size;
-  while (pre_p < pre_tokens && 2 * pre_p / cache.block_size <= kMaxPrefixPartitionBlocks &&
-         static_cast<int64_t>((pre_tokens + pre_p - 1) / pre_p) * cache.num_kv_heads * num_groups >
-             sms)
-    pre_p *= 2;
+  rc = device_sms(&sms);
+  if (rc != PKV_OK) return rc;
+  const int pre_p = prefix_partition_size(sms, num_groups, tiles, cache.num_kv_heads,
+                                          cache.block_size, max_prefix_blocks, partition_size);
+  if (pre_p < 0) return pre_p;
   const int npp = pre_tokens > 0 ? (pre_tokens + pre_p - 1) / pre_p : 0;
   const int nps = (maxc + partition_size - 1) / partition_size;
   const int npt = npp + nps;
-  if (npt > 65535) return PKV_ERR_UNSUPPORTED;
+  if (npt > 65535 || static_cast<int64_t>(npp) * tiles > 65535) return PKV_ERR_UNSUPPORTED;
   float* ws = static_cast<float*>(workspace);
   const int64_t rows = static_cast<int64_t>(num_seqs) * num_heads * npt;
   float* tmp = ws;
@@ -527,9 +591,12 @@ extern "C" int pkv_paged_attention_decode_shared_prefix(
     pp.group = g;
     pp.partition_blocks = pre_p / cache.block_size;
     pp.np_max = npt;
+    pp.tiles = tiles;
+    pp.members_per_tile = 128 / g;
+    pp.max_members = max_group_members;
     pp.qscale = scale * 1.4426950408889634f;
     rc = launch_prefix(pp, k_cache, v_cache, cache.head_dim, cache.block_size,
-                       dim3(npp, cache.num_kv_heads, num_groups), st);
+                       dim3(npp * tiles, cache.num_kv_heads, num_groups), st);
     if (rc != PKV_OK) return rc;
   }
   // 2. each sequence's own blocks past its group's prefix: the split decode

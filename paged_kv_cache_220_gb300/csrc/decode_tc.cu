@@ -545,9 +545,9 @@ static int launch_tc(const DecodeParams& p_in, const void* k_cache, const void* 
   if (rc != PKV_OK) return rc;
   rc = pool_tensor_map(&tv, v_cache, rows, D, BS, FP8, true);
   if (rc != PKV_OK) return rc;
-  static bool done[64] = {false};
+  static DeviceFlags done;
   auto kern = decode_tc_kernel<D, BS, FP8, NW, NST, UPB>;
-  rc = ensure_smem(kern, G::kSmem, done, 64);
+  rc = ensure_smem(kern, G::kSmem, done);
   if (rc != PKV_OK) return rc;
   DecodeParams p = p_in;
   if (p.partition_blocks > 0 || p.cluster <= 1) {
@@ -559,14 +559,14 @@ static int launch_tc(const DecodeParams& p_in, const void* k_cache, const void* 
   p.overlap_prev = 0;
   // One pass: a cluster of C CTAs per (KV head, sequence), C a power of two
   // <= 16; shrink C if the device cannot co-schedule clusters that large.
-  static bool nonportable[64] = {false};
+  static DeviceFlags nonportable;
   int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 64 && !nonportable[dev]) {
+  if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
+  if (dev >= 0 && dev < kMaxFlagDevices && !nonportable[dev].load(std::memory_order_acquire)) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
         cudaSuccess)
       return PKV_ERR_CUDA;
-    nonportable[dev] = true;
+    nonportable[dev].store(true, std::memory_order_release);
   }
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
@@ -579,7 +579,7 @@ static int launch_tc(const DecodeParams& p_in, const void* k_cache, const void* 
   // Largest cluster size <= the requested one that the device can co-schedule
   // with this kernel's resources, asked once per device and size (so calls
   // made during stream capture do no occupancy queries).
-  static int8_t fits[64][5] = {};  // 0 unknown, 1 yes, -1 no; index log2(C)
+  static std::atomic<int8_t> fits[64][5] = {};  // 0 unknown, 1 yes, -1 no; index log2(C)
   for (int C = p.cluster; C >= 2; C >>= 1) {
     int lg = 0;
     while ((1 << lg) < C) ++lg;

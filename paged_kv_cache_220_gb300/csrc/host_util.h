@@ -1,6 +1,7 @@
 // Host-side argument checks shared by the C entry points.
 #pragma once
 
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
 #include <cuda_runtime.h>
@@ -54,16 +55,23 @@ inline int launch_dependent(void (*kern)(Params...), dim3 grid, dim3 block, size
   return launch_status();
 }
 
+// Per-device flags of one-time set-up steps, safe to read and set from
+// several host threads (two first calls may both do the set-up; every step
+// guarded this way is idempotent).
+using DeviceFlags = std::atomic<bool>[64];
+constexpr int kMaxFlagDevices = 64;
+
 // Raise a kernel's dynamic shared-memory limit once per device.
 template <typename Kernel>
-inline int ensure_smem(Kernel k, size_t bytes, bool* done_per_device, int max_devices) {
+inline int ensure_smem(Kernel k, size_t bytes, DeviceFlags& done) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
-  if (dev < max_devices && done_per_device[dev]) return PKV_OK;
+  if (dev >= 0 && dev < kMaxFlagDevices && done[dev].load(std::memory_order_acquire))
+    return PKV_OK;
   if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(bytes)) != cudaSuccess)
     return PKV_ERR_CUDA;
-  if (dev < max_devices) done_per_device[dev] = true;
+  if (dev >= 0 && dev < kMaxFlagDevices) done[dev].store(true, std::memory_order_release);
   return PKV_OK;
 }
 

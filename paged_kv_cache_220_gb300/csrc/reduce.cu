@@ -254,15 +254,15 @@ int launch_reduce(void* out, const float* tmp, const float* ml, const float* es,
   if (smem > kMaxSmem) return PKV_ERR_UNSUPPORTED;
   const dim3 grid(num_heads, num_seqs, head_dim / 128);
   if (head_dim == 128) {
-    static bool done[64] = {false};
-    int rc = ensure_smem(reduce_kernel<128, 16>, kMaxSmem, done, 64);
+    static DeviceFlags done;
+    int rc = ensure_smem(reduce_kernel<128, 16>, kMaxSmem, done);
     if (rc != PKV_OK) return rc;
     return launch_dependent(reduce_kernel<128, 16>, grid, dim3(16 * 32), smem, st, o, tmp, ml, es,
                             context_lens, num_heads, np_max, partition_size, prefix_blocks,
                             block_size, slot_split, pp, err);
   } else {
-    static bool done[64] = {false};
-    int rc = ensure_smem(reduce_kernel<256, 16>, kMaxSmem, done, 64);
+    static DeviceFlags done;
+    int rc = ensure_smem(reduce_kernel<256, 16>, kMaxSmem, done);
     if (rc != PKV_OK) return rc;
     return launch_dependent(reduce_kernel<256, 16>, grid, dim3(16 * 32), smem, st, o, tmp, ml, es,
                             context_lens, num_heads, np_max, partition_size, prefix_blocks,

@@ -31,6 +31,7 @@
 // back) and continues where it stopped; nothing is recomputed.
 // EOS is a request's own token budget (max_new_tokens), known up front.
 #include <algorithm>
+#include <climits>
 #include <cstdint>
 #include <deque>
 #include <new>
@@ -106,9 +107,31 @@ extern "C" int pkv_sched_create(pkv_allocator* alloc, int block_size, int max_nu
 
 extern "C" void pkv_sched_destroy(pkv_scheduler* s) { delete s; }
 
+namespace {
+
+// Whether an id in [lo, hi) belongs to a request that is waiting (with its
+// samples' ids), running or swapped out. Finished ids may be reused.
+bool ids_in_use(const pkv_scheduler* s, int64_t lo, int64_t hi) {
+  auto hit = [lo, hi](int64_t a, int64_t b) { return a < hi && lo < b; };
+  for (const Req& r : s->waiting)
+    if (hit(r.id, r.id + std::max(1, r.samples))) return true;
+  for (const Req& r : s->running)
+    if (hit(r.id, r.id + 1)) return true;
+  for (const Req& r : s->swapped)
+    if (hit(r.id, r.id + 1)) return true;
+  return false;
+}
+
+}  // namespace
+
 extern "C" int pkv_sched_add_request_n(pkv_scheduler* s, int64_t request_id, int prompt_len,
                                        int max_new_tokens, int n) {
   if (!s || prompt_len < 0 || max_new_tokens <= 0 || n < 1 || n > s->max_num_seqs)
+    return PKV_ERR_INVALID_ARG;
+  // the samples take ids request_id .. request_id + n - 1: none may be taken
+  // by a live request (the lookups by id would then find the wrong one)
+  if (request_id < 0 || request_id > INT64_MAX - n ||
+      ids_in_use(s, request_id, request_id + n))
     return PKV_ERR_INVALID_ARG;
   try {
     s->waiting.push_back(Req{request_id, prompt_len, max_new_tokens, 0, -1, {}, {}, n});

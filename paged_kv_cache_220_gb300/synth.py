@@ -85,11 +85,31 @@ def normal_table(device="cpu") -> torch.Tensor:
     return _TABLES[key]
 
 
+def mix64_inplace_(z: torch.Tensor) -> torch.Tensor:
+    """mix64_tensor without the gamma step, computed in place on z (one
+    scratch tensor instead of a temporary per operation; used for the large
+    host-side streams of the parity tests)."""
+    t = torch.empty_like(z)
+    for sh, c in ((30, _C1), (27, _C2)):
+        torch.bitwise_right_shift(z, sh, out=t)
+        t.bitwise_and_((1 << (64 - sh)) - 1)
+        z.bitwise_xor_(t)
+        z.mul_(_signed(c))
+    torch.bitwise_right_shift(z, 31, out=t)
+    t.bitwise_and_((1 << 33) - 1)
+    return z.bitwise_xor_(t)
+
+
 def normal_bf16(key: int, n: int, offset: int = 0, device="cpu") -> torch.Tensor:
     """n bf16 values of stream `key`, elements offset .. offset+n-1."""
-    idx = torch.arange(n, dtype=torch.int64, device=device) + (key + offset)
-    z = mix64_tensor(idx)
-    return normal_table(device)[_lsr(z, 48)]
+    # counter + gamma: key < 2^62 and the signed gamma is negative, so the
+    # sum stays inside int64 without wrapping
+    z = torch.arange(n, dtype=torch.int64, device=device)
+    z.add_(key + offset + _signed(_GAMMA))
+    mix64_inplace_(z)
+    z.bitwise_right_shift_(48)
+    z.bitwise_and_(0xFFFF)
+    return normal_table(device)[z]
 
 
 def uniform01(key: int, i: int) -> float:

@@ -16,7 +16,7 @@ written.
 from __future__ import annotations
 
 from dataclasses import dataclass, field
-from typing import List, Optional
+from typing import List, NamedTuple, Optional
 
 import numpy as np
 import torch
@@ -77,7 +77,10 @@ def fp8_scales(w: synth.Workload, layer: int, device) -> tuple:
             r = w.rows(kind, layer, s, 0, w.ctx[s], device).float().abs()
             m = torch.maximum(m, r.amax(dim=(0, 2)))
         amax.append(m)
-    return amax[0] / 448.0, amax[1] / 448.0
+    # an IEEE fp32 quotient (a tensor divisor: torch turns division by a
+    # Python scalar into a product with its rounded reciprocal)
+    d = torch.full_like(amax[0], 448.0)
+    return torch.div(amax[0], d), torch.div(amax[1], d)
 
 
 def build(w: synth.Workload, device="cuda", layers: Optional[int] = None,
@@ -385,20 +388,27 @@ class ContinuousBatch:
         return ids, ctx, out
 
 
-def prefix_groups(pw: PagedWorkload, device="cuda"):
-    """Group metadata of a shared-prefix workload: (group_start int32 [G+1],
-    prefix_blocks int32 [S], max_prefix_blocks, max_own_context). The shared
-    prefix of a group is the run of leading full blocks whose physical ids
-    every member's table has in common (a partly filled prompt block is
-    cloned on divergence and so is private); max_own_context is the longest
-    context past its sequence's shared prefix."""
+class PrefixGroups(NamedTuple):
+    group_start: torch.Tensor       # int32 [G + 1] (device)
+    prefix_blocks: torch.Tensor     # int32 [S] (device)
+    max_prefix_blocks: int
+    max_own_context: int
+    max_group_members: int
+
+
+def prefix_groups(pw: PagedWorkload, device="cuda") -> PrefixGroups:
+    """Group metadata of a shared-prefix workload. The shared prefix of a
+    group is the run of leading full blocks whose physical ids every member's
+    table has in common (a partly filled prompt block is cloned on divergence
+    and so is private); max_own_context is the longest context past its
+    sequence's shared prefix; max_group_members the largest group."""
     w = pw.w
     S = w.num_seqs
     ctx = np.asarray(w.ctx, dtype=np.int64)
     if w.prefix_len <= 0:
-        return (torch.zeros(1, dtype=torch.int32, device=device),
-                torch.zeros(S, dtype=torch.int32, device=device), 0,
-                int(ctx.max()) if S else 0)
+        return PrefixGroups(torch.zeros(1, dtype=torch.int32, device=device),
+                            torch.zeros(S, dtype=torch.int32, device=device), 0,
+                            int(ctx.max()) if S else 0, 1)
     G = w.group
     n_prompt = S // G
     tables = pw.tables_host
@@ -412,22 +422,23 @@ def prefix_groups(pw: PagedWorkload, device="cuda"):
         pre[p * G:(p + 1) * G] = k
     starts = np.arange(0, n_prompt * G + 1, G, dtype=np.int32)
     own = ctx - pre.astype(np.int64) * w.block_size
-    return (torch.as_tensor(starts, device=device), torch.as_tensor(pre, device=device),
-            int(pre.max()) if S else 0, int(own.max()) if S else 0)
+    return PrefixGroups(torch.as_tensor(starts, device=device), torch.as_tensor(pre, device=device),
+                        int(pre.max()) if S else 0, int(own.max()) if S else 0, G)
 
 
 def step_shared_prefix(pw: PagedWorkload, out: List[torch.Tensor], groups, workspace,
                        partition_size: Optional[int] = None, stream=None) -> None:
     """One decode step over every layer with the shared-prefix decode."""
     P = pw.w.partition_size if partition_size is None else partition_size
-    gs, pre, maxpre, max_own = groups
     for layer, st in enumerate(pw.layers):
         pkv.kv_cache_write(st.k_new, st.v_new, pw.slot_mapping, st.k_cache, st.v_cache,
                            st.k_scale, st.v_scale, stream)
         pkv.paged_attention_shared_prefix(st.q, st.k_cache, st.v_cache, pw.block_tables,
-                                          pw.context_lens, pw.w.scale, max_own, gs, pre,
-                                          maxpre, P, out=out[layer], workspace=workspace,
-                                          stream=stream)
+                                          pw.context_lens, pw.w.scale, groups.max_own_context,
+                                          groups.group_start, groups.prefix_blocks,
+                                          groups.max_prefix_blocks, P,
+                                          groups.max_group_members, out=out[layer],
+                                          workspace=workspace, stream=stream)
 
 
 # ---- several GPUs: sequences are independent, so every rank runs its own

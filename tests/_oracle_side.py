@@ -30,17 +30,57 @@ def host_rows(w: synth.Workload, layer: int, s: int, t1: int = None):
             w.rows(synth.KIND_V, layer, s, 0, t1, "cpu"))
 
 
+class RowCache:
+    """Host rows of one layer, the shared prompt rows of a shared-prefix
+    workload generated once per prompt instead of once per member."""
+
+    def __init__(self, w: synth.Workload, layer: int):
+        self.w, self.layer = w, layer
+        self.prompts = {}
+
+    def rows(self, s: int):
+        """(K, V) bf16 [ctx_s, Hk, d] of sequence s."""
+        w = self.w
+        if w.prefix_len <= 0:
+            return host_rows(w, self.layer, s)
+        p = s // w.group
+        if p not in self.prompts:
+            self.prompts = {p: host_rows(w, self.layer, p * w.group, w.prefix_len)}
+        pk, pv = self.prompts[p]
+        t1 = w.ctx[s]
+        if t1 <= w.prefix_len:
+            return pk[:t1], pv[:t1]
+        k = w.rows(synth.KIND_K, self.layer, s, w.prefix_len, t1, "cpu")
+        v = w.rows(synth.KIND_V, self.layer, s, w.prefix_len, t1, "cpu")
+        return torch.cat([pk, k]), torch.cat([pv, v])
+
+
+def host_fp8_scales(w: synth.Workload, layer: int, rows=None):
+    """Per-KV-head E4M3 scales computed on the host: the fp32 maximum of |x|
+    over every logical row of every sequence of the layer (history and the
+    new token), divided by 448 in fp32. `rows(s)` may supply the rows."""
+    amax_k = np.zeros(w.num_kv_heads, dtype=np.float32)
+    amax_v = np.zeros(w.num_kv_heads, dtype=np.float32)
+    for s in range(w.num_seqs):
+        K, V = rows(s) if rows is not None else host_rows(w, layer, s)
+        amax_k = np.maximum(amax_k, K.float().abs().amax(dim=(0, 2)).numpy())
+        amax_v = np.maximum(amax_v, V.float().abs().amax(dim=(0, 2)).numpy())
+    return amax_k / np.float32(448.0), amax_v / np.float32(448.0)
+
+
 def quantize(rows_bf16: torch.Tensor, scale: np.ndarray) -> np.ndarray:
     """E4M3 codes of x / scale[h] (fp32 quotient) with the oracle's encoder."""
     return oracle.e4m3_encode_bf16(bits16(rows_bf16), scale)
 
 
-def expected(w: synth.Workload, layer: int, seqs, k_scale=None, v_scale=None) -> np.ndarray:
-    """fp64 oracle output [len(seqs), Hq, D] for the given sequences."""
+def expected(w: synth.Workload, layer: int, seqs, k_scale=None, v_scale=None,
+             rows=None) -> np.ndarray:
+    """fp64 oracle output [len(seqs), Hq, D] for the given sequences.
+    `rows(s)` may supply the host rows (e.g. RowCache(w, layer).rows)."""
     q = bits16(w.q(layer, "cpu"))[list(seqs)]
     ks, vs = [], []
     for s in seqs:
-        K, V = host_rows(w, layer, s)
+        K, V = rows(s) if rows is not None else host_rows(w, layer, s)
         if w.fp8:
             ks.append(quantize(K, k_scale))
             vs.append(quantize(V, v_scale))

@@ -89,9 +89,11 @@ def test_one_call_and_shared_prefix_validation(lib):
     assert f(*args(maxc=1025)) == pkv.PKV_ERR_INVALID_ARG        # beyond the table
     g = lib.pkv_paged_attention_decode_shared_prefix
     sp = lambda **kw: [FAKE, FAKE, FAKE, FAKE, _desc(), FAKE, 64, FAKE, kw.get("S", 4), 8,
-                       kw.get("own", 100), 0.088, FAKE, kw.get("G", 1), FAKE,
+                       kw.get("own", 100), 0.088, FAKE, kw.get("G", 1), kw.get("mm", 4), FAKE,
                        kw.get("mp", 2), kw.get("P", 64), kw.get("ws", None), 0, None]
     assert g(*sp(S=0)) == pkv.PKV_OK
+    assert g(*sp(mm=0)) == pkv.PKV_ERR_INVALID_ARG               # groups need a member bound
+    assert g(*sp(mm=5)) == pkv.PKV_ERR_INVALID_ARG               # more members than sequences
     assert g(*sp(own=64 * 16 + 1)) == pkv.PKV_ERR_INVALID_ARG    # own part beyond the table
     assert g(*sp(mp=65)) == pkv.PKV_ERR_INVALID_ARG              # prefix beyond the table
     assert g(*sp(P=24)) == pkv.PKV_ERR_INVALID_ARG
@@ -100,6 +102,10 @@ def test_one_call_and_shared_prefix_validation(lib):
     n_own = lib.pkv_shared_prefix_workspace_bytes(4, 8, 128, 100, 32, 64)
     n_all = lib.pkv_shared_prefix_workspace_bytes(4, 8, 128, 1000, 32, 64)
     assert n_own == 4 * 8 * (1 + 2) * (128 + 2) * 4 and n_all > n_own
+    q = lib.pkv_shared_prefix_partition_size
+    assert q(1, 0, 2, 8, 16, 4, 64) == pkv.PKV_ERR_INVALID_ARG    # no member bound
+    assert q(1, 4, 2, 8, 16, 4, 24) == pkv.PKV_ERR_INVALID_ARG    # P not a multiple of B
+    assert q(1, 4, 2, 18, 16, 4, 64) == pkv.PKV_ERR_UNSUPPORTED   # group 9
 
 
 def test_scheduler_pair_export_validation(lib):

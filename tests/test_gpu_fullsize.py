@@ -1,18 +1,30 @@
 """Parity at the full workload sizes, in the launch configuration the
 benchmark times (split decode + reduce, every layer; the shared-prefix decode
-replayed from a CUDA graph for the copy-on-write rollouts). The oracle checks a
-seeded sample of sequences one by one; copy-on-write clones are checked bit
-for bit."""
+replayed from a CUDA graph for the copy-on-write rollouts).
+
+Every output of a whole layer is compared with the oracle: all 64 sequences
+of layer 0 of the Qwen-like batch (plus 4 sampled sequences of each other
+layer), all 256 mixed-length sequences, all 512 rollouts of both
+copy-on-write variants (through the plain split decode and through the
+shared-prefix decode), and all 8 long FP8 sequences. The cache writes of
+layer 0 of the Qwen-like batch and of the FP8 batch are checked bit for bit
+over the whole pool, and the FP8 scales are recomputed on the host from the
+host rows. Host rows come from the seeded generator; nothing but the outputs
+under test is read back from the device."""
 import numpy as np
 import pytest
 import torch
 
+import oracle
 import paged_kv_cache_220_gb300 as pkv
 from paged_kv_cache_220_gb300 import build as pkv_build
 from paged_kv_cache_220_gb300 import synth, workload
-from _oracle_side import assert_close, bits16, expected, host_rows, quantize
+from _oracle_side import (RowCache, assert_close, bits16, expected, host_fp8_scales, host_rows,
+                          quantize)
 
 pytestmark = pytest.mark.gpu
+
+CHUNK = 16      # sequences per oracle call (bounds host memory)
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -36,7 +48,50 @@ def _step(pw):
 
 def _sample(n, k, seed):
     rng = np.random.default_rng(seed)
-    return sorted(set([0, n - 1] + rng.choice(n, size=k, replace=False).tolist()))
+    return sorted(set(rng.choice(n, size=k, replace=False).tolist()))
+
+
+def _check_all(got, w, layer, rows, what, k_scale=None, v_scale=None, seqs=None):
+    """Compare every sequence (or `seqs`) of got [S, Hq, D] with the oracle,
+    CHUNK sequences per oracle call."""
+    seqs = list(range(w.num_seqs)) if seqs is None else list(seqs)
+    for i in range(0, len(seqs), CHUNK):
+        part = seqs[i:i + CHUNK]
+        ref = expected(w, layer, part, k_scale, v_scale, rows=rows)
+        assert_close(got[part], ref, "%s seqs %d..%d" % (what, part[0], part[-1]))
+
+
+def _pool_image(w, layer, pw, rows, num_blocks, k_scale=None, v_scale=None):
+    """Expected (K, V) pool images of a layer: every logical row of every
+    sequence at its slot (the oracle's scatter)."""
+    dt = np.uint8 if w.fp8 else np.uint16
+    shape = (num_blocks, w.num_kv_heads, w.block_size, w.head_dim)
+    pk, pv = np.zeros(shape, dtype=dt), np.zeros(shape, dtype=dt)
+    for s in range(w.num_seqs):
+        K, V = rows(s)
+        if w.fp8:
+            k, v = quantize(K, k_scale), quantize(V, v_scale)
+        else:
+            k, v = bits16(K), bits16(V)
+        oracle.scatter_rows_fast(pk, k, pw.history_slots[s])
+        oracle.scatter_rows_fast(pv, v, pw.history_slots[s])
+    return pk, pv
+
+
+def _memo(fn):
+    """Rows of a sequence generated once (the whole-layer checks read each
+    sequence's rows twice: the oracle, then the pool image)."""
+    cache = {}
+
+    def get(s):
+        if s not in cache:
+            cache[s] = fn(s)
+        return cache[s]
+    return get
+
+
+def _pool_bits(t):
+    return t.cpu().numpy() if t.dtype == torch.uint8 else bits16(t)
 
 
 def test_qwen_like_16_layers(_lib):
@@ -44,11 +99,19 @@ def test_qwen_like_16_layers(_lib):
     pw = workload.build(w)
     assert pw.alloc.stats()["free_blocks"] == 0          # the pool fits exactly
     out = _step(pw)
-    for layer in range(w.layers):
-        seqs = _sample(w.num_seqs, 4, layer) if layer == 0 else [(5 * layer) % w.num_seqs]
-        ref = expected(w, layer, seqs)
-        assert_close(out[layer][seqs], ref, "layer %d" % layer)
     assert int(_lib.item()) == 0
+    # layer 0: every sequence, and the whole pool after the step's write
+    rows = _memo(RowCache(w, 0).rows)
+    _check_all(out[0], w, 0, rows, "layer 0")
+    st = pw.layers[0]
+    pk, pv = _pool_image(w, 0, pw, rows, st.k_cache.shape[0])
+    assert np.array_equal(_pool_bits(st.k_cache), pk), "layer 0 K pool"
+    del pk
+    assert np.array_equal(_pool_bits(st.v_cache), pv), "layer 0 V pool"
+    del pv
+    for layer in range(1, w.layers):
+        seqs = _sample(w.num_seqs, 4, layer)
+        _check_all(out[layer], w, layer, None, "layer %d" % layer, seqs=seqs)
     del pw
     torch.cuda.empty_cache()
 
@@ -57,10 +120,8 @@ def test_mixed_lengths(_lib):
     w = synth.mixed()
     pw = workload.build(w)
     out = _step(pw)[0]
-    order = np.argsort(w.ctx)
-    seqs = sorted(set(order[:4].tolist() + order[-4:].tolist() + _sample(w.num_seqs, 24, 3)))
-    assert_close(out[seqs], expected(w, 0, seqs), "mixed")
     assert int(_lib.item()) == 0
+    _check_all(out, w, 0, None, "mixed")
 
 
 @pytest.mark.parametrize("prompt_len", [2048, 2040])
@@ -68,51 +129,57 @@ def test_cow_rollouts(prompt_len, _lib):
     w = synth.cow(prompt_len=prompt_len)
     pw = workload.build(w)
     pairs = pw.cow_pairs_host
+    rows = RowCache(w, 0).rows
     if prompt_len % w.block_size == 0:
         assert pairs is None or len(pairs) == 0
     else:
         assert len(pairs) == 32 * 15
-        # every clone holds the prompt's tail rows bit for bit
+        # every clone of every prompt holds the prompt's tail rows bit for bit
         B, tail = w.block_size, prompt_len % w.block_size
-        st = pw.layers[0]
-        kc = bits16(st.k_cache)
-        for p in range(0, 32, 7):
-            K, _ = host_rows(w, 0, p * w.group, prompt_len)
+        kc = bits16(pw.layers[0].k_cache)
+        for p in range(32):
+            K, _ = rows(p * w.group)
             want = bits16(K)[prompt_len - tail:prompt_len]          # [tail, Hk, D]
             for r in range(w.group):
                 s = p * w.group + r
                 blk = int(pw.tables_host[s][prompt_len // B])
                 got = kc[blk][:, :tail, :].transpose(1, 0, 2)
                 assert np.array_equal(got, want)
+        del kc
     out = _step(pw)[0]
-    seqs = _sample(w.num_seqs, 30, 4)
-    ref = expected(w, 0, seqs)
-    assert_close(out[seqs], ref, "cow %d" % prompt_len)
     # the shared-prefix decode as the benchmark runs it (a replayed CUDA graph)
     groups = workload.prefix_groups(pw)
     P = w.partition_size
-    ws = pkv.shared_prefix_workspace(w.num_seqs, w.num_heads, w.head_dim, groups[3],
-                                     groups[2] * w.block_size, P)
+    ws = pkv.shared_prefix_workspace(w.num_seqs, w.num_heads, w.head_dim, groups.max_own_context,
+                                     groups.max_prefix_blocks * w.block_size, P)
     sp = [torch.empty_like(pw.layers[0].q)]
     g = workload.capture_step(pw, sp, ws, P, groups=groups)
     g.replay()
     torch.cuda.synchronize()
-    assert_close(sp[0].cpu()[seqs], ref, "cow %d shared prefix" % prompt_len)
     assert int(_lib.item()) == 0
+    sp = sp[0].cpu()
+    for i in range(0, w.num_seqs, CHUNK):
+        part = list(range(i, i + CHUNK))
+        ref = expected(w, 0, part, rows=rows)
+        assert_close(out[part], ref, "cow %d split, seqs %d.." % (prompt_len, i))
+        assert_close(sp[part], ref, "cow %d shared prefix, seqs %d.." % (prompt_len, i))
 
 
 def test_long_context_fp8(_lib):
     w = synth.long_fp8()
     pw = workload.build(w)
     st = pw.layers[0]
-    ks, vs = st.k_scale.cpu().numpy(), st.v_scale.cpu().numpy()
-    # the stored codes of a sampled block equal the oracle's encoding
-    s, t0 = 5, 77 * w.block_size
-    K, V = host_rows(w, 0, s, t0 + w.block_size)
-    blk = int(pw.tables_host[s][t0 // w.block_size])
-    got = st.k_cache[blk].cpu().numpy().transpose(1, 0, 2)
-    assert np.array_equal(got, quantize(K[t0:], ks))
+    # the scales, recomputed on the host from every row of the layer
+    rows = _memo(lambda s: host_rows(w, 0, s))
+    ks, vs = host_fp8_scales(w, 0, rows)
+    assert np.array_equal(ks.view(np.uint32), st.k_scale.cpu().numpy().view(np.uint32))
+    assert np.array_equal(vs.view(np.uint32), st.v_scale.cpu().numpy().view(np.uint32))
     out = _step(pw)[0]
-    seqs = [0, 7]
-    assert_close(out[seqs], expected(w, 0, seqs, ks, vs), "long fp8")
     assert int(_lib.item()) == 0
+    # every sequence, on the oracle's own E4M3 codes of the host rows
+    _check_all(out, w, 0, rows, "long fp8", ks, vs)
+    # the whole pool after the step's write: the oracle's encoding at every slot
+    pk, pv = _pool_image(w, 0, pw, rows, st.k_cache.shape[0], ks, vs)
+    assert np.array_equal(_pool_bits(st.k_cache), pk), "fp8 K pool"
+    del pk
+    assert np.array_equal(_pool_bits(st.v_cache), pv), "fp8 V pool"

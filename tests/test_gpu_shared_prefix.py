@@ -5,10 +5,11 @@ import dataclasses
 import pytest
 import torch
 
+import oracle
 import paged_kv_cache_220_gb300 as pkv
 from paged_kv_cache_220_gb300 import build as pkv_build
 from paged_kv_cache_220_gb300 import synth, workload
-from _oracle_side import MAX_ABS, REL_L2, assert_close, errors, expected
+from _oracle_side import MAX_ABS, REL_L2, assert_close, bits16, errors, expected, host_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -25,17 +26,18 @@ def _lib():
 @pytest.mark.parametrize("prompt,B,P,rollouts,d", [(40, 16, 32, 4, 256), (48, 16, 16, 16, 256),
                                                     (2040, 16, 512, 16, 256), (200, 32, 64, 3, 256),
                                                     (100, 16, 512, 21, 256), (300, 16, 64, 16, 128),
-                                                    (330, 32, 128, 5, 128)])
+                                                    (330, 32, 128, 5, 128),
+                                                    (300, 16, 64, 32, 256),
+                                                    (130, 32, 64, 64, 128)])
 def test_shared_prefix_matches_oracle(prompt, B, P, rollouts, d, _lib):
     w = synth.cow(prompt_len=prompt, prompts=2, rollouts=rollouts)
     comp = w.extra["completion"][:2 * rollouts]
     w = dataclasses.replace(w, block_size=B, head_dim=d, ctx=[prompt + (c % 300) + 1 for c in comp],
                             slack_blocks=64)
-    if rollouts * w.num_heads // w.num_kv_heads > 128:
-        pytest.skip("group larger than one prefix CTA")
     pw = workload.build(w)
     groups = workload.prefix_groups(pw)
-    assert groups[2] == prompt // B
+    assert groups.max_prefix_blocks == prompt // B
+    assert groups.max_group_members == rollouts     # > 128 query rows: several row tiles
     out = [torch.empty_like(pw.layers[0].q)]
     workload.step_shared_prefix(pw, out, groups, None, P)
     torch.cuda.synchronize()
@@ -58,7 +60,7 @@ def test_shared_prefix_mixed_with_ungrouped_and_exact_prefix(_lib):
     w = synth.cow(prompt_len=64, prompts=2, rollouts=4)
     w = dataclasses.replace(w, ctx=[65, 66, 90, 65, 70, 71, 72, 200])
     pw = workload.build(w)
-    gs, pre, mp, _ = workload.prefix_groups(pw)
+    gs, pre, mp, _, _ = workload.prefix_groups(pw)
     # split the second prompt's group into singletons without a shared prefix
     gs2 = torch.tensor([0, 4], dtype=torch.int32, device="cuda")
     pre2 = pre.clone()
@@ -68,7 +70,7 @@ def test_shared_prefix_mixed_with_ungrouped_and_exact_prefix(_lib):
     out = pkv.paged_attention_shared_prefix(pw.layers[0].q, pw.layers[0].k_cache,
                                             pw.layers[0].v_cache, pw.block_tables,
                                             pw.context_lens, w.scale, pw.max_context, gs2, pre2,
-                                            mp, 32)
+                                            mp, 32, 4)
     torch.cuda.synchronize()
     assert_close(out.cpu(), expected(w, 0, range(w.num_seqs)), "mixed groups")
 
@@ -82,8 +84,8 @@ def test_shared_prefix_graph_replay_matches_eager(_lib):
     pw = workload.build(w)
     groups = workload.prefix_groups(pw)
     P = w.partition_size
-    ws = pkv.shared_prefix_workspace(w.num_seqs, w.num_heads, w.head_dim, groups[3],
-                                     groups[2] * w.block_size, P)
+    ws = pkv.shared_prefix_workspace(w.num_seqs, w.num_heads, w.head_dim, groups.max_own_context,
+                                     groups.max_prefix_blocks * w.block_size, P)
     eager = [torch.empty_like(pw.layers[0].q)]
     workload.step_shared_prefix(pw, eager, groups, ws, P)
     torch.cuda.synchronize()
@@ -106,21 +108,61 @@ def test_shared_prefix_own_part_bound(_lib):
     partitions is read."""
     w = synth.cow(prompt_len=2040, prompts=2, rollouts=16)
     pw = workload.build(w)
-    gs, pre, mp, own = workload.prefix_groups(pw)
+    gs, pre, mp, own, mm = workload.prefix_groups(pw)
     assert own < pw.max_context - 2000
     P = w.partition_size
     st = pw.layers[0]
     pkv.kv_cache_write(st.k_new, st.v_new, pw.slot_mapping, st.k_cache, st.v_cache)
     outs = [pkv.paged_attention_shared_prefix(st.q, st.k_cache, st.v_cache, pw.block_tables,
-                                              pw.context_lens, w.scale, bound, gs, pre, mp, P)
+                                              pw.context_lens, w.scale, bound, gs, pre, mp, P, mm)
             for bound in (own, pw.max_context)]
     torch.cuda.synchronize()
     assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
     assert int(_lib.item()) == 0
     assert_close(outs[0].cpu(), expected(w, 0, range(w.num_seqs)), "own-part bound")
     short = pkv.paged_attention_shared_prefix(st.q, st.k_cache, st.v_cache, pw.block_tables,
-                                              pw.context_lens, w.scale, own - P, gs, pre, mp, P)
+                                              pw.context_lens, w.scale, own - P, gs, pre, mp, P,
+                                              mm)
     torch.cuda.synchronize()
     assert int(_lib.item()) == pkv.DEVERR_CONTEXT
     assert torch.isfinite(short.float()).all()
     _lib.zero_()
+
+
+def test_shared_prefix_group_above_declared_bound(_lib):
+    """A group with more members than max_group_members: the error word says
+    so, the members a row tile covers are exact, and the uncovered members'
+    result is the attention over their own rows only (their shared partials
+    are written empty), never stale workspace."""
+    w = synth.cow(prompt_len=256, prompts=2, rollouts=32)
+    comp = w.extra["completion"]
+    w = dataclasses.replace(w, ctx=[256 + (c % 200) + 1 for c in comp])
+    pw = workload.build(w)
+    gs, pre, mp, own, mm = workload.prefix_groups(pw)
+    assert mm == 32
+    st = pw.layers[0]
+    pkv.kv_cache_write(st.k_new, st.v_new, pw.slot_mapping, st.k_cache, st.v_cache)
+    per_tile = 128 // (w.num_heads // w.num_kv_heads)            # 21 members at g = 6
+    ws = pkv.shared_prefix_workspace(w.num_seqs, w.num_heads, w.head_dim, own,
+                                     mp * w.block_size, 64)
+    ws.view(torch.float32).fill_(float("nan"))
+    out = pkv.paged_attention_shared_prefix(st.q, st.k_cache, st.v_cache, pw.block_tables,
+                                            pw.context_lens, w.scale, own, gs, pre, mp, 64,
+                                            per_tile, workspace=ws)
+    torch.cuda.synchronize()
+    assert int(_lib.item()) == pkv.DEVERR_CONTEXT
+    _lib.zero_()
+    got = out.cpu()
+    covered = [p * 32 + r for p in range(2) for r in range(per_tile)]
+    assert_close(got[covered], expected(w, 0, covered), "covered members")
+    uncovered = [p * 32 + r for p in range(2) for r in range(per_tile, 32)]
+    B = w.block_size
+    q = bits16(w.q(0, "cpu"))[uncovered]
+    ks, vs = [], []
+    for s in uncovered:
+        K, V = host_rows(w, 0, s)
+        t0 = int(pre[s]) * B
+        ks.append(bits16(K)[t0:])
+        vs.append(bits16(V)[t0:])
+    own_only = oracle.decode(q, ks, vs, w.scale)
+    assert_close(got[uncovered], own_only, "uncovered members: own rows only")

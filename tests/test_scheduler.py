@@ -303,3 +303,25 @@ def test_sampled_request_arguments():
     with pytest.raises(pkv.PagedKVError):
         sched.add_request(0, 10, 5, n=5)        # more samples than batch rows
     assert sched.cow_pairs().shape == (0, 2)
+
+
+def test_request_ids_must_not_collide_with_live_requests():
+    """Samples take ids id .. id + n - 1; an id still waiting, running or
+    swapped out is rejected (the id lookups would find the wrong request),
+    a finished one may be reused."""
+    a = pkv.BlockAllocator(64, 4, seed=3)
+    s = pkv.Scheduler(a, 8)
+    s.add_request(10, 6, 2, n=3)                        # ids 10, 11, 12
+    for rid, n in ((12, 1), (8, 3), (11, 2), (-1, 1)):
+        with pytest.raises(pkv.PagedKVError) as e:
+            s.add_request(rid, 4, 2, n=n)
+        assert e.value.status == pkv.PKV_ERR_INVALID_ARG
+    s.add_request(13, 4, 1)                             # adjacent ids are fine
+    s.step()                                            # all admitted: running now
+    with pytest.raises(pkv.PagedKVError):
+        s.add_request(11, 4, 2)
+    while not (s.counts()["running"] == 0 and s.counts()["waiting"] == 0):
+        s.step()
+    s.add_request(11, 4, 2)                             # finished ids are free again
+    s.close()
+    a.close()

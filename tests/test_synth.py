@@ -55,3 +55,14 @@ def test_workload_shapes():
     f = synth.long_fp8()
     assert f.fp8 and f.ctx == [131072] * 8
     assert abs(q.scale - 0.0625) == 0.0
+
+
+def test_normal_bf16_equals_elementwise_definition():
+    # the vectorised stream against SplitMix64 on Python ints, element by
+    # element, with counters near the top of the key range
+    key = (1 << 62) - 5000
+    vals = synth.normal_bf16(key, 64, 4000)
+    tab = synth.normal_table()
+    for i in range(64):
+        z = synth.mix64_int(key + 4000 + i)
+        assert vals[i].view(torch.int16).item() == tab[z >> 48].view(torch.int16).item()
