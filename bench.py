@@ -164,7 +164,11 @@ def ncu_traffic(config: str):
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    """nvidia-smi clocks and throttle reasons sampled every 20 ms during the
+    timed region (the `with` block). The sampler is started, and its first
+    sample awaited, before the region begins; the summary keeps the samples
+    written while the region ran (the nearest one on each side if it was
+    shorter than a sampling period)."""
 
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -174,6 +178,13 @@ class ClockSampler:
         self.idx = gpu_index
         self.proc = None
         self.path = os.path.join("/tmp", "pkv_clocks_%d_%d.csv" % (os.getpid(), gpu_index))
+        self.n0 = self.n1 = 0
+
+    def _rows(self):
+        try:
+            return [l for l in open(self.path).read().splitlines() if l.count(",") >= 8]
+        except OSError:
+            return []
 
     def __enter__(self):
         try:
@@ -184,10 +195,17 @@ class ClockSampler:
                 stdout=self.fh, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
+            return self
+        t0 = time.time()
+        while not self._rows() and time.time() - t0 < 3.0 and self.proc.poll() is None:
+            time.sleep(0.01)
+        self.n0 = len(self._rows())
         return self
 
     def __exit__(self, *a):
         if self.proc is not None:
+            self.n1 = len(self._rows())
+            time.sleep(0.05)               # one more sample after the region
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
@@ -196,17 +214,15 @@ class ClockSampler:
             self.fh.close()
 
     def summary(self):
-        if self.proc is None or not os.path.exists(self.path):
+        if self.proc is None:
             return None
-        rows = []
-        for line in open(self.path):
-            f = [x.strip() for x in line.split(",")]
-            if len(f) < 9:
-                continue
-            try:
-                rows.append(f)
-            except ValueError:
-                pass
+        allrows = self._rows()
+        inside = allrows[self.n0:self.n1]
+        note = "samples taken during the timed region"
+        if not inside:
+            inside = allrows[max(0, self.n0 - 1):self.n1 + 1]
+            note = "region shorter than the 20 ms sampling period: nearest samples"
+        rows = [[x.strip() for x in r.split(",")] for r in inside]
         if not rows:
             return None
         sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
@@ -219,7 +235,7 @@ class ClockSampler:
                     reasons.add(n)
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(mx) if mx else None,
-                "reasons": sorted(reasons), "samples": len(rows)}
+                "reasons": sorted(reasons), "samples": len(rows), "note": note}
 
 
 def fp8_scales_host(w, layer=0):
@@ -335,7 +351,8 @@ def make_step(pw, out, ws, cascade, stream):
                                                   cascade.prefix_blocks,
                                                   cascade.max_prefix_blocks, P,
                                                   cascade.max_group_members,
-                                                  out=out[layer], workspace=ws)
+                                                  out=out[layer], workspace=ws,
+                                                  k_scale=st.k_scale, v_scale=st.v_scale)
                 if ev is not None:
                     ev[layer][1].record(stream)
                 continue
@@ -372,7 +389,7 @@ def measure_other(name, steps=10, warmup=3):
     out = [torch.empty_like(st.q) for st in pw.layers]
     ws = pkv.alloc_workspace(w.num_seqs, w.num_heads, w.head_dim, pw.max_context, P) if P else None
     cascade = None
-    if w.prefix_len > 0 and P and not w.fp8:
+    if w.prefix_len > 0 and P:
         cascade = workload.prefix_groups(pw)
         ws = pkv.shared_prefix_workspace(w.num_seqs, w.num_heads, w.head_dim,
                                          cascade.max_own_context,
@@ -397,6 +414,9 @@ def measure_other(name, steps=10, warmup=3):
     graph = workload.capture_step(pw, out, ws, P, groups=cascade)
     for _ in range(warmup):
         graph.replay()
+    # enough steps for ~0.3 s of timed work (the clock sampler's period is 20 ms)
+    eager_ms = sum(evs[i][0][0].elapsed_time(evs[i][L - 1][1]) for i in range(steps)) / steps
+    steps = max(steps, int(0.3 / max(eager_ms / 1e3, 1e-6)))
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
     torch.cuda.synchronize()
     with ClockSampler(torch.cuda.current_device()) as clk:
@@ -516,7 +536,7 @@ def main():
     cow = pw.cow_pairs
 
     cascade = None
-    if w.prefix_len > 0 and args.shared_prefix and P and not w.fp8:
+    if w.prefix_len > 0 and args.shared_prefix and P:
         cascade = workload.prefix_groups(pw)
         ws = pkv.shared_prefix_workspace(w.num_seqs, w.num_heads, w.head_dim,
                                          cascade.max_own_context,
@@ -789,7 +809,8 @@ def run_e2e(args, pw, w, out, ws, P, per_step_bytes, world, dist, cascade=None):
                                                   d_cl, w.scale, cascade.max_own_context, dm[3],
                                                   dm[4], cascade.max_prefix_blocks, P,
                                                   cascade.max_group_members, out=do[layer],
-                                                  workspace=ws)
+                                                  workspace=ws, k_scale=st.k_scale,
+                                                  v_scale=st.v_scale)
             else:
                 pkv.paged_attention(dv[layer]["q"], st.k_cache, st.v_cache, d_bt, d_cl, w.scale,
                                     pw.max_context, P, st.k_scale, st.v_scale, out=do[layer],

@@ -246,11 +246,14 @@ int pkv_paged_attention(void* out, const void* q, const void* k_cache,
  *                   slot NPP + p the own partition p (tokens from
  *                   prefix_blocks[s]*block_size + p*P on), in the form of
  *                   pkv_paged_attention_decode's partials.
+ *   k_scale, v_scale : device fp32 [num_kv_heads] dequantisation scales of
+ *                   an E4M3 pool (required then, else ignored), as for
+ *                   pkv_paged_attention_decode
  * Per group, KV head and row tile, a kernel computes partials of the members'
  * query heads over the shared pages (the members' queries form the rows of
- * one tensor-core product); each member's own blocks go through the split
- * decode; the merge combines both. bf16 pools only (PKV_ERR_UNSUPPORTED
- * otherwise).
+ * one tensor-core product; for E4M3 pools the codes are turned into exact f16
+ * operands in shared memory and P is one f16 part); each member's own blocks
+ * go through the split decode; the merge combines both.
  * ------------------------------------------------------------------------ */
 size_t pkv_shared_prefix_workspace_bytes(int num_seqs, int num_heads, int head_dim,
                                          int max_own_context, int max_prefix_tokens,
@@ -263,7 +266,8 @@ int pkv_shared_prefix_partition_size(int num_groups, int max_group_members, int 
                                      int partition_size);
 int pkv_paged_attention_decode_shared_prefix(
     void* out, const void* q, const void* k_cache, const void* v_cache,
-    pkv_cache_desc cache, const int32_t* block_tables, int max_blocks_per_seq,
+    pkv_cache_desc cache, const float* k_scale, const float* v_scale,
+    const int32_t* block_tables, int max_blocks_per_seq,
     const int32_t* context_lens, int num_seqs, int num_heads, int max_own_context,
     float scale, const int32_t* group_start, int num_groups, int max_group_members,
     const int32_t* prefix_blocks, int max_prefix_blocks, int partition_size,

@@ -76,7 +76,8 @@ SIGNATURES = {
                                                 _I, _I, _I, ctypes.c_float, _I, _P]),
     "pkv_shared_prefix_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I, _I, _I, _I]),
     "pkv_shared_prefix_partition_size": (_I, [_I, _I, _I, _I, _I, _I, _I]),
-    "pkv_paged_attention_decode_shared_prefix": (_I, [_P, _P, _P, _P, CacheDesc, _P, _I, _P, _I,
+    "pkv_paged_attention_decode_shared_prefix": (_I, [_P, _P, _P, _P, CacheDesc, _P, _P, _P, _I,
+                                                      _P, _I,
                                                       _I, _I, ctypes.c_float, _P, _I, _I, _P,
                                                       _I, _I, _P, ctypes.c_size_t, _P]),
     "pkv_copy_blocks": (_I, [_P, _P, CacheDesc, _P, _I, _P]),
@@ -314,7 +315,7 @@ def shared_prefix_partition_size(num_groups, max_group_members, num_kv_heads, nu
 def paged_attention_shared_prefix(q, k_cache, v_cache, block_tables, context_lens, scale,
                                   max_own_context, group_start, prefix_blocks, max_prefix_blocks,
                                   partition_size, max_group_members, out=None, workspace=None,
-                                  stream=None) -> torch.Tensor:
+                                  k_scale=None, v_scale=None, stream=None) -> torch.Tensor:
     """Decode of groups sharing prompt blocks (see the C header): shared pages
     are read once per group. group_start int32 [G+1], prefix_blocks int32 [S];
     max_own_context bounds context_lens[s] - prefix_blocks[s] * block_size;
@@ -331,6 +332,7 @@ def paged_attention_shared_prefix(q, k_cache, v_cache, block_tables, context_len
     rc = lib().pkv_paged_attention_decode_shared_prefix(
         _dev_ptr(out, "out", torch.bfloat16), _dev_ptr(q, "q", torch.bfloat16),
         _dev_ptr(k_cache, "k_cache"), _dev_ptr(v_cache, "v_cache"), desc,
+        _dev_ptr(k_scale, "k_scale", torch.float32), _dev_ptr(v_scale, "v_scale", torch.float32),
         _dev_ptr(block_tables, "block_tables", torch.int32), int(block_tables.shape[1]),
         _dev_ptr(context_lens, "context_lens", torch.int32), S, Hq, int(max_own_context),
         float(scale), _dev_ptr(group_start, "group_start", torch.int32), G,

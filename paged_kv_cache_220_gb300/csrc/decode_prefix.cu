@@ -28,6 +28,8 @@ struct PrefixParams {
   const int32_t* block_tables;
   const int32_t* group_start;     // [G + 1]
   const int32_t* prefix_blocks;   // [S] shared full blocks of each sequence's group
+  const float* k_scale;           // E4M3 pools: [Hk] dequantisation scales
+  const float* v_scale;
   float* tmp_out;
   float* max_logits;
   float* exp_sums;
@@ -77,17 +79,34 @@ struct PrefixParams {
 // reference, so the result does not depend on when that happens). P carries
 // ~16 significant bits (high + low bf16 parts, two MMAs per k-step) like the
 // other kernels.
+//
+// E4M3 pools (FP8): the products run on f16 operands. TMA brings a step's
+// pages (codes) into a staging ring of two stages; four converter warps
+// (7-10) turn every code into its exact f16 value and store it where the
+// bf16 path's TMA would have put a page element, in the same swizzled
+// layout, then make the stores visible to the tensor core (proxy fence) and
+// release the staging stage. Q is converted to f16 once (exact in f16's
+// normal range), P is one f16 part (11 significant bits; one MMA per
+// k-step), the logit scale carries k_scale and the output v_scale. This
+// keeps the group product on the tensor core: the alternative, E4M3 operands
+// (kind::f8f6f4), would need Q and P in 8-bit form.
 
-template <int D, int BS>
+template <int D, int BS, bool FP8 = false>
 struct TmemPrefixGeom {
   static constexpr int kTok = 64;             // tokens per step (one 64-column load of S)
   static constexpr int kPages = kTok / BS;    // pages per step
-  static constexpr int kPage = BS * D * 2;    // bytes of one page of K (or V)
+  static constexpr int kPage = BS * D * 2;    // bytes of one page of K (or V), 16-bit operand
   static constexpr int kGroup = kTok * D * 2; // bytes of one step of K (or V)
   static constexpr int kChunk = kTok * 128;   // one 64-column chunk of a step
-  static constexpr int kSmem = 1024 + 1024 + 4 * kGroup;  // + the block ids
+  static constexpr int kPage8 = BS * D;       // FP8: bytes of one staged page of codes
+  static constexpr int kGroup8 = kTok * D;    // FP8: bytes of one staged step of K (or V)
+  static constexpr int kStage8 = FP8 ? 4 * kGroup8 : 0;    // K and V, two stages each
+  static constexpr int kNK = 2;               // K stages (steps) in shared memory
+  static constexpr int kNV = 2;               // V stages
+  static constexpr int kSmem = 1024 + 1024 + (kNK + kNV) * kGroup + kStage8;  // + the block ids
   static constexpr int kMaxIds = 2048;                     // partition_blocks limit
-  static constexpr int kThreads = 7 * 32;
+  static constexpr int kConvWarps = FP8 ? 4 : 0;
+  static constexpr int kThreads = (7 + kConvWarps) * 32;
   static constexpr uint32_t kColS = D;              // S of step t at kColS + 64 * (t & 1)
   static constexpr uint32_t kColQ = D + 2 * kTok;   // Q: k-step k at kColQ + 8 k
   static constexpr uint32_t kUsed = kColQ + D / 2;
@@ -96,30 +115,55 @@ struct TmemPrefixGeom {
   static_assert(BS == 16 || BS == 32, "page size");
 };
 
-template <int D, int BS>
-__global__ void __launch_bounds__(TmemPrefixGeom<D, BS>::kThreads)
+// E4M3 -> f16 of one 16-byte unit of codes (16 dims of one row) staged at
+// shared address `src`, stored as two 16-byte units at `dst0` / `dst1`.
+__device__ __forceinline__ void convert_unit_e4m3(uint32_t src, uint32_t dst0, uint32_t dst1) {
+  uint32_t c0, c1, c2, c3;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(c0), "=r"(c1), "=r"(c2), "=r"(c3)
+               : "r"(src));
+  asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(dst0), "r"(e4m3x2_f16x2(c0, 0)),
+               "r"(e4m3x2_f16x2(c0, 1)), "r"(e4m3x2_f16x2(c1, 0)), "r"(e4m3x2_f16x2(c1, 1))
+               : "memory");
+  asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(dst1), "r"(e4m3x2_f16x2(c2, 0)),
+               "r"(e4m3x2_f16x2(c2, 1)), "r"(e4m3x2_f16x2(c3, 0)), "r"(e4m3x2_f16x2(c3, 1))
+               : "memory");
+}
+
+__device__ __forceinline__ uint32_t swz128(uint32_t a) { return a ^ (((a >> 7) & 7u) << 4); }
+
+template <int D, int BS, bool FP8>
+__global__ void __launch_bounds__(TmemPrefixGeom<D, BS, FP8>::kThreads)
     prefix_tmem_kernel(const __grid_constant__ CUtensorMap tmk,
                        const __grid_constant__ CUtensorMap tmv, const PrefixParams p) {
-  using G = TmemPrefixGeom<D, BS>;
+  using G = TmemPrefixGeom<D, BS, FP8>;
   constexpr int KT = D / 16;
   constexpr int NP = G::kPages;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* sbase = smem_raw + (base - raw);
-  uint64_t* k_full = reinterpret_cast<uint64_t*>(sbase);  // [2]
-  uint64_t* k_empty = k_full + 2;                          // [2]
-  uint64_t* v_full = k_empty + 2;                          // [2]
-  uint64_t* v_empty = v_full + 2;                          // [2]
-  uint64_t* s_full = v_empty + 2;                          // [2]
+  uint64_t* k_full = reinterpret_cast<uint64_t*>(sbase);  // [NK]
+  uint64_t* k_empty = k_full + 4;                          // [NK]
+  uint64_t* v_full = k_empty + 4;                          // [NV]
+  uint64_t* v_empty = v_full + 4;                          // [NV]
+  uint64_t* s_full = v_empty + 4;                          // [2]
   uint64_t* p_full = s_full + 2;                           // [2]
   uint64_t* o_done = p_full + 2;                           // [2]
   uint64_t* drained = o_done + 2;
   uint64_t* q_ready = drained + 1;
+  uint64_t* k8_full = q_ready + 1;   // FP8: [2] codes of K staged
+  uint64_t* k8_empty = k8_full + 2;  // FP8: [2] staged K converted
+  uint64_t* v8_full = k8_empty + 2;
+  uint64_t* v8_empty = v8_full + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sbase + 1000);
-  const uint32_t kring = base + 1024;           // K stage b at kring + b * kGroup
-  const uint32_t vring = kring + 2 * G::kGroup; // V stage b at vring + b * kGroup
-  int32_t* ids = reinterpret_cast<int32_t*>(sbase + 1024 + 4 * G::kGroup);
+  constexpr int NK = G::kNK, NV = G::kNV;
+  const uint32_t kring = base + 1024;            // K stage b at kring + b * kGroup
+  const uint32_t vring = kring + NK * G::kGroup; // V stage b at vring + b * kGroup
+  const uint32_t k8ring = vring + NV * G::kGroup;  // FP8: staged K stage b at + b * kGroup8
+  const uint32_t v8ring = k8ring + 2 * G::kGroup8;
+  int32_t* ids =
+      reinterpret_cast<int32_t*>(sbase + 1024 + (NK + NV) * G::kGroup + G::kStage8);
   // the members' own-block decode launched next may start on the room this
   // grid leaves free (it writes other workspace slots and reads no output of
   // this kernel)
@@ -160,11 +204,23 @@ __global__ void __launch_bounds__(TmemPrefixGeom<D, BS>::kThreads)
   const int nsteps = (nblk + NP - 1) / NP;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&k_full[i], 2);  // one arrival per producer warp
+    // bf16: one arrival per producer warp (with the bytes); FP8: one per
+    // converter warp, the producers' arrivals go to the staging barriers
+    for (int i = 0; i < NK; ++i) {
+      mbar_init(&k_full[i], FP8 ? G::kConvWarps : 2);
       mbar_init(&k_empty[i], 1);
-      mbar_init(&v_full[i], 2);
+    }
+    for (int i = 0; i < NV; ++i) {
+      mbar_init(&v_full[i], FP8 ? G::kConvWarps : 2);
       mbar_init(&v_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      if constexpr (FP8) {
+        mbar_init(&k8_full[i], 2);
+        mbar_init(&k8_empty[i], G::kConvWarps);
+        mbar_init(&v8_full[i], 2);
+        mbar_init(&v8_empty[i], G::kConvWarps);
+      }
       mbar_init(&s_full[i], 1);
       mbar_init(&p_full[i], 128);
       mbar_init(&o_done[i], 1);
@@ -198,22 +254,30 @@ __global__ void __launch_bounds__(TmemPrefixGeom<D, BS>::kThreads)
   if (warp == 0 || warp == 6) {
     if (lane == 0) {
       const int half = warp == 0 ? 0 : 1;  // this producer's pages: q % 2 == half
-      // K (kind 0) or V (kind 1) of step st into stage st & 1; the stage was
-      // last read by S (K) or P.V (V) of step st - 2
+      // K (kind 0) or V (kind 1) of step st into stage st % N (N = NK or
+      // NV); the stage was last read by S (K) or P.V (V) of step st - N.
+      // FP8: the copies go to the two-stage staging ring, released by the
+      // converters
       auto issue = [&](int kind, int st) -> bool {
-        const int b = st & 1;
-        uint64_t* full = kind == 0 ? &k_full[b] : &v_full[b];
-        uint64_t* empty = kind == 0 ? &k_empty[b] : &v_empty[b];
-        if (st >= 2 && !mbar_wait(empty, ((st >> 1) - 1) & 1, p.err)) return false;
+        const int n = FP8 ? 2 : (kind == 0 ? NK : NV);
+        const int b = st % n;
+        uint64_t* full = FP8 ? (kind == 0 ? &k8_full[b] : &v8_full[b])
+                             : (kind == 0 ? &k_full[b] : &v_full[b]);
+        uint64_t* empty = FP8 ? (kind == 0 ? &k8_empty[b] : &v8_empty[b])
+                              : (kind == 0 ? &k_empty[b] : &v_empty[b]);
+        if (st >= n && !mbar_wait(empty, ((st / n) - 1) & 1, p.err)) return false;
         const int np = min(NP, nblk - st * NP);
         int good = 0;
         for (int q = half; q < np; q += 2) good += ids[st * NP + q] >= 0 ? 1 : 0;
-        mbar_arrive_expect_tx(full, good * G::kPage);
+        mbar_arrive_expect_tx(full, good * (FP8 ? G::kPage8 : G::kPage));
         for (int q = half; q < np; q += 2) {
           const int32_t pb = ids[st * NP + q];
           if (pb < 0) continue;
           const int y = (pb * p.num_kv_heads + h) * BS;
-          if (kind == 0) {
+          if constexpr (FP8) {
+            tma_load_page((kind == 0 ? k8ring : v8ring) + b * G::kGroup8 + q * G::kPage8,
+                          kind == 0 ? &tmk : &tmv, y, full);
+          } else if (kind == 0) {
 #pragma unroll
             for (int c = 0; c < D / 64; ++c)
               tma_load_2d(kring + b * G::kGroup + c * G::kChunk + q * BS * 128, &tmk, c * 64, y,
@@ -237,31 +301,33 @@ __global__ void __launch_bounds__(TmemPrefixGeom<D, BS>::kThreads)
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      constexpr uint32_t idesc_qk = umma_idesc_bf16(128, G::kTok, false);
-      constexpr uint32_t idesc_pv = umma_idesc_bf16(128, D, true);
+      constexpr uint32_t idesc_qk = FP8 ? umma_idesc_f16(128, G::kTok, false)
+                                        : umma_idesc_bf16(128, G::kTok, false);
+      constexpr uint32_t idesc_pv = FP8 ? umma_idesc_f16(128, D, true)
+                                        : umma_idesc_bf16(128, D, true);
       const bool ok = mbar_wait(q_ready, 0, p.err);
       for (int st = 0; st <= nsteps && ok; ++st) {
         if (st < nsteps) {
-          const int b = st & 1;
-          if (!mbar_wait(&k_full[b], (st >> 1) & 1, p.err)) break;
+          const int b = st & 1, bk = st % NK;
+          if (!mbar_wait(&k_full[bk], (st / NK) & 1, p.err)) break;
           // S of step st overwrites P of step st - 2
           if (st >= 2 && !mbar_wait(&o_done[b], ((st - 2) >> 1) & 1, p.err)) break;
           tc_fence_after();
-          const uint32_t kp = kring + b * G::kGroup;
+          const uint32_t kp = kring + bk * G::kGroup;
 #pragma unroll
           for (int k = 0; k < KT; ++k) {
             const uint64_t bk = umma_sdesc(kp + (k >> 2) * G::kChunk + (k & 3) * 32, 16, 1024, 2);
             umma_bf16_ta(t_s + b * G::kTok, t_q + 8 * k, bk, idesc_qk, k > 0 ? 1u : 0u);
           }
           umma_commit(&s_full[b]);
-          umma_commit(&k_empty[b]);
+          umma_commit(&k_empty[bk]);
         }
         if (st >= 1) {
-          const int j = st - 1, b = j & 1;
+          const int j = st - 1, b = j & 1, bv = j % NV;
           if (!mbar_wait(&p_full[b], (j >> 1) & 1, p.err)) break;
-          if (!mbar_wait(&v_full[b], (j >> 1) & 1, p.err)) break;
+          if (!mbar_wait(&v_full[bv], (j / NV) & 1, p.err)) break;
           tc_fence_after();
-          const uint32_t vp = vring + b * G::kGroup;
+          const uint32_t vp = vring + bv * G::kGroup;
           const uint32_t ph = t_s + b * G::kTok;
           const int ksteps = min(NP, nblk - j * NP) * (BS / 16);
           for (int kk = 0; kk < ksteps; ++kk) {
@@ -270,10 +336,10 @@ __global__ void __launch_bounds__(TmemPrefixGeom<D, BS>::kThreads)
             const uint32_t va = vp + (kk / (BS / 16)) * G::kPage + (kk % (BS / 16)) * 2048;
             const uint64_t bv = umma_sdesc(va, BS * 128, 1024, 2);
             umma_bf16_ta(t_o, ph + 8 * kk, bv, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
-            umma_bf16_ta(t_o, ph + 32 + 8 * kk, bv, idesc_pv, 1u);
+            if constexpr (!FP8) umma_bf16_ta(t_o, ph + 32 + 8 * kk, bv, idesc_pv, 1u);
           }
           umma_commit(&o_done[b]);
-          umma_commit(&v_empty[b]);
+          umma_commit(&v_empty[bv]);
         }
       }
       // every tensor-core operation issued here has finished before tensor
@@ -281,11 +347,11 @@ __global__ void __launch_bounds__(TmemPrefixGeom<D, BS>::kThreads)
       umma_commit(drained);
       (void)mbar_wait(drained, 0, p.err);
     }
-  } else {
+  } else if (warp >= 2 && warp <= 5) {
     // softmax: one query row per thread
     const int row = 32 * (warp & 3) + lane;
     const uint32_t lane_off = static_cast<uint32_t>(32 * (warp & 3)) << 16;
-    const float qs = p.qscale;
+    const float qs = FP8 ? p.qscale * p.k_scale[h] : p.qscale;
     float m_used = -INFINITY, l = 0.f;
     // Q row `row` (member row / g, head h*g + row % g) into tensor memory;
     // rows past the group's query rows are zero
@@ -305,6 +371,12 @@ __global__ void __launch_bounds__(TmemPrefixGeom<D, BS>::kThreads)
           w[4 * i + 1] = v.y;
           w[4 * i + 2] = v.z;
           w[4 * i + 3] = v.w;
+          if constexpr (FP8) {
+            // f16 operands: the bf16 pairs as f16 pairs
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              w[4 * i + k] = pack_f16(bf16lo(w[4 * i + k]), bf16hi(w[4 * i + k]));
+          }
         }
         tmem_st16_nowait(t_q + lane_off + c / 2, w);
       }
@@ -357,7 +429,8 @@ __global__ void __launch_bounds__(TmemPrefixGeom<D, BS>::kThreads)
         l *= alpha;
         m_used = mx;
       }
-      // P over S's columns: bf16 high parts, then the low parts
+      // P over S's columns: bf16 high parts, then the low parts (FP8: one
+      // f16 part)
       uint32_t hw[G::kTok / 2], lw[G::kTok / 2];
 #pragma unroll
       for (int i = 0; i < G::kTok / 2; ++i) {
@@ -365,14 +438,20 @@ __global__ void __launch_bounds__(TmemPrefixGeom<D, BS>::kThreads)
         const float p1 = fast_exp2(sv[2 * i + 1] - m_used);
         l += p0;
         l += p1;
-        hw[i] = pack_bf16(p0, p1);
-        const __nv_bfloat162 hv = *reinterpret_cast<const __nv_bfloat162*>(&hw[i]);
-        lw[i] = pack_bf16(p0 - __low2float(hv), p1 - __high2float(hv));
+        if constexpr (FP8) {
+          hw[i] = pack_f16(p0, p1);
+        } else {
+          hw[i] = pack_bf16(p0, p1);
+          const __nv_bfloat162 hv = *reinterpret_cast<const __nv_bfloat162*>(&hw[i]);
+          lw[i] = pack_bf16(p0 - __low2float(hv), p1 - __high2float(hv));
+        }
       }
       tmem_st16_nowait(ts, hw);
       tmem_st16_nowait(ts + 16, hw + 16);
-      tmem_st16_nowait(ts + 32, lw);
-      tmem_st16_nowait(ts + 48, lw + 16);
+      if constexpr (!FP8) {
+        tmem_st16_nowait(ts + 32, lw);
+        tmem_st16_nowait(ts + 48, lw + 16);
+      }
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&p_full[b]);
@@ -387,7 +466,7 @@ __global__ void __launch_bounds__(TmemPrefixGeom<D, BS>::kThreads)
       const int s = s0 + (live ? row / g : 0);
       const int64_t hq = static_cast<int64_t>(s) * p.num_heads + h * g + (live ? row % g : 0);
       float* dst = p.tmp_out + (hq * p.np_max + part) * D;
-      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const float inv = l > 0.f ? (FP8 ? p.v_scale[h] : 1.f) / l : 0.f;
 #pragma unroll 1
       for (int c = 0; c < D; c += 16) {
         float ov[16];
@@ -404,15 +483,65 @@ __global__ void __launch_bounds__(TmemPrefixGeom<D, BS>::kThreads)
         p.exp_sums[hq * p.np_max + part] = l;
       }
     }
+  } else if constexpr (FP8) {
+    // converters (warps 7-10): staged codes of K (kind 0) or V (kind 1) of a
+    // step -> f16 operand stage, in the order the MMAs need them (K of step
+    // t + 1 before V of step t, as the producers load them)
+    const int ct = threadIdx.x - 7 * 32;
+    constexpr int kUnitsRow = D / 16;  // 16-code units of one row
+    auto convert = [&](int kind, int st) -> bool {
+      const int b = st & 1;                       // staging stage
+      const int n = kind == 0 ? NK : NV;
+      const int bo = st % n;                      // operand stage
+      if (!__all_sync(0xffffffffu,
+                      mbar_wait(kind == 0 ? &k8_full[b] : &v8_full[b], (st >> 1) & 1, p.err)))
+        return false;
+      // the operand stage was last read by S (K) or P.V (V) of step st - n
+      if (st >= n && !__all_sync(0xffffffffu, mbar_wait(kind == 0 ? &k_empty[bo] : &v_empty[bo],
+                                                        ((st / n) - 1) & 1, p.err)))
+        return false;
+      const int np = min(NP, nblk - st * NP);
+      const uint32_t src0 = (kind == 0 ? k8ring : v8ring) + b * G::kGroup8;
+      for (int i = ct; i < np * BS * kUnitsRow; i += 32 * G::kConvWarps) {
+        const int g16 = i % kUnitsRow;  // dims 16 g16 .. 16 g16 + 15
+        const int row = i / kUnitsRow;  // row of the step: page row / BS
+        const int q = row / BS, r = row % BS;
+        // staged page [128-code chunk][BS rows][128 B]; operand [64-dim chunk]..
+        const uint32_t src =
+            swz128(src0 + q * G::kPage8 + (g16 >> 3) * (BS * 128) + r * 128 + (g16 & 7) * 16);
+        const uint32_t dst = kind == 0
+                                 ? kring + bo * G::kGroup + (g16 >> 2) * G::kChunk + row * 128
+                                 : vring + bo * G::kGroup + q * G::kPage + (g16 >> 2) * (BS * 128) +
+                                       r * 128;
+        const uint32_t u = 2 * (g16 & 3);
+        convert_unit_e4m3(src, swz128(dst + u * 16), swz128(dst + (u + 1) * 16));
+      }
+      // the tensor core reads the stage through the async proxy
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(kind == 0 ? &k_full[bo] : &v_full[bo]);
+        mbar_arrive(kind == 0 ? &k8_empty[b] : &v8_empty[b]);
+      }
+      return true;
+    };
+    bool ok = nsteps > 0 && convert(0, 0);
+    for (int st = 0; st < nsteps && ok; ++st) {
+      if (st + 1 < nsteps) ok = convert(0, st + 1);
+      if (ok) ok = convert(1, st);
+    }
   }
   tc_fence_before();
   __syncthreads();
   if ((warp == 0 || warp == 6) && lane == 0) {
     // no copy may still be writing this CTA's shared memory when it exits
-    for (int st = max(0, k_issued - 2); st < k_issued; ++st)
-      if (!mbar_wait(&k_full[st & 1], (st >> 1) & 1, p.err)) break;
-    for (int st = max(0, v_issued - 2); st < v_issued; ++st)
-      if (!mbar_wait(&v_full[st & 1], (st >> 1) & 1, p.err)) break;
+    uint64_t* kf = FP8 ? k8_full : k_full;
+    uint64_t* vf = FP8 ? v8_full : v_full;
+    const int nk = FP8 ? 2 : NK, nv = FP8 ? 2 : NV;
+    for (int st = max(0, k_issued - nk); st < k_issued; ++st)
+      if (!mbar_wait(&kf[st % nk], (st / nk) & 1, p.err)) break;
+    for (int st = max(0, v_issued - nv); st < v_issued; ++st)
+      if (!mbar_wait(&vf[st % nv], (st / nv) & 1, p.err)) break;
   }
   if (warp == 1) {
     tc_fence_after();
@@ -420,12 +549,12 @@ __global__ void __launch_bounds__(TmemPrefixGeom<D, BS>::kThreads)
   }
 }
 
-template <int D, int BS>
+template <int D, int BS, bool FP8>
 static int launch_prefix_tmem_t(const PrefixParams& p, const CUtensorMap& tk,
                                 const CUtensorMap& tv, dim3 grid, cudaStream_t st) {
-  using G = TmemPrefixGeom<D, BS>;
+  using G = TmemPrefixGeom<D, BS, FP8>;
   static DeviceFlags done;
-  auto kern = prefix_tmem_kernel<D, BS>;
+  auto kern = prefix_tmem_kernel<D, BS, FP8>;
   if (p.partition_blocks <= 0 || p.partition_blocks > G::kMaxIds) return PKV_ERR_UNSUPPORTED;
   int rc = ensure_smem(kern, G::kSmem + 4 * G::kMaxIds, done);
   if (rc != PKV_OK) return rc;
@@ -434,18 +563,31 @@ static int launch_prefix_tmem_t(const PrefixParams& p, const CUtensorMap& tk,
   return launch_status();
 }
 
-int launch_prefix(const PrefixParams& p, const void* k_cache, const void* v_cache, int head_dim,
-                  int block_size, dim3 grid, cudaStream_t st) {
+template <bool FP8>
+static int dispatch_prefix(const PrefixParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
+                           int head_dim, int block_size, dim3 grid, cudaStream_t st) {
+  if (head_dim == 256 && block_size == 16)
+    return launch_prefix_tmem_t<256, 16, FP8>(p, tk, tv, grid, st);
+  if (head_dim == 256 && block_size == 32)
+    return launch_prefix_tmem_t<256, 32, FP8>(p, tk, tv, grid, st);
+  if (head_dim == 128 && block_size == 16)
+    return launch_prefix_tmem_t<128, 16, FP8>(p, tk, tv, grid, st);
+  return launch_prefix_tmem_t<128, 32, FP8>(p, tk, tv, grid, st);
+}
+
+static int launch_prefix(const PrefixParams& p, const void* k_cache, const void* v_cache,
+                         int head_dim, int block_size, bool fp8, dim3 grid, cudaStream_t st) {
   const int64_t rows = static_cast<int64_t>(p.num_blocks) * p.num_kv_heads * block_size;
   CUtensorMap tk, tv;
-  int rc = pool_tensor_map(&tk, k_cache, rows, head_dim, block_size, false);
+  // bf16: K by 2-D boxes (one per page and 128-byte chunk, into the step's
+  // [chunk][64 rows][128 B] operand), V by whole pages; FP8: both by whole
+  // pages into the staging ring
+  int rc = pool_tensor_map(&tk, k_cache, rows, head_dim, block_size, fp8, fp8);
   if (rc != PKV_OK) return rc;
-  rc = pool_tensor_map(&tv, v_cache, rows, head_dim, block_size, false, true);
+  rc = pool_tensor_map(&tv, v_cache, rows, head_dim, block_size, fp8, true);
   if (rc != PKV_OK) return rc;
-  if (head_dim == 256 && block_size == 16) return launch_prefix_tmem_t<256, 16>(p, tk, tv, grid, st);
-  if (head_dim == 256 && block_size == 32) return launch_prefix_tmem_t<256, 32>(p, tk, tv, grid, st);
-  if (head_dim == 128 && block_size == 16) return launch_prefix_tmem_t<128, 16>(p, tk, tv, grid, st);
-  return launch_prefix_tmem_t<128, 32>(p, tk, tv, grid, st);
+  return fp8 ? dispatch_prefix<true>(p, tk, tv, head_dim, block_size, grid, st)
+             : dispatch_prefix<false>(p, tk, tv, head_dim, block_size, grid, st);
 }
 
 }  // namespace pkv
@@ -517,6 +659,7 @@ extern "C" int pkv_shared_prefix_partition_size(int num_groups, int max_group_me
 
 extern "C" int pkv_paged_attention_decode_shared_prefix(
     void* out, const void* q, const void* k_cache, const void* v_cache, pkv_cache_desc cache,
+    const float* k_scale, const float* v_scale,
     const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
     int num_seqs, int num_heads, int max_own_context, float scale, const int32_t* group_start,
     int num_groups, int max_group_members, const int32_t* prefix_blocks, int max_prefix_blocks,
@@ -524,7 +667,7 @@ extern "C" int pkv_paged_attention_decode_shared_prefix(
   using namespace pkv;
   int rc = check_cache_desc(cache);
   if (rc != PKV_OK) return rc;
-  if (cache.dtype != PKV_DTYPE_BF16) return PKV_ERR_UNSUPPORTED;
+  const bool fp8 = cache.dtype == PKV_DTYPE_FP8_E4M3;
   if (num_seqs < 0 || num_heads <= 0 || max_own_context < 0 || max_blocks_per_seq <= 0 ||
       num_groups < 0 || max_prefix_blocks < 0 || partition_size <= 0)
     return PKV_ERR_INVALID_ARG;
@@ -544,6 +687,8 @@ extern "C" int pkv_paged_attention_decode_shared_prefix(
     return PKV_ERR_INVALID_ARG;
   if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
     return PKV_ERR_INVALID_ARG;
+  if (fp8 && (!k_scale || !v_scale)) return PKV_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return PKV_ERR_INVALID_ARG;
   if (num_seqs > 65535 || num_groups > 65535) return PKV_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(cache.num_blocks) * cache.num_kv_heads * cache.block_size >=
       (int64_t{1} << 31))
@@ -580,6 +725,8 @@ extern "C" int pkv_paged_attention_decode_shared_prefix(
     pp.block_tables = block_tables;
     pp.group_start = group_start;
     pp.prefix_blocks = prefix_blocks;
+    pp.k_scale = k_scale;
+    pp.v_scale = v_scale;
     pp.tmp_out = tmp;
     pp.max_logits = ml;
     pp.exp_sums = es;
@@ -595,7 +742,7 @@ extern "C" int pkv_paged_attention_decode_shared_prefix(
     pp.members_per_tile = 128 / g;
     pp.max_members = max_group_members;
     pp.qscale = scale * 1.4426950408889634f;
-    rc = launch_prefix(pp, k_cache, v_cache, cache.head_dim, cache.block_size,
+    rc = launch_prefix(pp, k_cache, v_cache, cache.head_dim, cache.block_size, fp8,
                        dim3(npp * tiles, cache.num_kv_heads, num_groups), st);
     if (rc != PKV_OK) return rc;
   }
@@ -605,6 +752,8 @@ extern "C" int pkv_paged_attention_decode_shared_prefix(
   p.q = static_cast<const uint16_t*>(q);
   p.k_cache = static_cast<const uint8_t*>(k_cache);
   p.v_cache = static_cast<const uint8_t*>(v_cache);
+  p.k_scale = k_scale;
+  p.v_scale = v_scale;
   p.block_tables = block_tables;
   p.context_lens = context_lens;
   p.err = device_error_ptr();
@@ -622,7 +771,7 @@ extern "C" int pkv_paged_attention_decode_shared_prefix(
   p.block_offset = prefix_blocks;
   p.slot_offset = npp;
   p.overlap_prev = (num_groups > 0 && npp > 0) ? 1 : 0;
-  rc = launch_decode_tc(p, k_cache, v_cache, cache.head_dim, cache.block_size, false,
+  rc = launch_decode_tc(p, k_cache, v_cache, cache.head_dim, cache.block_size, fp8,
                         dim3(nps, cache.num_kv_heads, num_seqs), st);
   if (rc != PKV_OK) return rc;
   // 3. merge prefix and own partials

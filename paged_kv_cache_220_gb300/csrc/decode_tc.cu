@@ -68,8 +68,12 @@ struct TcGeom {
   static constexpr int kDW = D / NW;       // head-dim columns per consumer warp
   static constexpr int kKW = kDW / 16;     // their k-steps (and 16-row tiles of O^T)
   static_assert(kKW >= 1 && (!FP8 || kKW % 2 == 0), "consumer warp column slice");
-  // logit partials of one slice, double buffered: [2][NW][32 lanes] float4
-  static constexpr int kXchg = 2 * NW * 32 * 16;
+  // tokens whose logits are exchanged and put through the softmax at once:
+  // a whole 32-row FP8 page, else 16 rows
+  static constexpr int kSlice = (FP8 && BS == 32) ? 32 : 16;
+  static constexpr int kNH = kSlice / 16;  // 16-row halves of a slice
+  // logit partials of one slice, double buffered: [2][NW][kNH][32 lanes] float4
+  static constexpr int kXchg = 2 * NW * kNH * 32 * 16;
   // cluster merge: CTA state [8][D] + max/sum
   static constexpr int kMerge = 8 * D * 4 + 2 * 8 * 4;
   static constexpr int kSmem = 1024 /*barriers*/ + 1024 /*alignment*/ +
@@ -226,58 +230,75 @@ __global__ void __launch_bounds__(TcGeom<D, BS, FP8, NW, NST>::kThreads)
                          : "memory");
         __syncwarp();
       }
+      // one slice = kNH 16-row halves: their logits are exchanged once and
+      // go through one max / rescale step of the online softmax
+      constexpr int NH = G::kNH;
 #pragma unroll 1
-      for (int r0 = 0; r0 < BS; r0 += 16, ++slice) {
-        // ---- partial S^T = K_slice . Q^T over this warp's columns
-        float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
-        const int arow = r0 + (lane & 7) + ((lane >> 3) & 1) * 8;
-        if constexpr (!FP8) {
-          const int acol = (lane >> 4) * 16;  // bytes
+      for (int r0 = 0; r0 < BS; r0 += G::kSlice, ++slice) {
+        // ---- partial S^T = K_rows . Q^T over this warp's columns, per half
+        float sp[NH][4];
 #pragma unroll
-          for (int kk = 0; kk < KW; ++kk) {
-            uint32_t a0, a1, a2, a3;
-            ldsm_x4(swz_bytes<BS>(kp, arow, (kw0 + kk) * 32 + acol), a0, a1, a2, a3);
-            mma_bf16((kk & 1) ? sb : sa, a0, a1, a2, a3, bq[kk][0], bq[kk][1]);
-          }
-        } else {
-          // one x4 load covers 16 rows x 32 codes = two k-steps; each b16 lane
-          // element holds two codes, converted exactly to f16
-          const int acol = (lane >> 4) * 16;
+        for (int hh = 0; hh < NH; ++hh) {
+          float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+          const int arow = r0 + 16 * hh + (lane & 7) + ((lane >> 3) & 1) * 8;
+          if constexpr (!FP8) {
+            const int acol = (lane >> 4) * 16;  // bytes
 #pragma unroll
-          for (int kk = 0; kk < KW; kk += 2) {
-            uint32_t m0r, m1r, m2r, m3r;
-            ldsm_x4(swz_bytes<BS>(kp, arow, (kw0 + kk) * 16 + acol), m0r, m1r, m2r, m3r);
-            mma_f16(sa, e4m3x2_f16x2(m0r, 0), e4m3x2_f16x2(m1r, 0), e4m3x2_f16x2(m0r, 1),
-                    e4m3x2_f16x2(m1r, 1), bq[kk][0], bq[kk][1]);
-            mma_f16(sb, e4m3x2_f16x2(m2r, 0), e4m3x2_f16x2(m3r, 0), e4m3x2_f16x2(m2r, 1),
-                    e4m3x2_f16x2(m3r, 1), bq[kk + 1][0], bq[kk + 1][1]);
+            for (int kk = 0; kk < KW; ++kk) {
+              uint32_t a0, a1, a2, a3;
+              ldsm_x4(swz_bytes<BS>(kp, arow, (kw0 + kk) * 32 + acol), a0, a1, a2, a3);
+              mma_bf16((kk & 1) ? sb : sa, a0, a1, a2, a3, bq[kk][0], bq[kk][1]);
+            }
+          } else {
+            // one x4 load covers 16 rows x 32 codes = two k-steps; each b16
+            // lane element holds two codes, converted exactly to f16
+            const int acol = (lane >> 4) * 16;
+#pragma unroll
+            for (int kk = 0; kk < KW; kk += 2) {
+              uint32_t m0r, m1r, m2r, m3r;
+              ldsm_x4(swz_bytes<BS>(kp, arow, (kw0 + kk) * 16 + acol), m0r, m1r, m2r, m3r);
+              mma_f16(sa, e4m3x2_f16x2(m0r, 0), e4m3x2_f16x2(m1r, 0), e4m3x2_f16x2(m0r, 1),
+                      e4m3x2_f16x2(m1r, 1), bq[kk][0], bq[kk][1]);
+              mma_f16(sb, e4m3x2_f16x2(m2r, 0), e4m3x2_f16x2(m3r, 0), e4m3x2_f16x2(m2r, 1),
+                      e4m3x2_f16x2(m3r, 1), bq[kk + 1][0], bq[kk + 1][1]);
+            }
           }
+#pragma unroll
+          for (int i = 0; i < 4; ++i) sp[hh][i] = sa[i] + sb[i];
         }
         // ---- exchange: every warp sums the NW partials in warp order
         const int xb = slice & 1;
-        xs[(xb * NW + warp) * 32 + lane] =
-            make_float4(sa[0] + sb[0], sa[1] + sb[1], sa[2] + sb[2], sa[3] + sb[3]);
+#pragma unroll
+        for (int hh = 0; hh < NH; ++hh)
+          xs[((xb * NW + warp) * NH + hh) * 32 + lane] =
+              make_float4(sp[hh][0], sp[hh][1], sp[hh][2], sp[hh][3]);
         mbar_arrive(&xfull[xb]);
         if (!__all_sync(0xffffffffu, mbar_wait(&xfull[xb], (slice >> 1) & 1, p.err))) {
           ok = false;
           break;
         }
-        float sv[4] = {0.f, 0.f, 0.f, 0.f};
+        // ---- online softmax on the fragments: rows = tokens, cols = queries
+        float sc[NH][4];
+        float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < NW; ++w) {
-          const float4 x = xs[(xb * NW + w) * 32 + lane];
-          sv[0] += x.x;
-          sv[1] += x.y;
-          sv[2] += x.z;
-          sv[3] += x.w;
+        for (int hh = 0; hh < NH; ++hh) {
+          float sv[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int w = 0; w < NW; ++w) {
+            const float4 x = xs[((xb * NW + w) * NH + hh) * 32 + lane];
+            sv[0] += x.x;
+            sv[1] += x.y;
+            sv[2] += x.z;
+            sv[3] += x.w;
+          }
+          const int t0 = r0 + 16 * hh + (lane >> 2), t1 = t0 + 8;
+          sc[hh][0] = t0 < ntok ? sv[0] * qs : -INFINITY;
+          sc[hh][1] = t0 < ntok ? sv[1] * qs : -INFINITY;
+          sc[hh][2] = t1 < ntok ? sv[2] * qs : -INFINITY;
+          sc[hh][3] = t1 < ntok ? sv[3] * qs : -INFINITY;
+          mx0 = fmaxf(mx0, fmaxf(sc[hh][0], sc[hh][2]));
+          mx1 = fmaxf(mx1, fmaxf(sc[hh][1], sc[hh][3]));
         }
-        // ---- online softmax on the fragment: rows = tokens, cols = queries
-        const int t0 = r0 + (lane >> 2), t1 = t0 + 8;
-        const float s00 = t0 < ntok ? sv[0] * qs : -INFINITY;
-        const float s01 = t0 < ntok ? sv[1] * qs : -INFINITY;
-        const float s10 = t1 < ntok ? sv[2] * qs : -INFINITY;
-        const float s11 = t1 < ntok ? sv[3] * qs : -INFINITY;
-        float mx0 = fmaxf(s00, s10), mx1 = fmaxf(s01, s11);
 #pragma unroll
         for (int off = 4; off < 32; off <<= 1) {
           mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
@@ -298,53 +319,58 @@ __global__ void __launch_bounds__(TcGeom<D, BS, FP8, NW, NST>::kThreads)
           m0 = mn0;
           m1 = mn1;
         }
-        // every slice has a valid token in row 0 of the CTA's first page, so
-        // m is finite from the first slice on and masked logits give p = 0
-        const float p00 = fast_exp2(s00 - m0), p01 = fast_exp2(s01 - m1);
-        const float p10 = fast_exp2(s10 - m0), p11 = fast_exp2(s11 - m1);
-        l0 += p00 + p10;
-        l1 += p01 + p11;
-        if constexpr (!FP8) {
-          // ---- P = P_hi + P_lo in bf16, transposed into the B operand
-          const uint32_t hi_t = pack_bf16(p00, p01), hi_b = pack_bf16(p10, p11);
-          const __nv_bfloat162 ht = *reinterpret_cast<const __nv_bfloat162*>(&hi_t);
-          const __nv_bfloat162 hb = *reinterpret_cast<const __nv_bfloat162*>(&hi_b);
-          const uint32_t lo_t = pack_bf16(p00 - __low2float(ht), p01 - __high2float(ht));
-          const uint32_t lo_b = pack_bf16(p10 - __low2float(hb), p11 - __high2float(hb));
-          const uint32_t bh0 = movm_t(hi_t), bh1 = movm_t(hi_b);
-          const uint32_t bl0 = movm_t(lo_t), bl1 = movm_t(lo_b);
-          // ---- O^T += V_slice^T . P^T over this warp's columns, V^T
-          // fragments by ldmatrix.trans
-          const int vrow = r0 + (lane & 7) + ((lane >> 4) & 1) * 8;
-          const int vcol = ((lane >> 3) & 1) * 16;  // bytes
 #pragma unroll
-          for (int kk = 0; kk < KW; ++kk) {
-            uint32_t a0, a1, a2, a3;
-            ldsm_x4_t(swz_bytes<BS>(vp, vrow, (kw0 + kk) * 32 + vcol), a0, a1, a2, a3);
-            mma_bf16(o[kk], a0, a1, a2, a3, bh0, bh1);
-            mma_bf16(o[kk], a0, a1, a2, a3, bl0, bl1);
-          }
-        } else {
-          // ---- P in f16 (11-bit mantissa), transposed into the B operand
-          const uint32_t b0 = movm_t(pack_f16(p00, p01)), b1 = movm_t(pack_f16(p10, p11));
-          // ---- O^T += V_slice^T . P^T. A transposed x4 load of 16 tokens x 32
-          // codes gives each lane, per 8x8 b16 matrix, two tokens (2(lane%4),
-          // +1) of the dim pair (2j, 2j+1), j = lane/4; a byte permute puts
-          // each dim's two tokens in one half, converted exactly to f16x2. The
-          // even dims form one A operand (row j: dim 2j of the 32 columns, row
-          // j+8: dim 16+2j), the odd dims the next one.
-          const int vrow2 = r0 + (lane & 7) + ((lane >> 3) & 1) * 8;
-          const int vcol = (lane >> 4) * 16;
+        for (int hh = 0; hh < NH; ++hh) {
+          const int rh = r0 + 16 * hh;  // first row of this half
+          // every slice has a valid token in row 0 of the CTA's first page, so
+          // m is finite from the first slice on and masked logits give p = 0
+          const float p00 = fast_exp2(sc[hh][0] - m0), p01 = fast_exp2(sc[hh][1] - m1);
+          const float p10 = fast_exp2(sc[hh][2] - m0), p11 = fast_exp2(sc[hh][3] - m1);
+          l0 += p00 + p10;
+          l1 += p01 + p11;
+          if constexpr (!FP8) {
+            // ---- P = P_hi + P_lo in bf16, transposed into the B operand
+            const uint32_t hi_t = pack_bf16(p00, p01), hi_b = pack_bf16(p10, p11);
+            const __nv_bfloat162 ht = *reinterpret_cast<const __nv_bfloat162*>(&hi_t);
+            const __nv_bfloat162 hb = *reinterpret_cast<const __nv_bfloat162*>(&hi_b);
+            const uint32_t lo_t = pack_bf16(p00 - __low2float(ht), p01 - __high2float(ht));
+            const uint32_t lo_b = pack_bf16(p10 - __low2float(hb), p11 - __high2float(hb));
+            const uint32_t bh0 = movm_t(hi_t), bh1 = movm_t(hi_b);
+            const uint32_t bl0 = movm_t(lo_t), bl1 = movm_t(lo_b);
+            // ---- O^T += V_rows^T . P^T over this warp's columns, V^T
+            // fragments by ldmatrix.trans
+            const int vrow = rh + (lane & 7) + ((lane >> 4) & 1) * 8;
+            const int vcol = ((lane >> 3) & 1) * 16;  // bytes
 #pragma unroll
-          for (int kk = 0; kk < KW; kk += 2) {
-            uint32_t m0r, m1r, m2r, m3r;
-            ldsm_x4_t(swz_bytes<BS>(vp, vrow2, (kw0 + kk) * 16 + vcol), m0r, m1r, m2r, m3r);
-            const uint32_t t0 = pair_tokens(m0r), t1 = pair_tokens(m1r);
-            const uint32_t t2 = pair_tokens(m2r), t3 = pair_tokens(m3r);
-            mma_f16(o[kk], e4m3x2_f16x2(t0, 0), e4m3x2_f16x2(t2, 0), e4m3x2_f16x2(t1, 0),
-                    e4m3x2_f16x2(t3, 0), b0, b1);
-            mma_f16(o[kk + 1], e4m3x2_f16x2(t0, 1), e4m3x2_f16x2(t2, 1), e4m3x2_f16x2(t1, 1),
-                    e4m3x2_f16x2(t3, 1), b0, b1);
+            for (int kk = 0; kk < KW; ++kk) {
+              uint32_t a0, a1, a2, a3;
+              ldsm_x4_t(swz_bytes<BS>(vp, vrow, (kw0 + kk) * 32 + vcol), a0, a1, a2, a3);
+              mma_bf16(o[kk], a0, a1, a2, a3, bh0, bh1);
+              mma_bf16(o[kk], a0, a1, a2, a3, bl0, bl1);
+            }
+          } else {
+            // ---- P in f16 (11-bit mantissa), transposed into the B operand
+            const uint32_t b0 = movm_t(pack_f16(p00, p01)), b1 = movm_t(pack_f16(p10, p11));
+            // ---- O^T += V_rows^T . P^T. A transposed x4 load of 16 tokens x
+            // 32 codes gives each lane, per 8x8 b16 matrix, two tokens
+            // (2(lane%4), +1) of the dim pair (2j, 2j+1), j = lane/4; a byte
+            // permute puts each dim's two tokens in one half, converted
+            // exactly to f16x2. The even dims form one A operand (row j: dim
+            // 2j of the 32 columns, row j+8: dim 16+2j), the odd dims the next
+            // one.
+            const int vrow2 = rh + (lane & 7) + ((lane >> 3) & 1) * 8;
+            const int vcol = (lane >> 4) * 16;
+#pragma unroll
+            for (int kk = 0; kk < KW; kk += 2) {
+              uint32_t m0r, m1r, m2r, m3r;
+              ldsm_x4_t(swz_bytes<BS>(vp, vrow2, (kw0 + kk) * 16 + vcol), m0r, m1r, m2r, m3r);
+              const uint32_t t0 = pair_tokens(m0r), t1 = pair_tokens(m1r);
+              const uint32_t t2 = pair_tokens(m2r), t3 = pair_tokens(m3r);
+              mma_f16(o[kk], e4m3x2_f16x2(t0, 0), e4m3x2_f16x2(t2, 0), e4m3x2_f16x2(t1, 0),
+                      e4m3x2_f16x2(t3, 0), b0, b1);
+              mma_f16(o[kk + 1], e4m3x2_f16x2(t0, 1), e4m3x2_f16x2(t2, 1), e4m3x2_f16x2(t1, 1),
+                      e4m3x2_f16x2(t3, 1), b0, b1);
+            }
           }
         }
       }

@@ -31,6 +31,12 @@ __host__ __device__ constexpr uint32_t umma_idesc_bf16(int M, int N, bool b_mn_m
          (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// The same with f16 A and B.
+__host__ __device__ constexpr uint32_t umma_idesc_f16(int M, int N, bool b_mn_major) {
+  return (1u << 4) | ((b_mn_major ? 1u : 0u) << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(M >> 4) << 24);
+}
+
 // D[tmem] (+)= A[tmem] . B[smem]; issued by one thread. A (M = 128 rows x K)
 // sits in tensor memory with row i in lane i and the bf16 pair (2c, 2c + 1)
 // of the row in column c (low half first).

@@ -438,7 +438,8 @@ def step_shared_prefix(pw: PagedWorkload, out: List[torch.Tensor], groups, works
                                           groups.group_start, groups.prefix_blocks,
                                           groups.max_prefix_blocks, P,
                                           groups.max_group_members, out=out[layer],
-                                          workspace=workspace, stream=stream)
+                                          workspace=workspace, k_scale=st.k_scale,
+                                          v_scale=st.v_scale, stream=stream)
 
 
 # ---- several GPUs: sequences are independent, so every rank runs its own

@@ -88,10 +88,12 @@ def test_one_call_and_shared_prefix_validation(lib):
     assert f(*args(P=24)) == pkv.PKV_ERR_INVALID_ARG             # not a multiple of B
     assert f(*args(maxc=1025)) == pkv.PKV_ERR_INVALID_ARG        # beyond the table
     g = lib.pkv_paged_attention_decode_shared_prefix
-    sp = lambda **kw: [FAKE, FAKE, FAKE, FAKE, _desc(), FAKE, 64, FAKE, kw.get("S", 4), 8,
+    sp = lambda **kw: [FAKE, FAKE, FAKE, FAKE, kw.get("desc", _desc()), kw.get("ks", None),
+                       kw.get("vs", None), FAKE, 64, FAKE, kw.get("S", 4), 8,
                        kw.get("own", 100), 0.088, FAKE, kw.get("G", 1), kw.get("mm", 4), FAKE,
                        kw.get("mp", 2), kw.get("P", 64), kw.get("ws", None), 0, None]
     assert g(*sp(S=0)) == pkv.PKV_OK
+    assert g(*sp(desc=_desc(dt=1))) == pkv.PKV_ERR_INVALID_ARG      # E4M3 without scales
     assert g(*sp(mm=0)) == pkv.PKV_ERR_INVALID_ARG               # groups need a member bound
     assert g(*sp(mm=5)) == pkv.PKV_ERR_INVALID_ARG               # more members than sequences
     assert g(*sp(own=64 * 16 + 1)) == pkv.PKV_ERR_INVALID_ARG    # own part beyond the table

@@ -129,13 +129,19 @@ def test_split_partials_match_oracle(fp8, B, P, _lib):
         assert np.all(np.isnan(ml[s, :, n:])) and np.all(np.isnan(tmp[s, :, n:]))
 
 
-@pytest.mark.parametrize("prompt,prompts,rollouts,P", [(2040, 2, 16, 512), (1024, 8, 4, 64),
-                                                      (300, 2, 32, 64)])
-def test_shared_prefix_slots_match_oracle(prompt, prompts, rollouts, P, _lib):
+@pytest.mark.parametrize("prompt,prompts,rollouts,P,fp8", [(2040, 2, 16, 512, False),
+                                                          (1024, 8, 4, 64, False),
+                                                          (300, 2, 32, 64, False),
+                                                          (1024, 8, 4, 64, True),
+                                                          (300, 2, 32, 64, True)])
+def test_shared_prefix_slots_match_oracle(prompt, prompts, rollouts, P, fp8, _lib):
     w = synth.cow(prompt_len=prompt, prompts=prompts, rollouts=rollouts)
     comp = w.extra["completion"]
-    w = dataclasses.replace(w, ctx=[prompt + (c % 700) + 1 for c in comp])
+    w = dataclasses.replace(w, ctx=[prompt + (c % 700) + 1 for c in comp], fp8=fp8)
     pw = workload.build(w)
+    ks = vs = None
+    if fp8:
+        ks, vs = host_fp8_scales(w, 0)
     gr = workload.prefix_groups(pw)
     st = pw.layers[0]
     B = w.block_size
@@ -149,11 +155,13 @@ def test_shared_prefix_slots_match_oracle(prompt, prompts, rollouts, P, _lib):
     NPT = NPP + NPS
     ws = pkv.shared_prefix_workspace(S, Hq, D, gr.max_own_context, gr.max_prefix_blocks * B, P)
     ws.view(torch.float32).fill_(float("nan"))
-    pkv.kv_cache_write(st.k_new, st.v_new, pw.slot_mapping, st.k_cache, st.v_cache)
+    pkv.kv_cache_write(st.k_new, st.v_new, pw.slot_mapping, st.k_cache, st.v_cache,
+                       st.k_scale, st.v_scale)
     pkv.paged_attention_shared_prefix(st.q, st.k_cache, st.v_cache, pw.block_tables,
                                       pw.context_lens, w.scale, gr.max_own_context,
                                       gr.group_start, gr.prefix_blocks, gr.max_prefix_blocks, P,
-                                      gr.max_group_members, workspace=ws)
+                                      gr.max_group_members, workspace=ws, k_scale=st.k_scale,
+                                      v_scale=st.v_scale)
     torch.cuda.synchronize()
     assert int(_lib.item()) == 0
     tmp, ml, es = _views(ws, S, Hq, NPT, D)
@@ -164,12 +172,13 @@ def test_shared_prefix_slots_match_oracle(prompt, prompts, rollouts, P, _lib):
         t_pre = int(pre[s]) * B
         npre = -(-t_pre // Pp)
         nown = -(-(w.ctx[s] - t_pre) // P)
-        kk, vv = _oracle_rows(w, rows, 0, t_pre)
-        rm, rl, ro = oracle.decode_partials(q[s:s + 1], [kk], [vv], w.scale, Pp, NPP)
+        sc = (ks.astype(np.float64), vs.astype(np.float64)) if fp8 else ()
+        kk, vv = _oracle_rows(w, rows, 0, t_pre, ks, vs)
+        rm, rl, ro = oracle.decode_partials(q[s:s + 1], [kk], [vv], w.scale, Pp, NPP, *sc)
         _check_slots((tmp[s], ml[s], es[s]), (ro[0], rm[0], rl[0]),
                      [(p, p) for p in range(npre)], "seq %d shared" % s, exact_max=False)
-        kk, vv = _oracle_rows(w, rows, t_pre, w.ctx[s])
-        rm, rl, ro = oracle.decode_partials(q[s:s + 1], [kk], [vv], w.scale, P, NPS)
+        kk, vv = _oracle_rows(w, rows, t_pre, w.ctx[s], ks, vs)
+        rm, rl, ro = oracle.decode_partials(q[s:s + 1], [kk], [vv], w.scale, P, NPS, *sc)
         _check_slots((tmp[s], ml[s], es[s]), (ro[0], rm[0], rl[0]),
                      [(NPP + p, p) for p in range(nown)], "seq %d own" % s)
         assert np.all(np.isnan(ml[s, :, npre:NPP])) and np.all(np.isnan(ml[s, :, NPP + nown:]))

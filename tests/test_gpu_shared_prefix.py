@@ -2,6 +2,7 @@
 per group; the output matches the oracle and the plain split decode."""
 import dataclasses
 
+import numpy as np
 import pytest
 import torch
 
@@ -9,7 +10,8 @@ import oracle
 import paged_kv_cache_220_gb300 as pkv
 from paged_kv_cache_220_gb300 import build as pkv_build
 from paged_kv_cache_220_gb300 import synth, workload
-from _oracle_side import MAX_ABS, REL_L2, assert_close, bits16, errors, expected, host_rows
+from _oracle_side import (MAX_ABS, REL_L2, assert_close, bits16, errors, expected,
+                          host_fp8_scales, host_rows)
 
 pytestmark = pytest.mark.gpu
 
@@ -166,3 +168,33 @@ def test_shared_prefix_group_above_declared_bound(_lib):
         vs.append(bits16(V)[t0:])
     own_only = oracle.decode(q, ks, vs, w.scale)
     assert_close(got[uncovered], own_only, "uncovered members: own rows only")
+
+
+@pytest.mark.parametrize("prompt,B,P,rollouts,d", [(40, 16, 32, 4, 256), (2040, 16, 512, 16, 256),
+                                                    (200, 32, 64, 3, 256), (300, 16, 64, 32, 256),
+                                                    (330, 32, 128, 5, 128), (100, 32, 64, 8, 128)])
+def test_shared_prefix_fp8_matches_oracle(prompt, B, P, rollouts, d, _lib):
+    """E4M3 pools: the shared pages' codes become f16 operands of the
+    group product; the result matches the oracle on the same codes (scales
+    recomputed on the host) and the plain split decode over the same pool."""
+    w = synth.cow(prompt_len=prompt, prompts=2, rollouts=rollouts)
+    comp = w.extra["completion"][:2 * rollouts]
+    w = dataclasses.replace(w, block_size=B, head_dim=d, fp8=True,
+                            ctx=[prompt + (c % 300) + 1 for c in comp], slack_blocks=64)
+    pw = workload.build(w)
+    st = pw.layers[0]
+    ks, vs = host_fp8_scales(w, 0)
+    assert np.array_equal(ks.view(np.uint32), st.k_scale.cpu().numpy().view(np.uint32))
+    groups = workload.prefix_groups(pw)
+    assert groups.max_prefix_blocks == prompt // B
+    out = [torch.empty_like(st.q)]
+    workload.step_shared_prefix(pw, out, groups, None, P)
+    torch.cuda.synchronize()
+    assert int(_lib.item()) == 0
+    ref = expected(w, 0, range(w.num_seqs), ks, vs)
+    assert_close(out[0].cpu(), ref, "fp8 shared prefix %d" % prompt)
+    plain = pkv.paged_attention(st.q, st.k_cache, st.v_cache, pw.block_tables, pw.context_lens,
+                                w.scale, pw.max_context, P, st.k_scale, st.v_scale)
+    torch.cuda.synchronize()
+    ma, rl = errors(out[0].cpu(), plain.cpu().double().numpy())
+    assert ma <= MAX_ABS and rl <= REL_L2
