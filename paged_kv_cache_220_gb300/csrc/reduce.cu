@@ -161,11 +161,26 @@ __global__ void __launch_bounds__(kRowWarps * 32) reduce_rows_kernel(
     int partition_size, const int32_t* __restrict__ prefix_blocks, int block_size,
     int slot_split, int prefix_partition, int* err) {
   constexpr int V4 = D / 128;  // float4 per lane per partition row
+  constexpr int U = 4;         // partitions' loads in flight per lane
   wait_prerequisite();  // the partials come from the decode launched before
   const int lane = threadIdx.x & 31;
   const int64_t row = static_cast<int64_t>(blockIdx.x) * kRowWarps + (threadIdx.x >> 5);
   if (row >= num_rows) return;
   const int s = static_cast<int>(row / num_heads);
+  // One round of loads before anything depends on the row's lengths: the
+  // maximum and sum of every slot (lane j: slot j) and the partials of
+  // slots 0 .. U-1. All are inside the row's np_max slots, so reading slots
+  // the row does not use is harmless; they are simply not used.
+  const float m_raw = lane < np_max ? max_logits[row * np_max + lane] : -INFINITY;
+  const float l_raw = lane < np_max ? exp_sums[row * np_max + lane] : 0.f;
+  const float4* src = reinterpret_cast<const float4*>(tmp_out + row * np_max * D);
+  float4 x[U][V4];
+#pragma unroll
+  for (int u = 0; u < U; ++u)
+#pragma unroll
+    for (int v = 0; v < V4; ++v)
+      x[u][v] = u < np_max ? src[static_cast<int64_t>(u) * (D / 4) + lane + 32 * v]
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
   int npre, nsuf;
   row_slots(context_lens, prefix_blocks, s, partition_size, block_size, prefix_partition,
             slot_split, np_max, err, lane == 0, npre, nsuf);
@@ -177,8 +192,12 @@ __global__ void __launch_bounds__(kRowWarps * 32) reduce_rows_kernel(
     return;
   }
   auto slot_of = [&](int v) { return v < npre ? v : slot_split + (v - npre); };
-  const float m = lane < np ? max_logits[row * np_max + slot_of(lane)] : -INFINITY;
-  const float l = lane < np ? exp_sums[row * np_max + slot_of(lane)] : 0.f;
+  // partition i of the row is slot slot_of(i): its max and sum from that lane
+  const int sl = lane < np ? slot_of(lane) : 0;
+  const float m_sl = __shfl_sync(0xffffffffu, m_raw, sl & 31);
+  const float l_sl = __shfl_sync(0xffffffffu, l_raw, sl & 31);
+  const float m = lane < np ? m_sl : -INFINITY;
+  const float l = lane < np ? l_sl : 0.f;
   float M = m;
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
@@ -188,19 +207,29 @@ __global__ void __launch_bounds__(kRowWarps * 32) reduce_rows_kernel(
   for (int off = 16; off > 0; off >>= 1) W += __shfl_xor_sync(0xffffffffu, W, off);
   const float r = w / W;
 
-  const float4* src = reinterpret_cast<const float4*>(tmp_out + row * np_max * D);
   float4 acc[V4];
 #pragma unroll
   for (int v = 0; v < V4; ++v) acc[v] = make_float4(0.f, 0.f, 0.f, 0.f);
-  constexpr int U = 4;
   for (int i0 = 0; i0 < np; i0 += U) {
-    float4 x[U][V4];
+    if (i0 > 0) {
 #pragma unroll
-    for (int u = 0; u < U; ++u)
+      for (int u = 0; u < U; ++u)
 #pragma unroll
-      for (int v = 0; v < V4; ++v)
-        x[u][v] = i0 + u < np ? src[static_cast<int64_t>(slot_of(i0 + u)) * (D / 4) + lane + 32 * v]
-                              : make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int v = 0; v < V4; ++v)
+          x[u][v] = i0 + u < np
+                        ? src[static_cast<int64_t>(slot_of(i0 + u)) * (D / 4) + lane + 32 * v]
+                        : make_float4(0.f, 0.f, 0.f, 0.f);
+    } else {
+      // the first U partitions were loaded as slots 0 .. U-1; a partition
+      // stored elsewhere (shared-prefix rows) is loaded now
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+        if (u < np && slot_of(u) != u) {
+#pragma unroll
+          for (int v = 0; v < V4; ++v)
+            x[u][v] = src[static_cast<int64_t>(slot_of(u)) * (D / 4) + lane + 32 * v];
+        }
+    }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const float ru = __shfl_sync(0xffffffffu, r, (i0 + u) & 31);
