@@ -2,6 +2,9 @@
 
 python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
 
+NAME: qwen_like (default), tiny, mixed, cow, cow2040, cow2040_fp8 (the 2040-token rollouts
+over an E4M3 cache), long_fp8.
+
 A step is one pass of the whole hot path over the workload's batch: for every
 layer the new token's K/V are written into their slots (kv_cache_write), the
 split decode attends over the paged cache (paged_attention_decode) and the
@@ -49,6 +52,8 @@ def workload_for(name: str):
         "mixed": lambda: synth.mixed(),
         "cow": lambda: synth.cow(prompt_len=2048),
         "cow2040": lambda: synth.cow(prompt_len=2040),
+        "cow2040_fp8": lambda: __import__("dataclasses").replace(
+            synth.cow(prompt_len=2040), fp8=True, name="cow_shared_prefix_2040_fp8"),
         "long_fp8": lambda: synth.long_fp8(),
     }
     w = table[name]()

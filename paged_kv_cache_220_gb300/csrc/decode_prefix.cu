@@ -67,13 +67,13 @@ struct PrefixParams {
 // on the way. K of a step is laid out [128-byte chunk][64 rows][128 B] (the
 // N = 64 operand needs the rows of all its pages at one stride), which takes
 // one TMA box per page and chunk; V is laid out page by page and takes one
-// 3-D box per page. A TMA instruction costs its issuing thread ~100 cycles,
-// so two producer warps share the pages of each step. Each issues K of step
-// t + 1 before V of step t: K(t+1) waits for S(t-1), V(t) for P.V(t-2), which
-// completes later.
+// 3-D box per page. A TMA instruction costs its issuing thread ~100-200
+// cycles, so several producer warps share the pages of each step. Each
+// issues K of step t + 1 before V of step t: K(t+1) waits for S(t-1), V(t)
+// for P.V(t-2), which completes later.
 //
-// Warps: 0 and 6 load pages (TMA), 1 owns tensor memory and issues the MMAs
-// (one thread), 2-5 run the softmax: thread t of warp w owns query row
+// Warps: 0, 6 (and 7, 8 for bf16) load pages (TMA), 1 owns tensor memory and
+// issues the MMAs (one thread), 2-5 run the softmax: thread t of warp w owns query row
 // 32*(w%4) + t, so row maxima and sums need no shuffles. O is rescaled only
 // when a row maximum grows by more than 2^8 (the final O / l uses the same
 // reference, so the result does not depend on when that happens). P carries
@@ -81,8 +81,8 @@ struct PrefixParams {
 // other kernels.
 //
 // E4M3 pools (FP8): the products run on f16 operands. TMA brings a step's
-// pages (codes) into a staging ring of two stages; four converter warps
-// (7-10) turn every code into its exact f16 value and store it where the
+// pages (codes) into a staging ring of two stages; eight converter warps
+// (7-14) turn every code into its exact f16 value and store it where the
 // bf16 path's TMA would have put a page element, in the same swizzled
 // layout, then make the stores visible to the tensor core (proxy fence) and
 // release the staging stage. Q is converted to f16 once (exact in f16's
@@ -105,8 +105,12 @@ struct TmemPrefixGeom {
   static constexpr int kNV = 2;               // V stages
   static constexpr int kSmem = 1024 + 1024 + (kNK + kNV) * kGroup + kStage8;  // + the block ids
   static constexpr int kMaxIds = 2048;                     // partition_blocks limit
-  static constexpr int kConvWarps = FP8 ? 4 : 0;
-  static constexpr int kThreads = (7 + kConvWarps) * 32;
+  static constexpr int kConvWarps = FP8 ? 8 : 0;
+  // TMA producers: a 2-D K box costs its issuing thread ~200 cycles, and a
+  // step takes 16 of them, so bf16 steps are loaded by four warps (warps 0, 6,
+  // 7, 8), one page each; FP8 steps take 8 whole-page boxes (two warps)
+  static constexpr int kProducers = FP8 ? 2 : 4;
+  static constexpr int kThreads = (5 + kProducers + kConvWarps) * 32;
   static constexpr uint32_t kColS = D;              // S of step t at kColS + 64 * (t & 1)
   static constexpr uint32_t kColQ = D + 2 * kTok;   // Q: k-step k at kColQ + 8 k
   static constexpr uint32_t kUsed = kColQ + D / 2;
@@ -207,18 +211,18 @@ __global__ void __launch_bounds__(TmemPrefixGeom<D, BS, FP8>::kThreads)
     // bf16: one arrival per producer warp (with the bytes); FP8: one per
     // converter warp, the producers' arrivals go to the staging barriers
     for (int i = 0; i < NK; ++i) {
-      mbar_init(&k_full[i], FP8 ? G::kConvWarps : 2);
+      mbar_init(&k_full[i], FP8 ? G::kConvWarps : G::kProducers);
       mbar_init(&k_empty[i], 1);
     }
     for (int i = 0; i < NV; ++i) {
-      mbar_init(&v_full[i], FP8 ? G::kConvWarps : 2);
+      mbar_init(&v_full[i], FP8 ? G::kConvWarps : G::kProducers);
       mbar_init(&v_empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       if constexpr (FP8) {
-        mbar_init(&k8_full[i], 2);
+        mbar_init(&k8_full[i], G::kProducers);
         mbar_init(&k8_empty[i], G::kConvWarps);
-        mbar_init(&v8_full[i], 2);
+        mbar_init(&v8_full[i], G::kProducers);
         mbar_init(&v8_empty[i], G::kConvWarps);
       }
       mbar_init(&s_full[i], 1);
@@ -251,9 +255,11 @@ __global__ void __launch_bounds__(TmemPrefixGeom<D, BS, FP8>::kThreads)
   const uint32_t t_q = tmem + G::kColQ;
 
   int k_issued = 0, v_issued = 0;  // producer lanes 0 only
-  if (warp == 0 || warp == 6) {
+  // producer index: warp 0 -> 0, warp 6 -> 1, bf16 warps 7, 8 -> 2, 3
+  const int prod = warp == 0 ? 0 : (warp >= 6 && warp < 5 + G::kProducers) ? warp - 5 : -1;
+  if (prod >= 0) {
     if (lane == 0) {
-      const int half = warp == 0 ? 0 : 1;  // this producer's pages: q % 2 == half
+      const int half = prod;  // this producer's pages: q % kProducers == prod
       // K (kind 0) or V (kind 1) of step st into stage st % N (N = NK or
       // NV); the stage was last read by S (K) or P.V (V) of step st - N.
       // FP8: the copies go to the two-stage staging ring, released by the
@@ -268,9 +274,9 @@ __global__ void __launch_bounds__(TmemPrefixGeom<D, BS, FP8>::kThreads)
         if (st >= n && !mbar_wait(empty, ((st / n) - 1) & 1, p.err)) return false;
         const int np = min(NP, nblk - st * NP);
         int good = 0;
-        for (int q = half; q < np; q += 2) good += ids[st * NP + q] >= 0 ? 1 : 0;
+        for (int q = half; q < np; q += G::kProducers) good += ids[st * NP + q] >= 0 ? 1 : 0;
         mbar_arrive_expect_tx(full, good * (FP8 ? G::kPage8 : G::kPage));
-        for (int q = half; q < np; q += 2) {
+        for (int q = half; q < np; q += G::kProducers) {
           const int32_t pb = ids[st * NP + q];
           if (pb < 0) continue;
           const int y = (pb * p.num_kv_heads + h) * BS;
@@ -316,8 +322,8 @@ __global__ void __launch_bounds__(TmemPrefixGeom<D, BS, FP8>::kThreads)
           const uint32_t kp = kring + bk * G::kGroup;
 #pragma unroll
           for (int k = 0; k < KT; ++k) {
-            const uint64_t bk = umma_sdesc(kp + (k >> 2) * G::kChunk + (k & 3) * 32, 16, 1024, 2);
-            umma_bf16_ta(t_s + b * G::kTok, t_q + 8 * k, bk, idesc_qk, k > 0 ? 1u : 0u);
+            const uint64_t kd = umma_sdesc(kp + (k >> 2) * G::kChunk + (k & 3) * 32, 16, 1024, 2);
+            umma_bf16_ta(t_s + b * G::kTok, t_q + 8 * k, kd, idesc_qk, k > 0 ? 1u : 0u);
           }
           umma_commit(&s_full[b]);
           umma_commit(&k_empty[bk]);
@@ -334,9 +340,9 @@ __global__ void __launch_bounds__(TmemPrefixGeom<D, BS, FP8>::kThreads)
             // V rows 16 kk .. 16 kk + 15 of the step: page kk / (B/16), page
             // layout [chunk][B rows][128 B]
             const uint32_t va = vp + (kk / (BS / 16)) * G::kPage + (kk % (BS / 16)) * 2048;
-            const uint64_t bv = umma_sdesc(va, BS * 128, 1024, 2);
-            umma_bf16_ta(t_o, ph + 8 * kk, bv, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
-            if constexpr (!FP8) umma_bf16_ta(t_o, ph + 32 + 8 * kk, bv, idesc_pv, 1u);
+            const uint64_t vd = umma_sdesc(va, BS * 128, 1024, 2);
+            umma_bf16_ta(t_o, ph + 8 * kk, vd, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+            if constexpr (!FP8) umma_bf16_ta(t_o, ph + 32 + 8 * kk, vd, idesc_pv, 1u);
           }
           umma_commit(&o_done[b]);
           umma_commit(&v_empty[bv]);
@@ -484,10 +490,10 @@ __global__ void __launch_bounds__(TmemPrefixGeom<D, BS, FP8>::kThreads)
       }
     }
   } else if constexpr (FP8) {
-    // converters (warps 7-10): staged codes of K (kind 0) or V (kind 1) of a
+    // converters (warps 7-14): staged codes of K (kind 0) or V (kind 1) of a
     // step -> f16 operand stage, in the order the MMAs need them (K of step
     // t + 1 before V of step t, as the producers load them)
-    const int ct = threadIdx.x - 7 * 32;
+    const int ct = threadIdx.x - (5 + G::kProducers) * 32;
     constexpr int kUnitsRow = D / 16;  // 16-code units of one row
     auto convert = [&](int kind, int st) -> bool {
       const int b = st & 1;                       // staging stage
@@ -533,7 +539,7 @@ __global__ void __launch_bounds__(TmemPrefixGeom<D, BS, FP8>::kThreads)
   }
   tc_fence_before();
   __syncthreads();
-  if ((warp == 0 || warp == 6) && lane == 0) {
+  if (prod >= 0 && lane == 0) {
     // no copy may still be writing this CTA's shared memory when it exits
     uint64_t* kf = FP8 ? k8_full : k_full;
     uint64_t* vf = FP8 ? v8_full : v_full;
