@@ -384,6 +384,7 @@ def measure_other(name, steps=10, warmup=3):
     """A short run of another workload, for the same JSON line: device-timed
     step (graph replay) after `warmup` steps, the decode kernel's launch time
     from an eager pass, clocks sampled during the timed steps."""
+    import dataclasses
     import torch
     import paged_kv_cache_220_gb300 as pkv
     from paged_kv_cache_220_gb300 import workload
@@ -396,6 +397,10 @@ def measure_other(name, steps=10, warmup=3):
     cascade = None
     if w.prefix_len > 0 and P:
         cascade = workload.prefix_groups(pw)
+        # own parts: the split size without a nearly empty last partition
+        P = pkv.split_partition_size(cascade.max_own_context, w.block_size, P)
+        w = dataclasses.replace(w, partition_size=P)
+        pw.w = w
         ws = pkv.shared_prefix_workspace(w.num_seqs, w.num_heads, w.head_dim,
                                          cascade.max_own_context,
                                          cascade.max_prefix_blocks * w.block_size, P)
@@ -543,6 +548,11 @@ def main():
     cascade = None
     if w.prefix_len > 0 and args.shared_prefix and P:
         cascade = workload.prefix_groups(pw)
+        # own parts: the split size without a nearly empty last partition
+        # (1033-token own parts at 512: 528, two partitions instead of three)
+        P = pkv.split_partition_size(cascade.max_own_context, w.block_size, P)
+        w = dataclasses.replace(w, partition_size=P)
+        pw.w = w
         ws = pkv.shared_prefix_workspace(w.num_seqs, w.num_heads, w.head_dim,
                                          cascade.max_own_context,
                                          cascade.max_prefix_blocks * w.block_size, P)

@@ -153,6 +153,19 @@ int pkv_kv_cache_write(const void* k, const void* v, const int64_t* slot_mapping
 size_t pkv_decode_workspace_bytes(int num_seqs, int num_heads, int head_dim,
                                   int max_context, int partition_size);
 
+/* Host helper: a split size near partition_size without a nearly empty last
+ * partition. With n = max(1, round(max_context / partition_size)) (halves
+ * round up), the result is the smallest multiple of block_size that covers
+ * max_context in n partitions, so the longest context takes n partitions of
+ * about equal length instead of, e.g., two full ones and a few-token third
+ * (1033 tokens at P = 512, B = 16: 528, two partitions). It equals
+ * partition_size whenever partition_size divides max_context. Any result is
+ * a valid partition_size for the calls above (size the workspace with it).
+ * Returns partition_size if max_context <= 0, PKV_ERR_INVALID_ARG if
+ * block_size <= 0 or partition_size is not a positive multiple of it. (The
+ * pages leave the split size open; this is a load-balancing choice.) */
+int pkv_split_partition_size(int max_context, int block_size, int partition_size);
+
 int pkv_paged_attention_decode(void* out, const void* q, const void* k_cache,
                                const void* v_cache, pkv_cache_desc cache,
                                const float* k_scale, const float* v_scale,

@@ -67,6 +67,7 @@ _lib = None
 SIGNATURES = {
     "pkv_kv_cache_write": (_I, [_P, _P, _P, _I, _P, _P, CacheDesc, _P, _P, _P]),
     "pkv_decode_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I, _I, _I]),
+    "pkv_split_partition_size": (_I, [_I, _I, _I]),
     "pkv_paged_attention_decode": (_I, [_P, _P, _P, _P, CacheDesc, _P, _P, _P, _I, _P, _I, _I,
                                         _I, ctypes.c_float, _I, _P, ctypes.c_size_t, _P]),
     "pkv_paged_attention_reduce": (_I, [_P, _P, ctypes.c_size_t, _P, _I, _I, _I, _I, _I, _P]),
@@ -203,6 +204,15 @@ def kv_cache_write(k, v, slot_mapping, k_cache, v_cache, k_scale=None, v_scale=N
 def decode_workspace_bytes(num_seqs, num_heads, head_dim, max_context, partition_size) -> int:
     return int(lib().pkv_decode_workspace_bytes(num_seqs, num_heads, head_dim, max_context,
                                                 partition_size))
+
+
+def split_partition_size(max_context, block_size, partition_size) -> int:
+    """A split size near partition_size without a nearly empty last
+    partition (see pkv_split_partition_size)."""
+    rc = lib().pkv_split_partition_size(int(max_context), int(block_size), int(partition_size))
+    if rc < 0:
+        _check(rc, "split_partition_size")
+    return int(rc)
 
 
 def alloc_workspace(num_seqs, num_heads, head_dim, max_context, partition_size,

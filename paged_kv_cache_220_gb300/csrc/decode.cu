@@ -12,6 +12,8 @@
 // Split form (partition_size > 0): a CTA covers logical blocks
 // [p*P/B, (p+1)*P/B) and stores (max logit, exp-sum, normalised output) of its
 // partition; paged_attention_reduce merges them.
+#include <algorithm>
+#include <climits>
 #include <cmath>
 
 #include "common.cuh"
@@ -29,6 +31,17 @@ extern "C" size_t pkv_decode_workspace_bytes(int num_seqs, int num_heads, int he
     return 0;
   const size_t np = (static_cast<size_t>(max_context) + partition_size - 1) / partition_size;
   return static_cast<size_t>(num_seqs) * num_heads * np * (head_dim + 2) * sizeof(float);
+}
+
+extern "C" int pkv_split_partition_size(int max_context, int block_size, int partition_size) {
+  if (block_size <= 0 || partition_size <= 0 || partition_size % block_size != 0)
+    return PKV_ERR_INVALID_ARG;
+  if (max_context <= 0) return partition_size;
+  const int64_t n = std::max<int64_t>(
+      1, (2 * static_cast<int64_t>(max_context) + partition_size) / (2 * partition_size));
+  const int64_t per = (max_context + n - 1) / n;  // tokens per partition
+  const int64_t p = (per + block_size - 1) / block_size * block_size;
+  return static_cast<int>(std::min<int64_t>(p, INT32_MAX / 2));
 }
 
 extern "C" int pkv_paged_attention_decode(void* out, const void* q, const void* k_cache,

@@ -147,3 +147,27 @@ def test_binding_fails_loudly_without_cuda_tensors(lib):
     cache = torch.zeros(8, 2, 16, 128, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         pkv.kv_cache_write(k, k, torch.zeros(4, dtype=torch.int64), cache, cache)
+
+
+def test_split_partition_size(lib):
+    """Covers the longest context in round(max/P) partitions of equal
+    length (a multiple of B); unchanged when P divides the longest context."""
+    f = pkv.split_partition_size
+    assert f(1033, 16, 512) == 528            # 2 partitions instead of 512 + 512 + 9
+    assert f(8192, 16, 1024) == 1024
+    assert f(131072, 32, 512) == 512
+    assert f(16384, 32, 512) == 512
+    assert f(100, 16, 512) == 112             # one partition
+    assert f(0, 16, 512) == 512
+    assert lib.pkv_split_partition_size(100, 16, 24) == pkv.PKV_ERR_INVALID_ARG
+    import random
+    rng = random.Random(3)
+    for _ in range(2000):
+        B = rng.choice([16, 32])
+        P = B * rng.randint(1, 128)
+        m = rng.randint(1, 200000)
+        Q = f(m, B, P)
+        n = max(1, (2 * m + P) // (2 * P))
+        assert Q % B == 0 and Q >= B
+        assert -(-m // Q) <= n                 # at most n partitions
+        assert Q < m / n + B                   # the smallest such multiple of B
