@@ -147,9 +147,11 @@ def test_cow_rollouts(prompt_len, _lib):
                 assert np.array_equal(got, want)
         del kc
     out = _step(pw)[0]
-    # the shared-prefix decode as the benchmark runs it (a replayed CUDA graph)
+    # the shared-prefix decode as the benchmark runs it (a replayed CUDA graph,
+    # own parts split by split_partition_size)
     groups = workload.prefix_groups(pw)
-    P = w.partition_size
+    P = pkv.split_partition_size(groups.max_own_context, w.block_size, w.partition_size)
+    assert P == 528
     ws = pkv.shared_prefix_workspace(w.num_seqs, w.num_heads, w.head_dim, groups.max_own_context,
                                      groups.max_prefix_blocks * w.block_size, P)
     sp = [torch.empty_like(pw.layers[0].q)]
