@@ -100,7 +100,9 @@ struct TmemPrefixGeom {
   static constexpr int kChunk = kTok * 128;   // one 64-column chunk of a step
   static constexpr int kPage8 = BS * D;       // FP8: bytes of one staged page of codes
   static constexpr int kGroup8 = kTok * D;    // FP8: bytes of one staged step of K (or V)
-  static constexpr int kStage8 = FP8 ? 4 * kGroup8 : 0;    // K and V, two stages each
+  static constexpr int kNS8 = 2;              // FP8: staging stages of K and of V
+  static_assert(kNS8 >= 1 && kNS8 <= 2, "two staging barriers of each kind");
+  static constexpr int kStage8 = FP8 ? 2 * kNS8 * kGroup8 : 0;
   static constexpr int kNK = 2;               // K stages (steps) in shared memory
   static constexpr int kNV = 2;               // V stages
   static constexpr int kSmem = 1024 + 1024 + (kNK + kNV) * kGroup + kStage8;  // + the block ids
@@ -165,7 +167,7 @@ __global__ void __launch_bounds__(TmemPrefixGeom<D, BS, FP8>::kThreads)
   const uint32_t kring = base + 1024;            // K stage b at kring + b * kGroup
   const uint32_t vring = kring + NK * G::kGroup; // V stage b at vring + b * kGroup
   const uint32_t k8ring = vring + NV * G::kGroup;  // FP8: staged K stage b at + b * kGroup8
-  const uint32_t v8ring = k8ring + 2 * G::kGroup8;
+  const uint32_t v8ring = k8ring + G::kNS8 * G::kGroup8;
   int32_t* ids =
       reinterpret_cast<int32_t*>(sbase + 1024 + (NK + NV) * G::kGroup + G::kStage8);
   // the members' own-block decode launched next may start on the room this
@@ -265,7 +267,7 @@ __global__ void __launch_bounds__(TmemPrefixGeom<D, BS, FP8>::kThreads)
       // FP8: the copies go to the two-stage staging ring, released by the
       // converters
       auto issue = [&](int kind, int st) -> bool {
-        const int n = FP8 ? 2 : (kind == 0 ? NK : NV);
+        const int n = FP8 ? G::kNS8 : (kind == 0 ? NK : NV);
         const int b = st % n;
         uint64_t* full = FP8 ? (kind == 0 ? &k8_full[b] : &v8_full[b])
                              : (kind == 0 ? &k_full[b] : &v_full[b]);
@@ -496,11 +498,12 @@ __global__ void __launch_bounds__(TmemPrefixGeom<D, BS, FP8>::kThreads)
     const int ct = threadIdx.x - (5 + G::kProducers) * 32;
     constexpr int kUnitsRow = D / 16;  // 16-code units of one row
     auto convert = [&](int kind, int st) -> bool {
-      const int b = st & 1;                       // staging stage
+      const int b = st % G::kNS8;                 // staging stage
       const int n = kind == 0 ? NK : NV;
       const int bo = st % n;                      // operand stage
       if (!__all_sync(0xffffffffu,
-                      mbar_wait(kind == 0 ? &k8_full[b] : &v8_full[b], (st >> 1) & 1, p.err)))
+                      mbar_wait(kind == 0 ? &k8_full[b] : &v8_full[b], (st / G::kNS8) & 1,
+                                p.err)))
         return false;
       // the operand stage was last read by S (K) or P.V (V) of step st - n
       if (st >= n && !__all_sync(0xffffffffu, mbar_wait(kind == 0 ? &k_empty[bo] : &v_empty[bo],
@@ -543,7 +546,7 @@ __global__ void __launch_bounds__(TmemPrefixGeom<D, BS, FP8>::kThreads)
     // no copy may still be writing this CTA's shared memory when it exits
     uint64_t* kf = FP8 ? k8_full : k_full;
     uint64_t* vf = FP8 ? v8_full : v_full;
-    const int nk = FP8 ? 2 : NK, nv = FP8 ? 2 : NV;
+    const int nk = FP8 ? G::kNS8 : NK, nv = FP8 ? G::kNS8 : NV;
     for (int st = max(0, k_issued - nk); st < k_issued; ++st)
       if (!mbar_wait(&kf[st % nk], (st / nk) & 1, p.err)) break;
     for (int st = max(0, v_issued - nv); st < v_issued; ++st)
