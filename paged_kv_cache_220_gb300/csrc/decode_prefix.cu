@@ -1,5 +1,6 @@
 // Shared-prefix decode (the kernel over a group's shared pages and the C entry
 // points that chain it with the split decode and the merge).
+#include <algorithm>
 #include <cmath>
 
 #include "common.cuh"
@@ -91,7 +92,12 @@ struct PrefixParams {
 // keeps the group product on the tensor core: the alternative, E4M3 operands
 // (kind::f8f6f4), would need Q and P in 8-bit form.
 
-template <int D, int BS, bool FP8 = false>
+// LEAN (bf16): one V stage and two producer warps, 99 KB of shared memory
+// and 224 threads instead of 133 KB and 288, so three 38 KB decode CTAs of
+// the members' own blocks fit beside a prefix CTA instead of two. The prefix
+// kernel itself is slower, so this pays only when the own-block decode is
+// the longer of the two (see launch_prefix's caller).
+template <int D, int BS, bool FP8 = false, bool LEAN = false>
 struct TmemPrefixGeom {
   static constexpr int kTok = 64;             // tokens per step (one 64-column load of S)
   static constexpr int kPages = kTok / BS;    // pages per step
@@ -104,14 +110,14 @@ struct TmemPrefixGeom {
   static_assert(kNS8 >= 1 && kNS8 <= 2, "two staging barriers of each kind");
   static constexpr int kStage8 = FP8 ? 2 * kNS8 * kGroup8 : 0;
   static constexpr int kNK = 2;               // K stages (steps) in shared memory
-  static constexpr int kNV = 2;               // V stages
+  static constexpr int kNV = LEAN ? 1 : 2;    // V stages
   static constexpr int kSmem = 1024 + 1024 + (kNK + kNV) * kGroup + kStage8;  // + the block ids
   static constexpr int kMaxIds = 2048;                     // partition_blocks limit
   static constexpr int kConvWarps = FP8 ? 8 : 0;
   // TMA producers: a 2-D K box costs its issuing thread ~200 cycles, and a
   // step takes 16 of them, so bf16 steps are loaded by four warps (warps 0, 6,
   // 7, 8), one page each; FP8 steps take 8 whole-page boxes (two warps)
-  static constexpr int kProducers = FP8 ? 2 : 4;
+  static constexpr int kProducers = (FP8 || LEAN) ? 2 : 4;
   static constexpr int kThreads = (5 + kProducers + kConvWarps) * 32;
   static constexpr uint32_t kColS = D;              // S of step t at kColS + 64 * (t & 1)
   static constexpr uint32_t kColQ = D + 2 * kTok;   // Q: k-step k at kColQ + 8 k
@@ -138,11 +144,11 @@ __device__ __forceinline__ void convert_unit_e4m3(uint32_t src, uint32_t dst0, u
 
 __device__ __forceinline__ uint32_t swz128(uint32_t a) { return a ^ (((a >> 7) & 7u) << 4); }
 
-template <int D, int BS, bool FP8>
-__global__ void __launch_bounds__(TmemPrefixGeom<D, BS, FP8>::kThreads)
+template <int D, int BS, bool FP8, bool LEAN>
+__global__ void __launch_bounds__(TmemPrefixGeom<D, BS, FP8, LEAN>::kThreads)
     prefix_tmem_kernel(const __grid_constant__ CUtensorMap tmk,
                        const __grid_constant__ CUtensorMap tmv, const PrefixParams p) {
-  using G = TmemPrefixGeom<D, BS, FP8>;
+  using G = TmemPrefixGeom<D, BS, FP8, LEAN>;
   constexpr int KT = D / 16;
   constexpr int NP = G::kPages;
   extern __shared__ uint8_t smem_raw[];
@@ -558,12 +564,12 @@ __global__ void __launch_bounds__(TmemPrefixGeom<D, BS, FP8>::kThreads)
   }
 }
 
-template <int D, int BS, bool FP8>
+template <int D, int BS, bool FP8, bool LEAN>
 static int launch_prefix_tmem_t(const PrefixParams& p, const CUtensorMap& tk,
                                 const CUtensorMap& tv, dim3 grid, cudaStream_t st) {
-  using G = TmemPrefixGeom<D, BS, FP8>;
+  using G = TmemPrefixGeom<D, BS, FP8, LEAN>;
   static DeviceFlags done;
-  auto kern = prefix_tmem_kernel<D, BS, FP8>;
+  auto kern = prefix_tmem_kernel<D, BS, FP8, LEAN>;
   if (p.partition_blocks <= 0 || p.partition_blocks > G::kMaxIds) return PKV_ERR_UNSUPPORTED;
   int rc = ensure_smem(kern, G::kSmem + 4 * G::kMaxIds, done);
   if (rc != PKV_OK) return rc;
@@ -572,20 +578,21 @@ static int launch_prefix_tmem_t(const PrefixParams& p, const CUtensorMap& tk,
   return launch_status();
 }
 
-template <bool FP8>
+template <bool FP8, bool LEAN>
 static int dispatch_prefix(const PrefixParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
                            int head_dim, int block_size, dim3 grid, cudaStream_t st) {
   if (head_dim == 256 && block_size == 16)
-    return launch_prefix_tmem_t<256, 16, FP8>(p, tk, tv, grid, st);
+    return launch_prefix_tmem_t<256, 16, FP8, LEAN>(p, tk, tv, grid, st);
   if (head_dim == 256 && block_size == 32)
-    return launch_prefix_tmem_t<256, 32, FP8>(p, tk, tv, grid, st);
+    return launch_prefix_tmem_t<256, 32, FP8, LEAN>(p, tk, tv, grid, st);
   if (head_dim == 128 && block_size == 16)
-    return launch_prefix_tmem_t<128, 16, FP8>(p, tk, tv, grid, st);
-  return launch_prefix_tmem_t<128, 32, FP8>(p, tk, tv, grid, st);
+    return launch_prefix_tmem_t<128, 16, FP8, LEAN>(p, tk, tv, grid, st);
+  return launch_prefix_tmem_t<128, 32, FP8, LEAN>(p, tk, tv, grid, st);
 }
 
 static int launch_prefix(const PrefixParams& p, const void* k_cache, const void* v_cache,
-                         int head_dim, int block_size, bool fp8, dim3 grid, cudaStream_t st) {
+                         int head_dim, int block_size, bool fp8, bool lean, dim3 grid,
+                         cudaStream_t st) {
   const int64_t rows = static_cast<int64_t>(p.num_blocks) * p.num_kv_heads * block_size;
   CUtensorMap tk, tv;
   // bf16: K by 2-D boxes (one per page and 128-byte chunk, into the step's
@@ -595,8 +602,9 @@ static int launch_prefix(const PrefixParams& p, const void* k_cache, const void*
   if (rc != PKV_OK) return rc;
   rc = pool_tensor_map(&tv, v_cache, rows, head_dim, block_size, fp8, true);
   if (rc != PKV_OK) return rc;
-  return fp8 ? dispatch_prefix<true>(p, tk, tv, head_dim, block_size, grid, st)
-             : dispatch_prefix<false>(p, tk, tv, head_dim, block_size, grid, st);
+  if (fp8) return dispatch_prefix<true, false>(p, tk, tv, head_dim, block_size, grid, st);
+  return lean ? dispatch_prefix<false, true>(p, tk, tv, head_dim, block_size, grid, st)
+              : dispatch_prefix<false, false>(p, tk, tv, head_dim, block_size, grid, st);
 }
 
 }  // namespace pkv
@@ -751,7 +759,20 @@ extern "C" int pkv_paged_attention_decode_shared_prefix(
     pp.members_per_tile = 128 / g;
     pp.max_members = max_group_members;
     pp.qscale = scale * 1.4426950408889634f;
-    rc = launch_prefix(pp, k_cache, v_cache, cache.head_dim, cache.block_size, fp8,
+    // The lean prefix CTA (room for a third own-block decode CTA per SM)
+    // when the own-block decode is the longer kernel: from the call's bounds,
+    // its token-heads per SM at least 2.4x a prefix CTA's tokens (both stream
+    // ~1 KB per token-head at d = 256 bf16, ~43 GB/s per SM for the decode,
+    // ~36 GB/s per prefix CTA), i.e. the own decode takes at least twice as
+    // long. GB300, copy-on-write rollouts (512 x 1033-token own parts, 2032-
+    // token prefixes): 0.2247 -> 0.2221 ms; long prompts with short
+    // completions (8 x 8184-token prompts, 16 rollouts, own parts <= 129
+    // tokens) would lose: 0.0762 -> 0.0966 ms, and take the full CTA.
+    const int64_t own_per_sm =
+        static_cast<int64_t>(num_seqs) * cache.num_kv_heads * max_own_context / sms;
+    const int64_t pre_per_cta = std::min<int64_t>(pre_p, pre_tokens);
+    const bool lean = !fp8 && 5 * own_per_sm >= 12 * pre_per_cta;
+    rc = launch_prefix(pp, k_cache, v_cache, cache.head_dim, cache.block_size, fp8, lean,
                        dim3(npp * tiles, cache.num_kv_heads, num_groups), st);
     if (rc != PKV_OK) return rc;
   }
