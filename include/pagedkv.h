@@ -83,6 +83,7 @@ typedef enum { PKV_DTYPE_BF16 = 0, PKV_DTYPE_FP8_E4M3 = 1 } pkv_dtype;
 #define PKV_DEVERR_WAIT_TIMEOUT 3 /* a bounded barrier wait gave up           */
 #define PKV_DEVERR_CONTEXT 4     /* context_len outside [0, max_blocks_per_seq*block_size],
                                     or longer than the call's context bound */
+#define PKV_DEVERR_ORDER 5       /* seq_order entry outside [0, num_seqs)      */
 
 /* Geometry of one layer's K and V pools (both share it). */
 typedef struct {
@@ -148,6 +149,17 @@ int pkv_kv_cache_write(const void* k, const void* v, const int64_t* slot_mapping
  *   workspace, workspace_bytes : device scratch for the split form, at least
  *               pkv_decode_workspace_bytes(...) bytes (ignored when
  *               partition_size == 0; may be NULL then).
+ *   seq_order : NULL, or device int32 [num_seqs], a permutation of
+ *               0..num_seqs-1: the order in which the kernel's CTAs take the
+ *               sequences (the grid's first CTAs work on seq_order[0]). Every
+ *               order gives the same bits; only the schedule changes. With
+ *               contexts of very different lengths, longest first
+ *               (pkv_longest_first_order) starts the long sequences while
+ *               the short ones fill in behind them, instead of leaving a long
+ *               one to run alone at the end of the grid. An entry outside
+ *               [0, num_seqs) is reported as PKV_DEVERR_ORDER and its CTAs
+ *               write nothing; a repeated entry leaves another sequence's
+ *               result unwritten.
  * Errors: PKV_ERR_INVALID_ARG, PKV_ERR_UNSUPPORTED, PKV_ERR_CUDA.
  * ------------------------------------------------------------------------ */
 size_t pkv_decode_workspace_bytes(int num_seqs, int num_heads, int head_dim,
@@ -166,6 +178,13 @@ size_t pkv_decode_workspace_bytes(int num_seqs, int num_heads, int head_dim,
  * pages leave the split size open; this is a load-balancing choice.) */
 int pkv_split_partition_size(int max_context, int block_size, int partition_size);
 
+/* Host helper: order[0..n) = the indices 0..n-1 sorted by lengths[i], longest
+ * first, equal lengths in index order (a stable sort), for the seq_order
+ * arguments below. lengths and order are host arrays of n int32.
+ * Returns PKV_OK; PKV_ERR_INVALID_ARG if n < 0 or (n > 0 and a pointer is
+ * NULL). */
+int pkv_longest_first_order(const int32_t* lengths, int n, int32_t* order);
+
 int pkv_paged_attention_decode(void* out, const void* q, const void* k_cache,
                                const void* v_cache, pkv_cache_desc cache,
                                const float* k_scale, const float* v_scale,
@@ -173,7 +192,8 @@ int pkv_paged_attention_decode(void* out, const void* q, const void* k_cache,
                                const int32_t* context_lens, int num_seqs,
                                int num_heads, int max_context, float scale,
                                int partition_size, void* workspace,
-                               size_t workspace_bytes, void* stream);
+                               size_t workspace_bytes, const int32_t* seq_order,
+                               void* stream);
 
 /* ------------------------------------------------------------------------ *
  * paged_attention_reduce: merge the per-partition partials of a split decode.
@@ -209,7 +229,8 @@ int pkv_paged_attention(void* out, const void* q, const void* k_cache,
                         const int32_t* block_tables, int max_blocks_per_seq,
                         const int32_t* context_lens, int num_seqs, int num_heads,
                         int max_context, float scale, int partition_size,
-                        void* workspace, size_t workspace_bytes, void* stream);
+                        void* workspace, size_t workspace_bytes, const int32_t* seq_order,
+                        void* stream);
 
 /* ------------------------------------------------------------------------ *
  * paged_attention_decode_shared_prefix: decode for groups of sequences that
@@ -262,6 +283,11 @@ int pkv_paged_attention(void* out, const void* q, const void* k_cache,
  *   k_scale, v_scale : device fp32 [num_kv_heads] dequantisation scales of
  *                   an E4M3 pool (required then, else ignored), as for
  *                   pkv_paged_attention_decode
+ *   seq_order     : NULL or a permutation of the sequences, the order in
+ *                   which the own-block decode takes them, as for
+ *                   pkv_paged_attention_decode (there, longest own part
+ *                   first: pkv_longest_first_order of context_lens[s] -
+ *                   prefix_blocks[s]*block_size)
  * Per group, KV head and row tile, a kernel computes partials of the members'
  * query heads over the shared pages (the members' queries form the rows of
  * one tensor-core product; for E4M3 pools the codes are turned into exact f16
@@ -284,7 +310,7 @@ int pkv_paged_attention_decode_shared_prefix(
     const int32_t* context_lens, int num_seqs, int num_heads, int max_own_context,
     float scale, const int32_t* group_start, int num_groups, int max_group_members,
     const int32_t* prefix_blocks, int max_prefix_blocks, int partition_size,
-    void* workspace, size_t workspace_bytes, void* stream);
+    void* workspace, size_t workspace_bytes, const int32_t* seq_order, void* stream);
 
 /* ------------------------------------------------------------------------ *
  * copy_blocks: copy-on-write duplication. Sequences forked from one prompt
@@ -318,8 +344,9 @@ int pkv_copy_blocks(void* k_cache, void* v_cache, pkv_cache_desc cache,
  * holds that array until the process exits.
  *
  * Arguments and result are those of pkv_paged_attention_decode with
- * partition_size > 0 followed by pkv_paged_attention_reduce: `out` receives
- * the merged bf16 output. The caller still passes every input and output.
+ * partition_size > 0 (and seq_order NULL) followed by
+ * pkv_paged_attention_reduce: `out` receives the merged bf16 output. The
+ * caller still passes every input and output.
  *   - Returns PKV_ERR_UNSUPPORTED when the partials,
  *     pkv_decode_workspace_bytes(num_seqs, num_heads, head_dim, max_context,
  *     partition_size), exceed PKV_NOALLOC_SCRATCH_BYTES (use a larger

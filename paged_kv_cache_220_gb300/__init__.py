@@ -45,6 +45,7 @@ DEVERR_BLOCK_ID = 1
 DEVERR_SLOT = 2
 DEVERR_WAIT_TIMEOUT = 3
 DEVERR_CONTEXT = 4
+DEVERR_ORDER = 5
 
 
 class PagedKVError(RuntimeError):
@@ -68,11 +69,12 @@ SIGNATURES = {
     "pkv_kv_cache_write": (_I, [_P, _P, _P, _I, _P, _P, CacheDesc, _P, _P, _P]),
     "pkv_decode_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I, _I, _I]),
     "pkv_split_partition_size": (_I, [_I, _I, _I]),
+    "pkv_longest_first_order": (_I, [_P, _I, _P]),
     "pkv_paged_attention_decode": (_I, [_P, _P, _P, _P, CacheDesc, _P, _P, _P, _I, _P, _I, _I,
-                                        _I, ctypes.c_float, _I, _P, ctypes.c_size_t, _P]),
+                                        _I, ctypes.c_float, _I, _P, ctypes.c_size_t, _P, _P]),
     "pkv_paged_attention_reduce": (_I, [_P, _P, ctypes.c_size_t, _P, _I, _I, _I, _I, _I, _P]),
     "pkv_paged_attention": (_I, [_P, _P, _P, _P, CacheDesc, _P, _P, _P, _I, _P, _I, _I, _I,
-                                 ctypes.c_float, _I, _P, ctypes.c_size_t, _P]),
+                                 ctypes.c_float, _I, _P, ctypes.c_size_t, _P, _P]),
     "pkv_paged_attention_decode_noalloc": (_I, [_P, _P, _P, _P, CacheDesc, _P, _P, _P, _I, _P,
                                                 _I, _I, _I, ctypes.c_float, _I, _P]),
     "pkv_shared_prefix_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I, _I, _I, _I]),
@@ -80,7 +82,7 @@ SIGNATURES = {
     "pkv_paged_attention_decode_shared_prefix": (_I, [_P, _P, _P, _P, CacheDesc, _P, _P, _P, _I,
                                                       _P, _I,
                                                       _I, _I, ctypes.c_float, _P, _I, _I, _P,
-                                                      _I, _I, _P, ctypes.c_size_t, _P]),
+                                                      _I, _I, _P, ctypes.c_size_t, _P, _P]),
     "pkv_copy_blocks": (_I, [_P, _P, CacheDesc, _P, _I, _P]),
     "pkv_swap_out": (_I, [_P, _P, CacheDesc, _P, _I, _P, _P, _P]),
     "pkv_swap_in": (_I, [_P, _P, CacheDesc, _P, _I, _P, _P, _P]),
@@ -221,10 +223,31 @@ def alloc_workspace(num_seqs, num_heads, head_dim, max_context, partition_size,
     return torch.empty(max(n, 16), dtype=torch.uint8, device=device or "cuda")
 
 
+def longest_first_order(lengths) -> np.ndarray:
+    """The indices of `lengths` sorted longest first, ties in index order
+    (int32, host): the seq_order that starts the long sequences first."""
+    a = np.ascontiguousarray(np.asarray(lengths, dtype=np.int32).reshape(-1))
+    order = np.empty(a.shape[0], dtype=np.int32)
+    rc = lib().pkv_longest_first_order(a.ctypes.data_as(_P), int(a.shape[0]),
+                                       order.ctypes.data_as(_P))
+    _check(rc, "longest_first_order")
+    return order
+
+
+def _order_ptr(seq_order, num_seqs):
+    if seq_order is None:
+        return None
+    if tuple(seq_order.shape) != (num_seqs,):
+        raise ValueError("seq_order must be [num_seqs]")
+    return _dev_ptr(seq_order, "seq_order", torch.int32)
+
+
 def paged_attention_decode(out, q, k_cache, v_cache, block_tables, context_lens, scale,
                            max_context, partition_size=0, workspace=None, k_scale=None,
-                           v_scale=None, stream=None) -> None:
-    """One launch of the decode kernel (see pkv_paged_attention_decode)."""
+                           v_scale=None, stream=None, seq_order=None) -> None:
+    """One launch of the decode kernel (see pkv_paged_attention_decode).
+    seq_order: None or a device int32 [S] permutation, the order in which the
+    CTAs take the sequences (see longest_first_order)."""
     desc = cache_desc(k_cache)
     S, Hq, D = q.shape
     if D != desc.head_dim:
@@ -240,7 +263,7 @@ def paged_attention_decode(out, q, k_cache, v_cache, block_tables, context_lens,
         _dev_ptr(block_tables, "block_tables", torch.int32), int(block_tables.shape[1]),
         _dev_ptr(context_lens, "context_lens", torch.int32), S, Hq, int(max_context),
         float(scale), int(partition_size), _dev_ptr(workspace, "workspace"), ws_bytes,
-        _stream(stream))
+        _order_ptr(seq_order, S), _stream(stream))
     _check(rc, "paged_attention_decode")
 
 
@@ -257,10 +280,10 @@ def paged_attention_reduce(out, workspace, context_lens, max_context, partition_
 
 def paged_attention(q, k_cache, v_cache, block_tables, context_lens, scale, max_context,
                     partition_size=0, k_scale=None, v_scale=None, out=None, workspace=None,
-                    stream=None) -> torch.Tensor:
+                    stream=None, seq_order=None) -> torch.Tensor:
     """Decode attention in one C call: the one-pass decode, or the split
     decode followed by the merge of its partitions. Returns out [S, Hq, D]
-    bf16."""
+    bf16. seq_order as for paged_attention_decode."""
     desc = cache_desc(k_cache)
     S, Hq, D = q.shape
     if out is None:
@@ -276,7 +299,7 @@ def paged_attention(q, k_cache, v_cache, block_tables, context_lens, scale, max_
         _dev_ptr(block_tables, "block_tables", torch.int32), int(block_tables.shape[1]),
         _dev_ptr(context_lens, "context_lens", torch.int32), S, Hq, int(max_context),
         float(scale), int(partition_size), _dev_ptr(workspace, "workspace"), wsb,
-        _stream(stream))
+        _order_ptr(seq_order, S), _stream(stream))
     _check(rc, "paged_attention")
     return out
 
@@ -325,11 +348,13 @@ def shared_prefix_partition_size(num_groups, max_group_members, num_kv_heads, nu
 def paged_attention_shared_prefix(q, k_cache, v_cache, block_tables, context_lens, scale,
                                   max_own_context, group_start, prefix_blocks, max_prefix_blocks,
                                   partition_size, max_group_members, out=None, workspace=None,
-                                  k_scale=None, v_scale=None, stream=None) -> torch.Tensor:
+                                  k_scale=None, v_scale=None, stream=None,
+                                  seq_order=None) -> torch.Tensor:
     """Decode of groups sharing prompt blocks (see the C header): shared pages
     are read once per group. group_start int32 [G+1], prefix_blocks int32 [S];
     max_own_context bounds context_lens[s] - prefix_blocks[s] * block_size;
-    max_group_members bounds the members of a group."""
+    max_group_members bounds the members of a group; seq_order, the order of
+    the members' own-block decode (longest own part first pays)."""
     desc = cache_desc(k_cache)
     S, Hq, D = q.shape
     if out is None:
@@ -348,7 +373,7 @@ def paged_attention_shared_prefix(q, k_cache, v_cache, block_tables, context_len
         float(scale), _dev_ptr(group_start, "group_start", torch.int32), G,
         int(max_group_members), _dev_ptr(prefix_blocks, "prefix_blocks", torch.int32),
         int(max_prefix_blocks), int(partition_size), _dev_ptr(workspace, "workspace"),
-        workspace.numel() * workspace.element_size(), _stream(stream))
+        workspace.numel() * workspace.element_size(), _order_ptr(seq_order, S), _stream(stream))
     _check(rc, "paged_attention_decode_shared_prefix")
     return out
 

@@ -44,6 +44,18 @@ extern "C" int pkv_split_partition_size(int max_context, int block_size, int par
   return static_cast<int>(std::min<int64_t>(p, INT32_MAX / 2));
 }
 
+// Longest first: the grid's CTAs are dispatched in index order, so the long
+// sequences start first and the short ones fill the SMs the long ones leave
+// free, instead of one long sequence running on its own at the grid's end
+// (longest-processing-time-first list scheduling).
+extern "C" int pkv_longest_first_order(const int32_t* lengths, int n, int32_t* order) {
+  if (n < 0 || (n > 0 && (!lengths || !order))) return PKV_ERR_INVALID_ARG;
+  for (int i = 0; i < n; ++i) order[i] = i;
+  std::stable_sort(order, order + n,
+                   [lengths](int32_t a, int32_t b) { return lengths[a] > lengths[b]; });
+  return PKV_OK;
+}
+
 extern "C" int pkv_paged_attention_decode(void* out, const void* q, const void* k_cache,
                                           const void* v_cache, pkv_cache_desc cache,
                                           const float* k_scale, const float* v_scale,
@@ -51,7 +63,8 @@ extern "C" int pkv_paged_attention_decode(void* out, const void* q, const void* 
                                           const int32_t* context_lens, int num_seqs,
                                           int num_heads, int max_context, float scale,
                                           int partition_size, void* workspace,
-                                          size_t workspace_bytes, void* stream) {
+                                          size_t workspace_bytes, const int32_t* seq_order,
+                                          void* stream) {
   using namespace pkv;
   int rc = check_cache_desc(cache);
   if (rc != PKV_OK) return rc;
@@ -85,6 +98,7 @@ extern "C" int pkv_paged_attention_decode(void* out, const void* q, const void* 
   p.num_heads = num_heads;
   p.group = group;
   p.max_blocks_per_seq = max_blocks_per_seq;
+  p.seq_order = seq_order;
   p.qscale = scale * kLog2e;
   dim3 grid(1, cache.num_kv_heads, num_seqs);
   if (partition_size == 0) {

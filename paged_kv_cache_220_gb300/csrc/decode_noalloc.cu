@@ -97,7 +97,7 @@ extern "C" int pkv_paged_attention_decode_noalloc(
   rc = pkv_paged_attention_decode(out, q, k_cache, v_cache, cache, k_scale, v_scale, block_tables,
                                   max_blocks_per_seq, context_lens, num_seqs, num_heads,
                                   max_context, scale, partition_size, ws,
-                                  PKV_NOALLOC_SCRATCH_BYTES, stream);
+                                  PKV_NOALLOC_SCRATCH_BYTES, nullptr, stream);
   if (rc != PKV_OK) return rc;
   return pkv_paged_attention_reduce(out, ws, PKV_NOALLOC_SCRATCH_BYTES, context_lens, num_seqs,
                                     num_heads, cache.head_dim, max_context, partition_size,

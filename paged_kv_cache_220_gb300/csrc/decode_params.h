@@ -35,6 +35,9 @@ struct DecodeParams {
   // this launch completes only after the earlier one: work queued behind it
   // sees both results.
   int overlap_prev;
+  // NULL, or the sequence each z index of the grid works on (a permutation of
+  // 0..gridDim.z-1): the CTAs take the sequences in this order
+  const int32_t* seq_order;
   float qscale;          // scale * log2(e)
 };
 

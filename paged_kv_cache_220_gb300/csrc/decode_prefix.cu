@@ -680,7 +680,8 @@ extern "C" int pkv_paged_attention_decode_shared_prefix(
     const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
     int num_seqs, int num_heads, int max_own_context, float scale, const int32_t* group_start,
     int num_groups, int max_group_members, const int32_t* prefix_blocks, int max_prefix_blocks,
-    int partition_size, void* workspace, size_t workspace_bytes, void* stream) {
+    int partition_size, void* workspace, size_t workspace_bytes, const int32_t* seq_order,
+    void* stream) {
   using namespace pkv;
   int rc = check_cache_desc(cache);
   if (rc != PKV_OK) return rc;
@@ -801,6 +802,7 @@ extern "C" int pkv_paged_attention_decode_shared_prefix(
   p.block_offset = prefix_blocks;
   p.slot_offset = npp;
   p.overlap_prev = (num_groups > 0 && npp > 0) ? 1 : 0;
+  p.seq_order = seq_order;
   rc = launch_decode_tc(p, k_cache, v_cache, cache.head_dim, cache.block_size, fp8,
                         dim3(nps, cache.num_kv_heads, num_seqs), st);
   if (rc != PKV_OK) return rc;

@@ -105,15 +105,24 @@ __global__ void __launch_bounds__(TcGeom<D, BS, FP8, NW, NST>::kThreads)
 
   const int part = blockIdx.x;
   const int h = blockIdx.y;
-  const int s = blockIdx.z;
   // overlapped with the kernel before it: thread 0 of CTA (0, 0, 0), which
   // every launch has, keeps the grid alive until that kernel has completed
-  PrerequisiteTail tail{p.overlap_prev != 0 && threadIdx.x == 0 && part == 0 && h == 0 && s == 0};
+  PrerequisiteTail tail{p.overlap_prev != 0 && threadIdx.x == 0 && part == 0 && h == 0 &&
+                        blockIdx.z == 0};
   // launched as a programmatic dependent of the kernel before it (e.g. the
   // cache write): nothing below reads global memory before that kernel has
   // completed, except in the overlapped shared-prefix form, whose inputs the
   // earlier kernel does not write
   if (p.overlap_prev == 0) wait_prerequisite();
+  // the sequence of this z index: the grid takes them in seq_order's order
+  int s = static_cast<int>(blockIdx.z);
+  if (p.seq_order != nullptr) {
+    s = p.seq_order[blockIdx.z];
+    if (s < 0 || s >= static_cast<int>(gridDim.z)) {
+      if (threadIdx.x == 0 && part == 0 && h == 0) report_error(p.err, PKV_DEVERR_ORDER);
+      return;
+    }
+  }
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int g = p.group;

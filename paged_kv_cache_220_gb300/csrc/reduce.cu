@@ -339,11 +339,13 @@ extern "C" int pkv_paged_attention(void* out, const void* q, const void* k_cache
                                    const int32_t* block_tables, int max_blocks_per_seq,
                                    const int32_t* context_lens, int num_seqs, int num_heads,
                                    int max_context, float scale, int partition_size,
-                                   void* workspace, size_t workspace_bytes, void* stream) {
+                                   void* workspace, size_t workspace_bytes,
+                                   const int32_t* seq_order, void* stream) {
   const int rc = pkv_paged_attention_decode(out, q, k_cache, v_cache, cache, k_scale, v_scale,
                                             block_tables, max_blocks_per_seq, context_lens,
                                             num_seqs, num_heads, max_context, scale,
-                                            partition_size, workspace, workspace_bytes, stream);
+                                            partition_size, workspace, workspace_bytes,
+                                            seq_order, stream);
   if (rc != PKV_OK || partition_size == 0) return rc;
   return pkv_paged_attention_reduce(out, workspace, workspace_bytes, context_lens, num_seqs,
                                     num_heads, cache.head_dim, max_context, partition_size,

@@ -50,6 +50,10 @@ class PagedWorkload:
     cow_pairs_host: Optional[np.ndarray] = None
     tables_host: Optional[np.ndarray] = None
     history_slots: Optional[List[np.ndarray]] = None
+    # [S] int32 (device) or None: the order in which step() has the decode
+    # take the sequences (None: batch order; visit_order(w.ctx) gives longest
+    # first)
+    visit_order: Optional[torch.Tensor] = None
 
     @property
     def num_seqs(self):
@@ -191,6 +195,15 @@ def build(w: synth.Workload, device="cuda", layers: Optional[int] = None,
     return pw
 
 
+def visit_order(lengths, device="cuda") -> Optional[torch.Tensor]:
+    """Longest first (pkv.longest_first_order) as a device tensor, or None
+    when all lengths are equal (the identity order needs no table)."""
+    a = np.asarray(lengths, dtype=np.int64)
+    if a.size == 0 or np.all(a == a[0]):
+        return None
+    return torch.as_tensor(pkv.longest_first_order(a), device=device)
+
+
 def step(pw: PagedWorkload, out: List[torch.Tensor], workspace: Optional[torch.Tensor],
          partition_size: Optional[int] = None, stream=None) -> None:
     """One decode step over every layer: write the new token, attend, merge."""
@@ -200,7 +213,8 @@ def step(pw: PagedWorkload, out: List[torch.Tensor], workspace: Optional[torch.T
                            st.k_scale, st.v_scale, stream)
         pkv.paged_attention(st.q, st.k_cache, st.v_cache, pw.block_tables, pw.context_lens,
                             pw.w.scale, pw.max_context, P, st.k_scale, st.v_scale,
-                            out=out[layer], workspace=workspace, stream=stream)
+                            out=out[layer], workspace=workspace, stream=stream,
+                            seq_order=pw.visit_order)
 
 
 def capture_step(pw: PagedWorkload, out: List[torch.Tensor], workspace: Optional[torch.Tensor],
@@ -394,6 +408,9 @@ class PrefixGroups(NamedTuple):
     max_prefix_blocks: int
     max_own_context: int
     max_group_members: int
+    # the members' own-block decode order: longest own part first (None:
+    # all own parts equal)
+    visit_order: Optional[torch.Tensor] = None
 
 
 def prefix_groups(pw: PagedWorkload, device="cuda") -> PrefixGroups:
@@ -401,14 +418,16 @@ def prefix_groups(pw: PagedWorkload, device="cuda") -> PrefixGroups:
     group is the run of leading full blocks whose physical ids every member's
     table has in common (a partly filled prompt block is cloned on divergence
     and so is private); max_own_context is the longest context past its
-    sequence's shared prefix; max_group_members the largest group."""
+    sequence's shared prefix; max_group_members the largest group;
+    visit_order the members' own-block decode order, longest own part
+    first."""
     w = pw.w
     S = w.num_seqs
     ctx = np.asarray(w.ctx, dtype=np.int64)
     if w.prefix_len <= 0:
         return PrefixGroups(torch.zeros(1, dtype=torch.int32, device=device),
                             torch.zeros(S, dtype=torch.int32, device=device), 0,
-                            int(ctx.max()) if S else 0, 1)
+                            int(ctx.max()) if S else 0, 1, visit_order(ctx, device))
     G = w.group
     n_prompt = S // G
     tables = pw.tables_host
@@ -423,7 +442,8 @@ def prefix_groups(pw: PagedWorkload, device="cuda") -> PrefixGroups:
     starts = np.arange(0, n_prompt * G + 1, G, dtype=np.int32)
     own = ctx - pre.astype(np.int64) * w.block_size
     return PrefixGroups(torch.as_tensor(starts, device=device), torch.as_tensor(pre, device=device),
-                        int(pre.max()) if S else 0, int(own.max()) if S else 0, G)
+                        int(pre.max()) if S else 0, int(own.max()) if S else 0, G,
+                        visit_order(own, device))
 
 
 def step_shared_prefix(pw: PagedWorkload, out: List[torch.Tensor], groups, workspace,
@@ -439,7 +459,8 @@ def step_shared_prefix(pw: PagedWorkload, out: List[torch.Tensor], groups, works
                                           groups.max_prefix_blocks, P,
                                           groups.max_group_members, out=out[layer],
                                           workspace=workspace, k_scale=st.k_scale,
-                                          v_scale=st.v_scale, stream=stream)
+                                          v_scale=st.v_scale, stream=stream,
+                                          seq_order=groups.visit_order)
 
 
 # ---- several GPUs: sequences are independent, so every rank runs its own

@@ -107,17 +107,24 @@ static int validation(void) {
   pkv_cache_desc c = {8, 16, 2, 128, PKV_DTYPE_BF16};
   /* group of 9 query heads per KV head: unsupported */
   CHECK(pkv_paged_attention_decode(fake, fake, fake, fake, c, NULL, NULL, fake, 64, fake, 4, 18,
-                                   100, 0.088f, 0, NULL, 0, NULL) == PKV_ERR_UNSUPPORTED,
+                                   100, 0.088f, 0, NULL, 0, NULL, NULL) == PKV_ERR_UNSUPPORTED,
         "group 9");
   /* split form without a workspace */
   CHECK(pkv_paged_attention_decode(fake, fake, fake, fake, c, NULL, NULL, fake, 64, fake, 4, 8,
-                                   100, 0.088f, 64, NULL, 0, NULL) == PKV_ERR_INVALID_ARG,
+                                   100, 0.088f, 64, NULL, 0, NULL, NULL) == PKV_ERR_INVALID_ARG,
         "no workspace");
   CHECK(pkv_paged_attention_reduce(fake, NULL, 0, fake, 4, 8, 96, 100, 64, NULL) ==
             PKV_ERR_UNSUPPORTED,
         "head_dim 96");
   CHECK(pkv_copy_blocks(fake, fake, c, NULL, 3, NULL) == PKV_ERR_INVALID_ARG, "no pairs");
   CHECK(pkv_split_partition_size(1033, 16, 512) == 528, "split size");
+  {
+    const int32_t lens[5] = {3, 9, 1, 9, 5};
+    int32_t order[5];
+    CHECK(pkv_longest_first_order(lens, 5, order) == PKV_OK && order[0] == 1 && order[1] == 3 &&
+              order[2] == 4 && order[3] == 0 && order[4] == 2,
+          "longest first");
+  }
   CHECK(pkv_decode_workspace_bytes(8, 24, 256, 131072, 512) ==
             (size_t)8 * 24 * 256 * (256 + 2) * 4,
         "workspace bytes");

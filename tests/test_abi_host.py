@@ -4,6 +4,7 @@ import ctypes
 import os
 import re
 
+import numpy as np
 import pytest
 
 import paged_kv_cache_220_gb300 as pkv
@@ -30,6 +31,14 @@ def test_every_declared_symbol_is_exported(lib):
     for n in names:
         assert hasattr(lib, n), n
     assert set(names) == set(pkv.SIGNATURES), set(names) ^ set(pkv.SIGNATURES)
+
+
+def test_device_error_codes_match_the_header():
+    src = open(os.path.join(ROOT, "include", "pagedkv.h")).read()
+    codes = dict(re.findall(r"#define PKV_(DEVERR_[A-Z_]+)\s+(\d+)", src))
+    assert len(codes) >= 6
+    for name, value in codes.items():
+        assert getattr(pkv, name) == int(value), name
 
 
 def test_version_and_status_strings(lib):
@@ -63,7 +72,7 @@ def test_decode_validation(lib):
     args = lambda **kw: [kw.get("out", FAKE), FAKE, FAKE, FAKE, kw.get("desc", _desc()), None, None,
                          FAKE, kw.get("mb", 64), FAKE, kw.get("S", 4), kw.get("Hq", 8),
                          kw.get("maxc", 1024), kw.get("scale", 0.088), kw.get("P", 0),
-                         kw.get("ws", None), kw.get("wsb", 0), None]
+                         kw.get("ws", None), kw.get("wsb", 0), None, None]
     assert f(*args(S=0)) == pkv.PKV_OK
     assert f(*args(Hq=7)) == pkv.PKV_ERR_INVALID_ARG           # not a multiple of Hk
     assert f(*args(Hq=18)) == pkv.PKV_ERR_UNSUPPORTED          # group 9
@@ -82,7 +91,7 @@ def test_one_call_and_shared_prefix_validation(lib):
     f = lib.pkv_paged_attention
     args = lambda **kw: [FAKE, FAKE, FAKE, FAKE, _desc(), None, None, FAKE, 64, FAKE,
                          kw.get("S", 4), 8, kw.get("maxc", 1024), 0.088, kw.get("P", 512),
-                         kw.get("ws", None), kw.get("wsb", 0), None]
+                         kw.get("ws", None), kw.get("wsb", 0), None, None]
     assert f(*args(S=0)) == pkv.PKV_OK
     assert f(*args()) == pkv.PKV_ERR_INVALID_ARG                 # no workspace
     assert f(*args(P=24)) == pkv.PKV_ERR_INVALID_ARG             # not a multiple of B
@@ -91,7 +100,7 @@ def test_one_call_and_shared_prefix_validation(lib):
     sp = lambda **kw: [FAKE, FAKE, FAKE, FAKE, kw.get("desc", _desc()), kw.get("ks", None),
                        kw.get("vs", None), FAKE, 64, FAKE, kw.get("S", 4), 8,
                        kw.get("own", 100), 0.088, FAKE, kw.get("G", 1), kw.get("mm", 4), FAKE,
-                       kw.get("mp", 2), kw.get("P", 64), kw.get("ws", None), 0, None]
+                       kw.get("mp", 2), kw.get("P", 64), kw.get("ws", None), 0, None, None]
     assert g(*sp(S=0)) == pkv.PKV_OK
     assert g(*sp(desc=_desc(dt=1))) == pkv.PKV_ERR_INVALID_ARG      # E4M3 without scales
     assert g(*sp(mm=0)) == pkv.PKV_ERR_INVALID_ARG               # groups need a member bound
@@ -108,6 +117,23 @@ def test_one_call_and_shared_prefix_validation(lib):
     assert q(1, 0, 2, 8, 16, 4, 64) == pkv.PKV_ERR_INVALID_ARG    # no member bound
     assert q(1, 4, 2, 8, 16, 4, 24) == pkv.PKV_ERR_INVALID_ARG    # P not a multiple of B
     assert q(1, 4, 2, 18, 16, 4, 64) == pkv.PKV_ERR_UNSUPPORTED   # group 9
+
+
+def test_longest_first_order(lib):
+    """Indices sorted by length, longest first, equal lengths in index order
+    (stable): checked against a brute-force stable sort and a hand case."""
+    assert pkv.longest_first_order([3, 9, 1, 9, 5]).tolist() == [1, 3, 4, 0, 2]
+    assert pkv.longest_first_order([]).tolist() == []
+    rng = np.random.default_rng(5)
+    for n in (1, 2, 17, 512):
+        lens = rng.integers(0, 8, size=n)            # many ties
+        got = pkv.longest_first_order(lens)
+        want = sorted(range(n), key=lambda i: (-int(lens[i]), i))
+        assert got.dtype == np.int32 and got.tolist() == want
+    f = lib.pkv_longest_first_order
+    assert f(None, 0, None) == pkv.PKV_OK
+    assert f(None, 3, None) == pkv.PKV_ERR_INVALID_ARG
+    assert f(None, -1, None) == pkv.PKV_ERR_INVALID_ARG
 
 
 def test_scheduler_pair_export_validation(lib):

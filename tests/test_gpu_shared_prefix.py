@@ -62,7 +62,7 @@ def test_shared_prefix_mixed_with_ungrouped_and_exact_prefix(_lib):
     w = synth.cow(prompt_len=64, prompts=2, rollouts=4)
     w = dataclasses.replace(w, ctx=[65, 66, 90, 65, 70, 71, 72, 200])
     pw = workload.build(w)
-    gs, pre, mp, _, _ = workload.prefix_groups(pw)
+    gs, pre, mp, _, _, _ = workload.prefix_groups(pw)
     # split the second prompt's group into singletons without a shared prefix
     gs2 = torch.tensor([0, 4], dtype=torch.int32, device="cuda")
     pre2 = pre.clone()
@@ -110,7 +110,7 @@ def test_shared_prefix_own_part_bound(_lib):
     partitions is read."""
     w = synth.cow(prompt_len=2040, prompts=2, rollouts=16)
     pw = workload.build(w)
-    gs, pre, mp, own, mm = workload.prefix_groups(pw)
+    gs, pre, mp, own, mm, _ = workload.prefix_groups(pw)
     assert own < pw.max_context - 2000
     P = w.partition_size
     st = pw.layers[0]
@@ -140,7 +140,7 @@ def test_shared_prefix_group_above_declared_bound(_lib):
     comp = w.extra["completion"]
     w = dataclasses.replace(w, ctx=[256 + (c % 200) + 1 for c in comp])
     pw = workload.build(w)
-    gs, pre, mp, own, mm = workload.prefix_groups(pw)
+    gs, pre, mp, own, mm, _ = workload.prefix_groups(pw)
     assert mm == 32
     st = pw.layers[0]
     pkv.kv_cache_write(st.k_new, st.v_new, pw.slot_mapping, st.k_cache, st.v_cache)
