@@ -158,8 +158,10 @@ int pkv_kv_cache_write(const void* k, const void* v, const int64_t* slot_mapping
  *               the short ones fill in behind them, instead of leaving a long
  *               one to run alone at the end of the grid. An entry outside
  *               [0, num_seqs) is reported as PKV_DEVERR_ORDER and its CTAs
- *               write nothing; a repeated entry leaves another sequence's
- *               result unwritten.
+ *               do nothing; a sequence that no entry names (because of such
+ *               an entry or a repeated one) is not decoded, and its result
+ *               is undefined (the split form's merge still combines that
+ *               row's workspace slots).
  * Errors: PKV_ERR_INVALID_ARG, PKV_ERR_UNSUPPORTED, PKV_ERR_CUDA.
  * ------------------------------------------------------------------------ */
 size_t pkv_decode_workspace_bytes(int num_seqs, int num_heads, int head_dim,
