@@ -151,7 +151,7 @@ def test_cow_rollouts(prompt_len, _lib):
     # own parts split by split_partition_size)
     groups = workload.prefix_groups(pw)
     P = pkv.split_partition_size(groups.max_own_context, w.block_size, w.partition_size)
-    assert P == 528
+    assert P == 1040                      # each own part in one partition
     ws = pkv.shared_prefix_workspace(w.num_seqs, w.num_heads, w.head_dim, groups.max_own_context,
                                      groups.max_prefix_blocks * w.block_size, P)
     sp = [torch.empty_like(pw.layers[0].q)]

@@ -112,7 +112,7 @@ def test_shared_prefix_own_part_bound(_lib):
     pw = workload.build(w)
     gs, pre, mp, own, mm, _ = workload.prefix_groups(pw)
     assert own < pw.max_context - 2000
-    P = w.partition_size
+    P = 512                               # own parts in two partitions
     st = pw.layers[0]
     pkv.kv_cache_write(st.k_new, st.v_new, pw.slot_mapping, st.k_cache, st.v_cache)
     outs = [pkv.paged_attention_shared_prefix(st.q, st.k_cache, st.v_cache, pw.block_tables,
