@@ -483,12 +483,10 @@ def main():
                     help="override the number of sequences (profiling of a smaller case)")
     ap.add_argument("--partition", type=int, default=-1,
                     help="override the partition size (0 = one pass)")
-    ap.add_argument("--visit-order", default="auto", choices=["auto", "longest", "batch"],
+    ap.add_argument("--visit-order", default="longest", choices=["longest", "batch"],
                     help="order in which the decode takes the sequences: longest context "
-                         "(own part, with the shared-prefix decode) first, or batch order; "
-                         "auto: longest first for the shared-prefix decode (copy-on-write "
-                         "rollouts 0.2207 -> 0.2122 ms), batch order for the split decode "
-                         "(mixed lengths 0.3273 -> 0.3294 ms with longest first)")
+                         "(own part, with the shared-prefix decode) first, or batch order "
+                         "(workloads whose contexts are all equal always run in batch order)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -564,10 +562,10 @@ def main():
         ws = pkv.shared_prefix_workspace(w.num_seqs, w.num_heads, w.head_dim,
                                          cascade.max_own_context,
                                          cascade.max_prefix_blocks * w.block_size, P)
-    if args.visit_order == "batch" and cascade is not None:
-        cascade = cascade._replace(visit_order=None)
-    if args.visit_order == "longest" and cascade is None:
-        pw.visit_order = workload.visit_order(w.ctx)
+    if args.visit_order == "batch":
+        pw.visit_order = None
+        if cascade is not None:
+            cascade = cascade._replace(visit_order=None)
     order = pw.visit_order if cascade is None else cascade.visit_order
 
     one_step = make_step(pw, out, ws, cascade, stream)

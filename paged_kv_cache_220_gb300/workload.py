@@ -50,9 +50,9 @@ class PagedWorkload:
     cow_pairs_host: Optional[np.ndarray] = None
     tables_host: Optional[np.ndarray] = None
     history_slots: Optional[List[np.ndarray]] = None
-    # [S] int32 (device) or None: the order in which step() has the decode
-    # take the sequences (None: batch order; visit_order(w.ctx) gives longest
-    # first)
+    # [S] int32 (device): the order in which step() has the decode take the
+    # sequences, longest context first; None: batch order (all contexts equal,
+    # or set by the caller)
     visit_order: Optional[torch.Tensor] = None
 
     @property
@@ -191,7 +191,8 @@ def build(w: synth.Workload, device="cuda", layers: Optional[int] = None,
         slot_mapping=torch.as_tensor(slot_new, device=device),
         max_context=w.max_context, layers=states,
         cow_pairs=torch.as_tensor(cow_pairs, device=device) if len(cow_pairs) else None,
-        cow_pairs_host=cow_pairs, tables_host=tables, history_slots=hist_slots)
+        cow_pairs_host=cow_pairs, tables_host=tables, history_slots=hist_slots,
+        visit_order=visit_order(w.ctx, device))
     return pw
 
 
