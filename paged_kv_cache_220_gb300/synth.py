@@ -236,11 +236,13 @@ def qwen_like(seed: int = 1002, layers: int = 16, num_seqs: int = 64,
 def mixed(seed: int = 1003, num_seqs: int = 256) -> Workload:
     """256 sequences, lengths log-uniform in [16, 16384], 24/4 heads, d=256,
     B=32, free list in seeded random order, 256 slack blocks. Split decode in
-    768-token partitions (GB300, step: 512 / 640 / 768 / 896 tokens ->
-    0.3272 / 0.3238 / 0.3236 / 0.3241 ms)."""
+    1536-token partitions with the sequences taken longest first (GB300, one
+    box, step: 768 / 1024 / 1536 / 1664 tokens -> 0.3195 / 0.3160 / 0.3138 /
+    0.3133 ms; 1280 and 1408 tokens 0.335 ms, 2048 0.339 ms; 1536 in batch
+    order 0.3465 ms)."""
     ctx = _loguniform_lengths(seed, num_seqs, 16, 16384)
     return Workload("mixed_lengths_continuous_batching", seed, 24, 4, 256, 32, ctx,
-                    slack_blocks=256, partition_size=768)
+                    slack_blocks=256, partition_size=1536)
 
 
 def cow(seed: int = 1004, prompt_len: int = 2048, prompts: int = 32,
