@@ -11,8 +11,13 @@
 //   of K and V with TMA tensor copies into a ring of shared memory stages, one
 //   3-D box per page (cp.async.bulk.tensor over a [128-byte chunk][row][128 B]
 //   view of the pool, 128-byte swizzle), which lands as [chunk][B rows][128 B];
-//   an mbarrier per stage counts the bytes in. One instruction per page
-//   instead of one per chunk measured 0.1-0.7 % faster across the workloads;
+//   a stage's K page and its V page each have an mbarrier that counts the
+//   bytes in and one that the consumer warps release, so a K page is
+//   refilled as soon as every warp has its logits, while the V page is still
+//   being read (GB300, same box: long FP8 0.3322 -> 0.3303 ms, copy-on-write
+//   0.2098 -> 0.2078, Qwen-like 4.850 -> 4.841, mixed lengths equal). One
+//   instruction per page instead of one per chunk measured 0.1-0.7 % faster
+//   across the workloads;
 // - the swizzle makes the row-strided fragment loads below bank-conflict
 //   free although a page row is 256 or 512 bytes long.
 //
@@ -55,8 +60,9 @@ namespace pkv {
 // partial sum over its columns, the warps exchange the partials through
 // shared memory (summed in warp order, so every warp holds the same logits
 // and the same softmax state) and each warp accumulates P.V for its own
-// columns. A page's stage is released when all NW warps are done with it.
-// Spreading one page over NW warps shortens the time a stage is held, so
+// columns. A stage's K page is released when all NW warps have read it, its V
+// page when all NW warps are done with P.V. Spreading one page over NW warps
+// shortens the time a stage is held, so
 // more of the ring is in flight (a probe that only streams pages reads
 // 7.4 TB/s; the stage hold time is what keeps the decode below that).
 template <int D, int BS, bool FP8, int NW, int NST>
@@ -95,9 +101,11 @@ __global__ void __launch_bounds__(TcGeom<D, BS, FP8, NW, NST>::kThreads)
   const uint32_t raw = smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* sbase = smem_raw + (base - raw);
-  uint64_t* full = reinterpret_cast<uint64_t*>(sbase);
-  uint64_t* empty = full + NST;
-  uint64_t* xfull = empty + NST;  // [2] logit partials of a slice are in
+  uint64_t* full = reinterpret_cast<uint64_t*>(sbase);  // [NST] K page of a stage landed
+  uint64_t* empty = full + NST;                          // [NST] K page read by every warp
+  uint64_t* vfull = empty + NST;                         // [NST] V page landed
+  uint64_t* vempty = vfull + NST;                        // [NST] V page read by every warp
+  uint64_t* xfull = vempty + NST;  // [2] logit partials of a slice are in
   const uint32_t ring = base + 1024;
   float* ring_f = reinterpret_cast<float*>(sbase + 1024);
   constexpr int kRegion = G::kRing > G::kMerge ? G::kRing : G::kMerge;
@@ -152,6 +160,8 @@ __global__ void __launch_bounds__(TcGeom<D, BS, FP8, NW, NST>::kThreads)
     for (int i = 0; i < NST; ++i) {
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], NW);
+      mbar_init(&vfull[i], 1);
+      mbar_init(&vempty[i], NW);
     }
     mbar_init(&xfull[0], NW * 32);
     mbar_init(&xfull[1], NW * 32);
@@ -159,7 +169,7 @@ __global__ void __launch_bounds__(TcGeom<D, BS, FP8, NW, NST>::kThreads)
   }
   __syncthreads();
 
-  int issued = 0;  // producer lane 0 only
+  int issued = 0, vissued = 0;  // producer lane 0 only
   // per-thread softmax state for queries q0 = 2*(lane%4), q1 = q0 + 1
   // (the same in every consumer warp)
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
@@ -175,17 +185,27 @@ __global__ void __launch_bounds__(TcGeom<D, BS, FP8, NW, NST>::kThreads)
         if (it >= NST && !mbar_wait(&empty[st], ((it / NST) - 1) & 1, p.err)) break;
         const int u = blk_begin + it;  // page of the sequence
         const int32_t pb = bt[u / UPB];
-        issued = it + 1;
-        if (pb < 0 || pb >= p.num_blocks) {
-          report_error(p.err, PKV_DEVERR_BLOCK_ID);
-          mbar_arrive(&full[st]);  // release the stage without data
-          continue;
-        }
+        const bool bad = pb < 0 || pb >= p.num_blocks;
         const uint32_t kdst = ring + st * G::kStage;
-        const int y = (pb * p.num_kv_heads + h) * (BS * UPB) + (u % UPB) * BS;
-        mbar_arrive_expect_tx(&full[st], 2 * PAGE);
-        tma_load_page(kdst, &tmk, y, &full[st]);
-        tma_load_page(kdst + PAGE, &tmv, y, &full[st]);
+        const int y = bad ? 0 : (pb * p.num_kv_heads + h) * (BS * UPB) + (u % UPB) * BS;
+        issued = it + 1;
+        if (bad) {
+          report_error(p.err, PKV_DEVERR_BLOCK_ID);
+          mbar_arrive(&full[st]);  // release the K page without data
+        } else {
+          mbar_arrive_expect_tx(&full[st], PAGE);
+          tma_load_page(kdst, &tmk, y, &full[st]);
+        }
+        // the V page of the stage is free once every warp's P.V of the page
+        // NST before is done (later than its K page)
+        if (it >= NST && !mbar_wait(&vempty[st], ((it / NST) - 1) & 1, p.err)) break;
+        vissued = it + 1;
+        if (bad) {
+          mbar_arrive(&vfull[st]);
+        } else {
+          mbar_arrive_expect_tx(&vfull[st], PAGE);
+          tma_load_page(kdst + PAGE, &tmv, y, &vfull[st]);
+        }
       }
     }
   } else {
@@ -228,17 +248,7 @@ __global__ void __launch_bounds__(TcGeom<D, BS, FP8, NW, NST>::kThreads)
       const uint32_t kp = ring + st * G::kStage;
       const uint32_t vp = kp + PAGE;
       const int ntok = min(BS, ctx - (blk_begin + it) * BS);
-      if (ntok < BS) {
-        // slots past the context hold whatever was there: zero this warp's
-        // columns of their V rows so the zero probabilities cannot meet a NaN
-        for (int r = ntok; r < BS; ++r)
-          for (int c = lane * 16; c < G::kDW * ESZ; c += 512)
-            asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(
-                             swz_bytes<BS>(vp, r, warp * G::kDW * ESZ + c)),
-                         "r"(0u)
-                         : "memory");
-        __syncwarp();
-      }
+      bool vready = false;  // V page of this stage waited for (and its tail zeroed)
       // one slice = kNH 16-row halves: their logits are exchanged once and
       // go through one max / rescale step of the online softmax
       constexpr int NH = G::kNH;
@@ -274,6 +284,11 @@ __global__ void __launch_bounds__(TcGeom<D, BS, FP8, NW, NST>::kThreads)
           }
 #pragma unroll
           for (int i = 0; i < 4; ++i) sp[hh][i] = sa[i] + sb[i];
+        }
+        if (r0 + G::kSlice >= BS) {
+          // the last K rows of the page are read: the producer may refill it
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&empty[st]);
         }
         // ---- exchange: every warp sums the NW partials in warp order
         const int xb = slice & 1;
@@ -329,6 +344,25 @@ __global__ void __launch_bounds__(TcGeom<D, BS, FP8, NW, NST>::kThreads)
           m1 = mn1;
         }
 #pragma unroll
+        if (!vready) {
+          if (!__all_sync(0xffffffffu, mbar_wait(&vfull[st], (it / NST) & 1, p.err))) {
+            ok = false;
+            break;
+          }
+          if (ntok < BS) {
+            // slots past the context hold whatever was there: zero this
+            // warp's columns of their V rows so the zero probabilities cannot
+            // meet a NaN
+            for (int r = ntok; r < BS; ++r)
+              for (int c = lane * 16; c < G::kDW * ESZ; c += 512)
+                asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(
+                                 swz_bytes<BS>(vp, r, warp * G::kDW * ESZ + c)),
+                             "r"(0u)
+                             : "memory");
+            __syncwarp();
+          }
+          vready = true;
+        }
         for (int hh = 0; hh < NH; ++hh) {
           const int rh = r0 + 16 * hh;  // first row of this half
           // every slice has a valid token in row 0 of the CTA's first page, so
@@ -383,9 +417,10 @@ __global__ void __launch_bounds__(TcGeom<D, BS, FP8, NW, NST>::kThreads)
           }
         }
       }
+      if (!ok) break;
       if (ntok < BS) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[st]);
+      if (lane == 0) mbar_arrive(&vempty[st]);
     }
     // per-query sums over the 8 lanes that share a query pair
 #pragma unroll
@@ -401,6 +436,9 @@ __global__ void __launch_bounds__(TcGeom<D, BS, FP8, NW, NST>::kThreads)
     const int first = issued > NST ? issued - NST : 0;
     for (int it = first; it < issued; ++it)
       if (!mbar_wait(&full[it % NST], (it / NST) & 1, p.err)) break;
+    const int vfirst = vissued > NST ? vissued - NST : 0;
+    for (int it = vfirst; it < vissued; ++it)
+      if (!mbar_wait(&vfull[it % NST], (it / NST) & 1, p.err)) break;
   }
   __syncthreads();
   // the merge launched next may be scheduled once every CTA got here; it
