@@ -77,3 +77,18 @@ def test_host_iteration_timing_runs_the_whole_batch():
     h = bench.host_iteration_timing(w, iters=20)
     assert h["running"] == 40 and h["iterations"] == 20
     assert h["sched_step_us"] > 0 and h["block_tables_us"] > 0
+
+
+def test_visit_order_is_longest_first_or_none():
+    """The workload helpers' visit order: longest first (ties in batch order)
+    as a permutation of the batch, none when every length is equal."""
+    import numpy as np
+    from paged_kv_cache_220_gb300 import workload
+    assert workload.visit_order([8192] * 64, device="cpu") is None
+    lens = [5, 900, 17, 900, 3000, 1]
+    order = workload.visit_order(lens, device="cpu").numpy().tolist()
+    assert sorted(order) == list(range(len(lens)))
+    assert order == [4, 1, 3, 2, 0, 5]
+    ctx = np.asarray(synth.mixed().ctx)
+    order = workload.visit_order(ctx, device="cpu").numpy()
+    assert np.all(np.diff(ctx[order]) <= 0)
