@@ -85,6 +85,11 @@ struct TcGeom {
   static constexpr int kSmem = 1024 /*barriers*/ + 1024 /*alignment*/ +
                                (kRing > kMerge ? kRing : kMerge) + kXchg;
   static constexpr int kThreads = (NW + 1) * 32;
+  // separate barriers for a stage's K and V pages (K refilled right after the
+  // logits) pay from 8 KB pages on; with 4 KB pages (E4M3, B = 16) the extra
+  // barrier work per page costs more than the earlier refill gains (GB300,
+  // same box: copy-on-write over an E4M3 cache 0.1550 -> 0.1597 ms with them)
+  static constexpr bool kSplitKV = kPage >= 8192;
 };
 
 // BS = rows of a ring page; a pool block holds UPB such pages (UPB = 2 runs a
@@ -189,8 +194,19 @@ __global__ void __launch_bounds__(TcGeom<D, BS, FP8, NW, NST>::kThreads)
         const uint32_t kdst = ring + st * G::kStage;
         const int y = bad ? 0 : (pb * p.num_kv_heads + h) * (BS * UPB) + (u % UPB) * BS;
         issued = it + 1;
+        if (bad) report_error(p.err, PKV_DEVERR_BLOCK_ID);
+        if constexpr (!G::kSplitKV) {
+          // one barrier pair for the stage's K and V pages
+          if (bad) {
+            mbar_arrive(&full[st]);  // release the stage without data
+          } else {
+            mbar_arrive_expect_tx(&full[st], 2 * PAGE);
+            tma_load_page(kdst, &tmk, y, &full[st]);
+            tma_load_page(kdst + PAGE, &tmv, y, &full[st]);
+          }
+          continue;
+        }
         if (bad) {
-          report_error(p.err, PKV_DEVERR_BLOCK_ID);
           mbar_arrive(&full[st]);  // release the K page without data
         } else {
           mbar_arrive_expect_tx(&full[st], PAGE);
@@ -240,6 +256,18 @@ __global__ void __launch_bounds__(TcGeom<D, BS, FP8, NW, NST>::kThreads)
     float qs = p.qscale;
     if constexpr (FP8) qs *= p.k_scale[h];
 
+    // slots past the context hold whatever was there: zero this warp's
+    // columns of their V rows so the zero probabilities cannot meet a NaN
+    auto zero_v_tail = [&](uint32_t vpage, int ntok) {
+      if (ntok >= BS) return;
+      for (int r = ntok; r < BS; ++r)
+        for (int c = lane * 16; c < G::kDW * ESZ; c += 512)
+          asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(
+                           swz_bytes<BS>(vpage, r, warp * G::kDW * ESZ + c)),
+                       "r"(0u)
+                       : "memory");
+      __syncwarp();
+    };
     bool ok = true;
     int slice = 0;  // 16-token slices so far (exchange buffer and phase)
     for (int it = 0; it < nblk && ok; ++it) {
@@ -248,7 +276,13 @@ __global__ void __launch_bounds__(TcGeom<D, BS, FP8, NW, NST>::kThreads)
       const uint32_t kp = ring + st * G::kStage;
       const uint32_t vp = kp + PAGE;
       const int ntok = min(BS, ctx - (blk_begin + it) * BS);
-      bool vready = false;  // V page of this stage waited for (and its tail zeroed)
+      // V page of this stage waited for and its tail zeroed (with one barrier
+      // pair per stage it landed with K: the tail is zeroed before the slices)
+      bool vready = false;
+      if constexpr (!G::kSplitKV) {
+        vready = true;
+        zero_v_tail(vp, ntok);
+      }
       // one slice = kNH 16-row halves: their logits are exchanged once and
       // go through one max / rescale step of the online softmax
       constexpr int NH = G::kNH;
@@ -285,7 +319,7 @@ __global__ void __launch_bounds__(TcGeom<D, BS, FP8, NW, NST>::kThreads)
 #pragma unroll
           for (int i = 0; i < 4; ++i) sp[hh][i] = sa[i] + sb[i];
         }
-        if (r0 + G::kSlice >= BS) {
+        if (G::kSplitKV && r0 + G::kSlice >= BS) {
           // the last K rows of the page are read: the producer may refill it
           __syncwarp();
           if (lane == 0) mbar_arrive(&empty[st]);
@@ -349,18 +383,7 @@ __global__ void __launch_bounds__(TcGeom<D, BS, FP8, NW, NST>::kThreads)
             ok = false;
             break;
           }
-          if (ntok < BS) {
-            // slots past the context hold whatever was there: zero this
-            // warp's columns of their V rows so the zero probabilities cannot
-            // meet a NaN
-            for (int r = ntok; r < BS; ++r)
-              for (int c = lane * 16; c < G::kDW * ESZ; c += 512)
-                asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(
-                                 swz_bytes<BS>(vp, r, warp * G::kDW * ESZ + c)),
-                             "r"(0u)
-                             : "memory");
-            __syncwarp();
-          }
+          zero_v_tail(vp, ntok);
           vready = true;
         }
         for (int hh = 0; hh < NH; ++hh) {
@@ -420,7 +443,7 @@ __global__ void __launch_bounds__(TcGeom<D, BS, FP8, NW, NST>::kThreads)
       if (!ok) break;
       if (ntok < BS) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       __syncwarp();
-      if (lane == 0) mbar_arrive(&vempty[st]);
+      if (lane == 0) mbar_arrive(G::kSplitKV ? &vempty[st] : &empty[st]);
     }
     // per-query sums over the 8 lanes that share a query pair
 #pragma unroll
@@ -437,7 +460,7 @@ __global__ void __launch_bounds__(TcGeom<D, BS, FP8, NW, NST>::kThreads)
     for (int it = first; it < issued; ++it)
       if (!mbar_wait(&full[it % NST], (it / NST) & 1, p.err)) break;
     const int vfirst = vissued > NST ? vissued - NST : 0;
-    for (int it = vfirst; it < vissued; ++it)
+    for (int it = vfirst; it < vissued; ++it)  // (vissued stays 0 with one pair per stage)
       if (!mbar_wait(&vfull[it % NST], (it / NST) & 1, p.err)) break;
   }
   __syncthreads();
