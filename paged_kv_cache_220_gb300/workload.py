@@ -398,7 +398,7 @@ class ContinuousBatch:
         out = self.out[:n]
         mc = int(ctx.max())
         pkv.paged_attention(q, self.k_cache, self.v_cache, bt, cl, self.scale, mc, self.P,
-                            out=out, workspace=self.ws)
+                            out=out, workspace=self.ws, seq_order=visit_order(ctx, dev))
         self.tokens += n
         return ids, ctx, out
 
