@@ -11,11 +11,12 @@
 //   of K and V with TMA tensor copies into a ring of shared memory stages, one
 //   3-D box per page (cp.async.bulk.tensor over a [128-byte chunk][row][128 B]
 //   view of the pool, 128-byte swizzle), which lands as [chunk][B rows][128 B];
-//   a stage's K page and its V page each have an mbarrier that counts the
-//   bytes in and one that the consumer warps release, so a K page is
-//   refilled as soon as every warp has its logits, while the V page is still
-//   being read (GB300, same box: long FP8 0.3322 -> 0.3303 ms, copy-on-write
-//   0.2098 -> 0.2078, Qwen-like 4.850 -> 4.841, mixed lengths equal). One
+//   with pages of 8 KB and more, a stage's K page and its V page each have an
+//   mbarrier that counts the bytes in and one that the consumer warps
+//   release, so a K page is refilled as soon as every warp has its logits,
+//   while the V page is still being read (GB300, same box: long FP8 0.3322
+//   -> 0.3303 ms, copy-on-write 0.2098 -> 0.2078, Qwen-like 4.850 -> 4.841,
+//   mixed lengths equal); 4 KB pages keep one pair per stage. One
 //   instruction per page instead of one per chunk measured 0.1-0.7 % faster
 //   across the workloads;
 // - the swizzle makes the row-strided fragment loads below bank-conflict
@@ -61,8 +62,9 @@ namespace pkv {
 // shared memory (summed in warp order, so every warp holds the same logits
 // and the same softmax state) and each warp accumulates P.V for its own
 // columns. A stage's K page is released when all NW warps have read it, its V
-// page when all NW warps are done with P.V. Spreading one page over NW warps
-// shortens the time a stage is held, so
+// page when all NW warps are done with P.V (4 KB pages: the stage at once,
+// after P.V). Spreading one page over NW warps shortens the time a stage is
+// held, so
 // more of the ring is in flight (a probe that only streams pages reads
 // 7.4 TB/s; the stage hold time is what keeps the decode below that).
 template <int D, int BS, bool FP8, int NW, int NST>
