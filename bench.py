@@ -439,11 +439,13 @@ def measure_other(name, steps=10, warmup=3):
             graph.replay()
             ev[i][1].record(stream)
         torch.cuda.synchronize()
-    ms = sum(a.elapsed_time(b) for a, b in ev) / steps
+    per = [a.elapsed_time(b) for a, b in ev]
+    ms = sum(per) / steps
     peak, peak_kind = peaks()
     dec_bytes = decode_bytes(w) if cascade is None else unique_decode_bytes(w)
     achieved = dec_bytes / (dec_ms / 1e3) / 1e9
     r = {"workload": w.name, "steps": steps, "warmup": warmup, "ms_per_step": round(ms, 4),
+         "ms_per_step_median": round(statistics.median(per), 4),
          "value": round(step_bytes / (ms / 1e3) / 1e9, 2), "unit": "GB/s",
          "roofline": {"kernel": "paged_attention_decode" if cascade is None else
                       "paged_attention_decode_shared_prefix (3 kernels, unique bytes)",
@@ -660,6 +662,7 @@ def main():
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": args.gpus,
         "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+        "ms_per_step_median": round(statistics.median(step_ms), 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "fp8_e4m3" if w.fp8 else "bf16", "data": "synthetic",
         "config": {
