@@ -379,7 +379,6 @@ __global__ void __launch_bounds__(TcGeom<D, BS, FP8, NW, NST>::kThreads)
           m0 = mn0;
           m1 = mn1;
         }
-#pragma unroll
         if (!vready) {
           if (!__all_sync(0xffffffffu, mbar_wait(&vfull[st], (it / NST) & 1, p.err))) {
             ok = false;
@@ -388,6 +387,7 @@ __global__ void __launch_bounds__(TcGeom<D, BS, FP8, NW, NST>::kThreads)
           zero_v_tail(vp, ntok);
           vready = true;
         }
+#pragma unroll
         for (int hh = 0; hh < NH; ++hh) {
           const int rh = r0 + 16 * hh;  // first row of this half
           // every slice has a valid token in row 0 of the CTA's first page, so
