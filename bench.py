@@ -53,8 +53,7 @@ def workload_for(name: str):
         "cow": lambda: synth.cow(prompt_len=2048),
         "cow2040": lambda: synth.cow(prompt_len=2040),
         "cow2040_fp8": lambda: __import__("dataclasses").replace(
-            synth.cow(prompt_len=2040), fp8=True, name="cow_shared_prefix_2040_fp8",
-            partition_size=512),
+            synth.cow(prompt_len=2040), fp8=True, name="cow_shared_prefix_2040_fp8"),
         "long_fp8": lambda: synth.long_fp8(),
     }
     w = table[name]()

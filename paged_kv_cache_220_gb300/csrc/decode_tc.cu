@@ -95,8 +95,9 @@ struct TcGeom {
 };
 
 // BS = rows of a ring page; a pool block holds UPB such pages (UPB = 2 runs a
-// 32-token pool in 16-token pages).
-template <int D, int BS, bool FP8, int NW, int NST, int UPB>
+// 32-token pool in 16-token pages), or a page holds BPP pool blocks (BPP = 2
+// runs a 16-token E4M3 pool in 32-row pages, split form only).
+template <int D, int BS, bool FP8, int NW, int NST, int UPB, int BPP>
 __global__ void __launch_bounds__(TcGeom<D, BS, FP8, NW, NST>::kThreads)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tmk,
                      const __grid_constant__ CUtensorMap tmv, const DecodeParams p) {
@@ -104,6 +105,8 @@ __global__ void __launch_bounds__(TcGeom<D, BS, FP8, NW, NST>::kThreads)
   constexpr int PAGE = G::kPage;
   constexpr int ESZ = G::kEsz;
   constexpr int KW = G::kKW;
+  constexpr int PB = BS * UPB / BPP;  // rows of a pool block
+  static_assert(UPB == 1 || BPP == 1, "a ring page is part of a block or several blocks");
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -143,25 +146,41 @@ __global__ void __launch_bounds__(TcGeom<D, BS, FP8, NW, NST>::kThreads)
   const int g = p.group;
 
   int ctx = p.context_lens[s];
-  const int cap = p.max_blocks_per_seq * BS * UPB;
+  const int cap = p.max_blocks_per_seq * PB;
   if (ctx < 0 || ctx > cap) {
     if (threadIdx.x == 0 && part == 0 && h == 0) report_error(p.err, PKV_DEVERR_CONTEXT);
     ctx = ctx < 0 ? 0 : cap;
   }
-  int blk_begin = 0;
-  int blk_end = (ctx + BS - 1) / BS;
-  if (p.partition_blocks > 0) {
-    blk_begin = (part * p.partition_blocks + (p.block_offset ? p.block_offset[s] : 0)) * UPB;
+  // BPP == 1: ring pages [blk_begin, blk_end); BPP > 1 (split form only):
+  // pool blocks [blk_begin, blk_end), BPP of them to a ring page
+  int blk_begin = 0, blk_end = 0, nblk = 0;
+  int tok0 = 0;  // first token of this CTA's pages
+  if constexpr (BPP == 1) {
+    blk_end = (ctx + BS - 1) / BS;
+    if (p.partition_blocks > 0) {
+      blk_begin = (part * p.partition_blocks + (p.block_offset ? p.block_offset[s] : 0)) * UPB;
+      if (blk_begin >= blk_end) return;  // partition past the end: nothing to store
+      blk_end = min(blk_end, blk_begin + p.partition_blocks * UPB);
+    } else if (p.cluster > 1) {
+      // one pass over a cluster: rank r takes an equal share of the pages (it
+      // may get none, but it still takes part in the cluster merge below)
+      const int share = (blk_end + p.cluster - 1) / p.cluster;
+      blk_begin = min(blk_end, part * share);
+      blk_end = min(blk_end, blk_begin + share);
+    }
+    nblk = blk_end - blk_begin;
+    tok0 = blk_begin * BS;
+  } else {
+    blk_end = (ctx + PB - 1) / PB;
+    blk_begin = part * p.partition_blocks + (p.block_offset ? p.block_offset[s] : 0);
     if (blk_begin >= blk_end) return;  // partition past the end: nothing to store
-    blk_end = min(blk_end, blk_begin + p.partition_blocks * UPB);
-  } else if (p.cluster > 1) {
-    // one pass over a cluster: rank r takes an equal share of the pages (it may
-    // get none, but it still takes part in the cluster merge below)
-    const int share = (blk_end + p.cluster - 1) / p.cluster;
-    blk_begin = min(blk_end, part * share);
-    blk_end = min(blk_end, blk_begin + share);
+    blk_end = min(blk_end, blk_begin + p.partition_blocks);
+    nblk = (blk_end - blk_begin + BPP - 1) / BPP;
+    tok0 = blk_begin * PB;
   }
-  const int nblk = blk_end - blk_begin;
+  // one past the last token of this CTA's pages (a partition may end inside
+  // a page when BPP > 1)
+  const int tok_end = min(ctx, BPP == 1 ? blk_end * BS : blk_end * PB);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < NST; ++i) {
@@ -190,11 +209,41 @@ __global__ void __launch_bounds__(TcGeom<D, BS, FP8, NW, NST>::kThreads)
       for (int it = 0; it < nblk; ++it) {
         const int st = it % NST;
         if (it >= NST && !mbar_wait(&empty[st], ((it / NST) - 1) & 1, p.err)) break;
-        const int u = blk_begin + it;  // page of the sequence
-        const int32_t pb = bt[u / UPB];
-        const bool bad = pb < 0 || pb >= p.num_blocks;
+        // first pool row of each pool block of the page (y), their count (nb)
+        int y[BPP];
+        int nb = 0;
+        bool bad = false;
+        if constexpr (BPP == 1) {
+          const int u = blk_begin + it;  // page of the sequence
+          const int32_t pb = bt[u / UPB];
+          bad = pb < 0 || pb >= p.num_blocks;
+          y[0] = bad ? 0 : (pb * p.num_kv_heads + h) * (BS * UPB) + (u % UPB) * BS;
+          nb = 1;
+        } else {
+#pragma unroll
+          for (int b = 0; b < BPP; ++b) {
+            const int q = blk_begin + BPP * it + b;
+            if (q >= blk_end) break;
+            const int32_t pb = bt[q];
+            bad = bad || pb < 0 || pb >= p.num_blocks;
+            y[b] = (pb * p.num_kv_heads + h) * PB;
+            ++nb;
+          }
+        }
         const uint32_t kdst = ring + st * G::kStage;
-        const int y = bad ? 0 : (pb * p.num_kv_heads + h) * (BS * UPB) + (u % UPB) * BS;
+        // one page of K or V: a whole-page box, or (BPP > 1) one box per
+        // pool block and 128-byte chunk, block b at rows [b*PB, (b+1)*PB)
+        auto load = [&](uint32_t dst, const CUtensorMap* map, uint64_t* bar) {
+          if constexpr (BPP == 1) {
+            tma_load_page(dst, map, y[0], bar);
+          } else {
+            for (int b = 0; b < nb; ++b)
+#pragma unroll
+              for (int c = 0; c < D * ESZ / 128; ++c)
+                tma_load_2d(dst + c * (BS * 128) + b * (PB * 128), map, c * (128 / ESZ), y[b], bar);
+          }
+        };
+        const int bytes = nb * (PAGE / BPP);  // of K (or V) in this page
         issued = it + 1;
         if (bad) report_error(p.err, PKV_DEVERR_BLOCK_ID);
         if constexpr (!G::kSplitKV) {
@@ -202,17 +251,17 @@ __global__ void __launch_bounds__(TcGeom<D, BS, FP8, NW, NST>::kThreads)
           if (bad) {
             mbar_arrive(&full[st]);  // release the stage without data
           } else {
-            mbar_arrive_expect_tx(&full[st], 2 * PAGE);
-            tma_load_page(kdst, &tmk, y, &full[st]);
-            tma_load_page(kdst + PAGE, &tmv, y, &full[st]);
+            mbar_arrive_expect_tx(&full[st], 2 * bytes);
+            load(kdst, &tmk, &full[st]);
+            load(kdst + PAGE, &tmv, &full[st]);
           }
           continue;
         }
         if (bad) {
           mbar_arrive(&full[st]);  // release the K page without data
         } else {
-          mbar_arrive_expect_tx(&full[st], PAGE);
-          tma_load_page(kdst, &tmk, y, &full[st]);
+          mbar_arrive_expect_tx(&full[st], bytes);
+          load(kdst, &tmk, &full[st]);
         }
         // the V page of the stage is free once every warp's P.V of the page
         // NST before is done (later than its K page)
@@ -221,8 +270,8 @@ __global__ void __launch_bounds__(TcGeom<D, BS, FP8, NW, NST>::kThreads)
         if (bad) {
           mbar_arrive(&vfull[st]);
         } else {
-          mbar_arrive_expect_tx(&vfull[st], PAGE);
-          tma_load_page(kdst + PAGE, &tmv, y, &vfull[st]);
+          mbar_arrive_expect_tx(&vfull[st], bytes);
+          load(kdst + PAGE, &tmv, &vfull[st]);
         }
       }
     }
@@ -277,7 +326,7 @@ __global__ void __launch_bounds__(TcGeom<D, BS, FP8, NW, NST>::kThreads)
       if (!__all_sync(0xffffffffu, mbar_wait(&full[st], (it / NST) & 1, p.err))) break;
       const uint32_t kp = ring + st * G::kStage;
       const uint32_t vp = kp + PAGE;
-      const int ntok = min(BS, ctx - (blk_begin + it) * BS);
+      const int ntok = min(BS, tok_end - (tok0 + it * BS));
       // V page of this stage waited for and its tail zeroed (with one barrier
       // pair per stage it landed with K: the tail is zeroed before the slices)
       bool vready = false;
@@ -632,19 +681,22 @@ int pool_tensor_map(CUtensorMap* out, const void* base, int64_t rows, int D, int
   return PKV_OK;
 }
 
-template <int D, int BS, bool FP8, int NW, int NST, int UPB = 1>
+template <int D, int BS, bool FP8, int NW, int NST, int UPB = 1, int BPP = 1>
 static int launch_tc(const DecodeParams& p_in, const void* k_cache, const void* v_cache,
                      dim3 grid, cudaStream_t st) {
   using G = TcGeom<D, BS, FP8, NW, NST>;
-  // whole-page boxes of BS rows over the pool viewed as [NB*Hk*BS*UPB rows][D]
-  const int64_t rows = static_cast<int64_t>(p_in.num_blocks) * p_in.num_kv_heads * BS * UPB;
+  constexpr int PB = BS * UPB / BPP;  // rows of a pool block
+  // the pool viewed as [NB*Hk*PB rows][D]
+  const int64_t rows = static_cast<int64_t>(p_in.num_blocks) * p_in.num_kv_heads * PB;
   CUtensorMap tk, tv;
-  int rc = pool_tensor_map(&tk, k_cache, rows, D, BS, FP8, true);
+  // whole-page 3-D boxes, or (several blocks to a page) 2-D boxes of one
+  // pool block and 128-byte chunk
+  int rc = pool_tensor_map(&tk, k_cache, rows, D, BPP == 1 ? BS : PB, FP8, BPP == 1);
   if (rc != PKV_OK) return rc;
-  rc = pool_tensor_map(&tv, v_cache, rows, D, BS, FP8, true);
+  rc = pool_tensor_map(&tv, v_cache, rows, D, BPP == 1 ? BS : PB, FP8, BPP == 1);
   if (rc != PKV_OK) return rc;
   static DeviceFlags done;
-  auto kern = decode_tc_kernel<D, BS, FP8, NW, NST, UPB>;
+  auto kern = decode_tc_kernel<D, BS, FP8, NW, NST, UPB, BPP>;
   rc = ensure_smem(kern, G::kSmem, done);
   if (rc != PKV_OK) return rc;
   DecodeParams p = p_in;
@@ -721,6 +773,12 @@ static int dispatch_tc(const DecodeParams& p, const void* k_cache, const void* v
   // copy-on-write step 0.2250 -> 0.2228 ms, over an E4M3 cache 0.1757 ->
   // 0.1678; Qwen-like with three stages 4.849 -> 4.928 ms).
   if (head_dim == 256 && block_size == 16) {
+    // E4M3 split form: two 16-token blocks to a 32-row page (one 2-D box per
+    // block and 128-byte chunk), so a softmax slice is 32 rows as at B = 32
+    // (GB300, same box: long-context shapes at B = 16 0.3338 -> 0.3227 ms per
+    // decode, copy-on-write rollouts over an E4M3 cache 0.1533 -> 0.1460 ms)
+    if constexpr (FP8)
+      if (p.partition_blocks > 0) return launch_tc<256, 32, FP8, 2, 2, 1, 2>(p, k_cache, v_cache, grid, st);
     if (p.partition_blocks > 0 && p.partition_blocks <= 48)
       return launch_tc<256, 16, FP8, 2, 3>(p, k_cache, v_cache, grid, st);
     return launch_tc<256, 16, FP8, 2, 2>(p, k_cache, v_cache, grid, st);

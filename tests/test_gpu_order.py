@@ -42,7 +42,7 @@ def _orders(lengths, seed):
 
 
 @pytest.mark.parametrize("fp8,B,P", [(False, 16, 64), (False, 32, 512), (True, 32, 64),
-                                     (False, 16, 0), (True, 32, 0)])
+                                     (True, 16, 48), (False, 16, 0), (True, 32, 0), (True, 16, 0)])
 def test_order_gives_the_same_bits(fp8, B, P, _lib):
     ctx = [1, 700, 31, 2000, B, 5, 1500, 64, 333, 1200, 17, 900]
     w = synth.Workload("order", 1500 + B + P + (3 if fp8 else 0), 24, 4, 256, B, ctx, fp8=fp8,

@@ -87,7 +87,8 @@ def _check_slots(got, ref, slots, what, exact_max=True):
 
 
 CASES = [(False, 16, 16), (False, 16, 32), (False, 16, 64), (False, 16, 512), (False, 32, 32),
-         (False, 32, 512), (True, 32, 32), (True, 32, 64), (True, 32, 512), (True, 16, 64)]
+         (False, 32, 512), (True, 32, 32), (True, 32, 64), (True, 32, 512), (True, 16, 64),
+         (True, 16, 48), (True, 16, 528)]
 
 
 @pytest.mark.parametrize("fp8,B,P", CASES)
