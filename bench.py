@@ -55,6 +55,9 @@ def workload_for(name: str):
         "cow2040_fp8": lambda: __import__("dataclasses").replace(
             synth.cow(prompt_len=2040), fp8=True, name="cow_shared_prefix_2040_fp8"),
         "long_fp8": lambda: synth.long_fp8(),
+        # the same shapes and bytes in 16-token blocks
+        "long_fp8_b16": lambda: __import__("dataclasses").replace(
+            synth.long_fp8(), block_size=16, name="long_context_fp8_splitk_b16"),
     }
     w = table[name]()
     if name == "tiny":
