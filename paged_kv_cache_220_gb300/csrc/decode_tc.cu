@@ -225,8 +225,9 @@ __global__ void __launch_bounds__(TcGeom<D, BS, FP8, NW, NST>::kThreads)
             const int q = blk_begin + BPP * it + b;
             if (q >= blk_end) break;
             const int32_t pb = bt[q];
-            bad = bad || pb < 0 || pb >= p.num_blocks;
-            y[b] = (pb * p.num_kv_heads + h) * PB;
+            const bool ok_b = pb >= 0 && pb < p.num_blocks;
+            bad = bad || !ok_b;
+            y[b] = ok_b ? (pb * p.num_kv_heads + h) * PB : 0;
             ++nb;
           }
         }
