@@ -6,7 +6,8 @@ Every output of a whole layer is compared with the oracle: all 64 sequences
 of layer 0 of the Qwen-like batch (plus 4 sampled sequences of each other
 layer), all 256 mixed-length sequences, all 512 rollouts of both
 copy-on-write variants (through the plain split decode and through the
-shared-prefix decode), and all 8 long FP8 sequences. The cache writes of
+shared-prefix decode), the 512 rollouts over an E4M3 cache (shared-prefix
+decode), and all 8 long FP8 sequences. The cache writes of
 layer 0 of the Qwen-like batch and of the FP8 batch are checked bit for bit
 over the whole pool, and the FP8 scales are recomputed on the host from the
 host rows. Host rows come from the seeded generator; nothing but the outputs
@@ -185,3 +186,31 @@ def test_long_context_fp8(_lib):
     assert np.array_equal(_pool_bits(st.k_cache), pk), "fp8 K pool"
     del pk
     assert np.array_equal(_pool_bits(st.v_cache), pv), "fp8 V pool"
+
+
+def test_cow_rollouts_over_fp8_cache(_lib):
+    """All 512 rollouts of the 2040-token prompts over an E4M3 cache, through
+    the shared-prefix decode as the benchmark runs it (a replayed CUDA graph,
+    own parts longest first, split by split_partition_size; 16-token E4M3
+    blocks two to a decode page), against the oracle on its own E4M3 codes of
+    the host rows; the per-head scales recomputed on the host."""
+    import dataclasses
+    w = dataclasses.replace(synth.cow(prompt_len=2040), fp8=True)
+    pw = workload.build(w)
+    st = pw.layers[0]
+    rows = _memo(RowCache(w, 0).rows)
+    ks, vs = host_fp8_scales(w, 0, rows)
+    assert np.array_equal(ks.view(np.uint32), st.k_scale.cpu().numpy().view(np.uint32))
+    assert np.array_equal(vs.view(np.uint32), st.v_scale.cpu().numpy().view(np.uint32))
+    groups = workload.prefix_groups(pw)
+    assert groups.visit_order is not None
+    P = pkv.split_partition_size(groups.max_own_context, w.block_size, w.partition_size)
+    assert P == 1040
+    ws = pkv.shared_prefix_workspace(w.num_seqs, w.num_heads, w.head_dim, groups.max_own_context,
+                                     groups.max_prefix_blocks * w.block_size, P)
+    sp = [torch.empty_like(st.q)]
+    g = workload.capture_step(pw, sp, ws, P, groups=groups)
+    g.replay()
+    torch.cuda.synchronize()
+    assert int(_lib.item()) == 0
+    _check_all(sp[0].cpu(), w, 0, rows, "cow fp8 shared prefix", ks, vs)
