@@ -44,6 +44,17 @@ DECODE_SOURCES = ["paged_kv_cache_220_gb300/csrc/decode.cu",
                   "paged_kv_cache_220_gb300/csrc/tc_common.cuh"]
 
 
+def _long_prompt_rollouts():
+    """8 prompts of 8184 tokens x 16 rollouts, completion lengths (the copy-on-
+    write workload's draws) mod 129."""
+    import dataclasses
+    from paged_kv_cache_220_gb300 import synth
+    w = synth.cow(prompt_len=8184, prompts=8, rollouts=16)
+    comp = [c % 129 for c in w.extra["completion"]]
+    return dataclasses.replace(w, ctx=[8184 + c + 1 for c in comp], extra={"completion": comp},
+                               name="cow_long_prompts_8184")
+
+
 def workload_for(name: str):
     from paged_kv_cache_220_gb300 import synth
     table = {
@@ -58,6 +69,9 @@ def workload_for(name: str):
         # the same shapes and bytes in 16-token blocks
         "long_fp8_b16": lambda: __import__("dataclasses").replace(
             synth.long_fp8(), block_size=16, name="long_context_fp8_splitk_b16"),
+        # rollouts of long prompts with short completions: the shared prefix
+        # is most of the bytes
+        "cow_long_prompts": lambda: _long_prompt_rollouts(),
     }
     w = table[name]()
     if name == "tiny":
