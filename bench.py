@@ -488,7 +488,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--other-configs", default="tiny,mixed,cow,cow2040,long_fp8",
+    ap.add_argument("--other-configs", default="tiny,mixed,cow,cow2040,cow2040_fp8,long_fp8",
                     help="comma list of workloads timed briefly (10 steps) after the main one "
                          "and reported under other_configs ('' for none; 1 GPU only)")
     ap.add_argument("--shared-prefix", type=int, default=1,
