@@ -92,3 +92,20 @@ def test_visit_order_is_longest_first_or_none():
     ctx = np.asarray(synth.mixed().ctx)
     order = workload.visit_order(ctx, device="cpu").numpy()
     assert np.all(np.diff(ctx[order]) <= 0)
+
+
+@pytest.mark.parametrize("name", ["tiny", "qwen_like", "mixed", "cow", "cow2040", "cow2040_fp8",
+                                  "cow_long_prompts", "long_fp8", "long_fp8_b16"])
+def test_every_bench_configuration_is_a_valid_workload(name):
+    """The named workloads bench.py runs: shapes the kernels take, a split
+    size that is a multiple of the block size, contexts within the pool, and
+    shared prompts of whole groups."""
+    w = bench.workload_for(name)
+    assert w.num_seqs >= 1 and all(c >= 1 for c in w.ctx)
+    assert w.head_dim in (128, 256) and w.block_size in (16, 32)
+    assert w.num_heads % w.num_kv_heads == 0 and w.num_heads // w.num_kv_heads <= 8
+    assert w.partition_size % w.block_size == 0
+    if w.prefix_len > 0:
+        assert w.num_seqs % w.group == 0
+        assert all(c > w.prefix_len for c in w.ctx)
+    assert bench.decode_bytes(w) > 0

@@ -7,7 +7,8 @@ of layer 0 of the Qwen-like batch (plus 4 sampled sequences of each other
 layer), all 256 mixed-length sequences, all 512 rollouts of both
 copy-on-write variants (through the plain split decode and through the
 shared-prefix decode), the 512 rollouts over an E4M3 cache (shared-prefix
-decode), and all 8 long FP8 sequences. The cache writes of
+decode), the 128 rollouts of 8184-token prompts (shared-prefix decode), and
+all 8 long FP8 sequences. The cache writes of
 layer 0 of the Qwen-like batch and of the FP8 batch are checked bit for bit
 over the whole pool, and the FP8 scales are recomputed on the host from the
 host rows. Host rows come from the seeded generator; nothing but the outputs
@@ -214,3 +215,27 @@ def test_cow_rollouts_over_fp8_cache(_lib):
     torch.cuda.synchronize()
     assert int(_lib.item()) == 0
     _check_all(sp[0].cpu(), w, 0, rows, "cow fp8 shared prefix", ks, vs)
+
+
+def test_long_prompt_rollouts(_lib):
+    """128 rollouts of 8 prompts of 8184 tokens (own parts of at most 129
+    tokens): the shared prefix spans several prefix partitions, read by the
+    full prefix CTA; every output against the oracle, through the replayed
+    shared-prefix step as the benchmark runs it."""
+    import bench
+    w = bench.workload_for("cow_long_prompts")
+    pw = workload.build(w)
+    groups = workload.prefix_groups(pw)
+    P = pkv.split_partition_size(groups.max_own_context, w.block_size, w.partition_size)
+    Pp = pkv.shared_prefix_partition_size(int(groups.group_start.shape[0]) - 1,
+                                          groups.max_group_members, w.num_kv_heads, w.num_heads,
+                                          w.block_size, groups.max_prefix_blocks, P)
+    assert -(-groups.max_prefix_blocks * w.block_size // Pp) > 1     # several prefix partitions
+    ws = pkv.shared_prefix_workspace(w.num_seqs, w.num_heads, w.head_dim, groups.max_own_context,
+                                     groups.max_prefix_blocks * w.block_size, P)
+    sp = [torch.empty_like(pw.layers[0].q)]
+    g = workload.capture_step(pw, sp, ws, P, groups=groups)
+    g.replay()
+    torch.cuda.synchronize()
+    assert int(_lib.item()) == 0
+    _check_all(sp[0].cpu(), w, 0, RowCache(w, 0).rows, "long-prompt rollouts")
